@@ -1,0 +1,156 @@
+/*
+ * pa.h -- C ABI of the paged-KV GQA attention library for one GB300 (sm_103a).
+ *
+ * The library computes grouped-query attention over a paged BF16 KV cache addressed
+ * through a block table, in two shapes -- q=1 decode and a causal prefill chunk over
+ * earlier paged context -- plus the slot-mapping computation and the KV write of new
+ * tokens.  Sources, cited by page and section:
+ *   page832 post   = luanjiahao.me feed, "784 -> 832 KV page for the DCU vendor paged
+ *                    attention" (sections 1, 4, 5, 6, 7);
+ *   input-prep post = jsqmd.com, "single-token decode input preparation on DCU" (3.2, 5).
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *     allocates, frees or keeps a tensor; a call only reads and writes what it is given.
+ *   - BF16 values are passed as raw 16-bit patterns (pa_bf16).
+ *   - Cache layout [page832 §4]: K and V are separate arrays, each
+ *     [num_pages, block_size, num_kv_heads, head_dim] in the last three dimensions,
+ *     with the distance between consecutive pages given by page_stride (in elements):
+ *     block_size * num_kv_heads * head_dim for a plain tensor, twice that for the
+ *     unbind(1) views of a [num_pages, 2, block_size, Hkv, D] tensor.
+ *   - Address translation [page832 §1]: token t of a sequence lives in page
+ *     block_table[t / block_size] at offset t % block_size.
+ *   - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns a status code.  Arguments are checked on the host before any
+ *     work is queued; a bad argument returns an error and queues nothing.  No call
+ *     throws, traps or asserts on the device.
+ *   - Device-side checks: a block-table entry outside [0, num_pages), a slot outside
+ *     the pool, a sequence length outside [1, max_seq_len] or a bounded wait that ran
+ *     out do not fault: the access is skipped (a tile read outside the pool reads
+ *     zeros) and a bit is set in the library's device error word, which
+ *     pa_get_device_errors() reads.
+ *   - Supported shapes: head_dim 256 and num_q_heads / num_kv_heads in 1..8 for the
+ *     attention calls (anything else returns PA_ERR_UNSUPPORTED: there is no fallback
+ *     path).  Pointers must be 16-byte aligned.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pa_bf16;
+
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad workspace */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but outside the shapes the kernels are built for */
+    PA_ERR_CUDA = 3,          /* the CUDA runtime or driver reported an error */
+};
+
+/* Bits of the device error word (pa_get_device_errors). */
+enum pa_device_error {
+    PA_DEVERR_PAGE = 1u,      /* block-table entry outside [0, num_pages) */
+    PA_DEVERR_SEQLEN = 2u,    /* sequence length outside [1, max_seq_len] */
+    PA_DEVERR_SLOT = 4u,      /* slot (or its page) outside the pool */
+    PA_DEVERR_TIMEOUT = 8u,   /* a bounded wait inside a kernel ran out */
+    PA_DEVERR_POSITION = 16u, /* a position past the block table's capacity */
+};
+
+/*
+ * pa_slot_mapping -- slot of each new token [input-prep §3.2]:
+ *     slot[i] = block_table[s, p / block_size] * block_size + p % block_size
+ * with p = positions[i] and s = seq_idx[i] (seq_idx may be NULL: every token belongs
+ * to sequence 0).  block_table is int32 [num_seqs, bt_stride] row-major, of which the
+ * first max_blocks entries of a row are valid.  slot_mapping is int64 [num_tokens].
+ * A negative position is a padding token and gets slot -1.  A position whose logical
+ * page is >= max_blocks, or whose block-table entry is negative, gets slot -1 and sets
+ * PA_DEVERR_POSITION.  num_tokens == 0 is a no-op.
+ */
+int pa_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
+                    const int32_t *block_table, int64_t bt_stride, int max_blocks,
+                    int num_tokens, int block_size, int64_t *slot_mapping, void *stream);
+
+/*
+ * pa_reshape_and_cache -- KV write of new tokens.  key and value are BF16
+ * [num_tokens, num_kv_heads, head_dim], contiguous; token i's rows are copied bit for
+ * bit to page slot_mapping[i] / block_size, offset slot_mapping[i] % block_size of
+ * k_cache and v_cache [page832 §4 layout].  A negative slot is skipped (padding); a
+ * slot whose page is >= num_pages is skipped and sets PA_DEVERR_SLOT.
+ * num_kv_heads * head_dim must be a multiple of 8.  num_tokens == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *k_cache,
+                         pa_bf16 *v_cache, int64_t page_stride, int64_t num_pages,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, void *stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for this
+ * problem size on the current device.  Returns 0 for invalid sizes.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                int head_dim, int block_size, int max_seq_len);
+
+/*
+ * pa_decode -- q=1 paged attention for a batch [page832 §5, §7]: for each sequence s
+ * and query head h,
+ *     out[s, h] = softmax_t( scale * q[s, h] . k_t ) . v_t,   t in [0, seq_lens[s])
+ * with k_t, v_t of KV head h / (Hq / Hkv) fetched through row s of block_table.
+ *   q, out       BF16 [num_seqs, num_q_heads, head_dim], contiguous
+ *   block_table  int32 [num_seqs, bt_stride]; entries past a sequence's last page unused
+ *   seq_lens     int32 [num_seqs], device; each in [1, max_seq_len]
+ *   workspace    device scratch of >= pa_decode_workspace_size(...) bytes, 256-byte
+ *                aligned; its contents on entry do not matter.
+ * Optional fused write of each sequence's newest token (config of a serving step):
+ * when new_k, new_v and new_slots are all non-NULL, new_k / new_v ([num_seqs, Hkv, D])
+ * are first written at new_slots (int64 [num_seqs]) exactly as pa_reshape_and_cache
+ * does, and the attention then includes them.  Pass all three NULL to skip.
+ * The split-context kernel processes page-local tiles of 16 tokens, so any block_size
+ * works (784 leaves a 16-token tail tile per page, 832 does not).
+ */
+int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+              int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+              int64_t bt_stride, const int32_t *seq_lens, int num_seqs, int max_seq_len,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+              pa_bf16 *out, void *workspace, size_t workspace_bytes,
+              const pa_bf16 *new_k, const pa_bf16 *new_v, const int64_t *new_slots,
+              void *stream);
+
+/*
+ * pa_prefill_chunk -- attention of a chunk of q_len query rows of ONE sequence over
+ * that sequence's paged cache [page832 §6].  Row i sits at absolute position
+ * q_start + i; with causal != 0 it sees keys 0..q_start+i (diagonal included),
+ * otherwise all q_start + q_len keys.  The chunk's own K/V must already be in the cache
+ * (pa_slot_mapping + pa_reshape_and_cache first).
+ *   q, out       BF16 [q_len, num_q_heads, head_dim], contiguous
+ *   block_table  int32, the sequence's row: ceil((q_start + q_len) / block_size) entries
+ * Shapes accepted: 1 <= q_len, 0 <= q_start, q_start + q_len <= 2^31 - 1.
+ */
+int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                     int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                     int q_len, int q_start, int causal, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, float scale, pa_bf16 *out, void *stream);
+
+/*
+ * pa_get_device_errors -- waits for `stream`, then returns in *bits the device error
+ * word of the current device (PA_DEVERR_* bits set by any call since the last clear)
+ * and, if clear != 0, resets it to zero.
+ */
+int pa_get_device_errors(unsigned int *bits, int clear, void *stream);
+
+/* Human-readable name of a pa_status value (static storage). */
+const char *pa_status_string(int status);
+
+/* Build identity: target architecture, kernel tile sizes and compiler version. */
+const char *pa_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

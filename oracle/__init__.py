@@ -102,7 +102,7 @@ def slot_mapping(positions, block_table, block_size, seq_idx=None) -> np.ndarray
     rc = lib.pa_oracle_slot_mapping(_ptr(pos), _ptr(sidx), _ptr(bt), bt.shape[1], pos.shape[0],
                                     block_size, _ptr(out))
     if rc != 0:
-        raise ValueError("oracle slot_mapping: negative position")
+        raise ValueError("oracle slot_mapping failed")
     return out
 
 

@@ -25,7 +25,8 @@
  * Readings where the pages are silent (each is listed in the design notes):
  *   - query head h reads KV head h / (Hq / Hkv)  (consecutive grouping);
  *   - a prefill query at absolute position p sees keys 0..p inclusive;
- *   - a slot < 0 marks a padding token and is not written;
+ *   - a negative position is a padding token with slot -1, and a slot < 0 is not
+ *     written;
  *   - the caches are two separate arrays with a common page stride in elements,
  *     which covers both a plain [pages, BS, Hkv, D] tensor and the unbind(1) views.
  *
@@ -70,14 +71,15 @@ int pa_oracle_threads(void) {
 }
 
 /* Slot mapping [input-prep §3.2].  seq_idx may be NULL (every token in sequence 0).
- * Returns 0, or -1 if a position is negative. */
+ * A negative position marks a padding token: its slot is -1 (a reading; the pages do
+ * not say).  Returns 0. */
 int pa_oracle_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
                            const int32_t *block_table, int64_t bt_stride, int num_tokens,
                            int block_size, int64_t *slot_mapping) {
     for (int i = 0; i < num_tokens; ++i) {
         int64_t pos = positions[i];
         int64_t s = seq_idx ? seq_idx[i] : 0;
-        if (pos < 0) return -1;
+        if (pos < 0) { slot_mapping[i] = -1; continue; }
         int64_t logical_block = pos / block_size;
         int64_t block_number = block_table[s * bt_stride + logical_block];
         int64_t block_offset = pos % block_size;

@@ -319,3 +319,9 @@ def test_oracle_reports_unmapped_pages():
     bt[1] = 99
     with pytest.raises(ValueError):
         oracle.attend_row(_bf16(rng.standard_normal(8)), k_cache, v_cache, bt, 8, 0, 20, 0.5)
+
+
+def test_slot_mapping_padding_position():
+    bt = np.array([3, 1], dtype=np.int32)
+    got = oracle.slot_mapping(np.array([-1, 5, -7], dtype=np.int32), bt, 4)
+    assert [int(x) for x in got] == [-1, 3 * 4 + 1, -1]
