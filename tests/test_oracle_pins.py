@@ -324,4 +324,4 @@ def test_oracle_reports_unmapped_pages():
 def test_slot_mapping_padding_position():
     bt = np.array([3, 1], dtype=np.int32)
     got = oracle.slot_mapping(np.array([-1, 5, -7], dtype=np.int32), bt, 4)
-    assert [int(x) for x in got] == [-1, 3 * 4 + 1, -1]
+    assert [int(x) for x in got] == [-1, 1 * 4 + 1, -1]   # 5//4 = 1 -> page 1, offset 1
