@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV GQA attention hot path on GB300.
+
+Metric: paged decode KV GB/s (and % of HBM peak) at 4K-32K context; q=4096 prefill
+TFLOP/s.  One JSON line on stdout (rank 0).
+
+Headline workload (the `value`): decode, batch 1, context 8192 (the new token at
+position 8191 included), 24 query / 4 KV heads, head_dim 256, BF16 N(0,1), block_size
+832, over a shuffled 64-page pool.  One step = one serving-style pass of the hot path:
+slot mapping of the new token -> its fused KV write -> split-context decode -> LSE
+combine, replayed from a CUDA graph.  KV GB/s = 4096 bytes per context token / step
+time (K+V of 4 KV heads x 256 dims x 2 bytes).
+
+Other legs, each timed the same way and reported under "legs": the 4K/8K/16K/32K sweep
+(1 GiB pool, 5% of K rows x8), block_size 784 at 8K, batched decode (16 sequences,
+4K-32K, fused write), and the q=4096 prefill chunk over 4096 prior tokens (chunk KV
+write + prefill; TFLOP/s counts the causal work 4*D*Hq*sum_i(4096+i+1) = 6.185e11).
+
+Timing: CUDA events on the launching stream around each step; between steps a 256 MiB
+buffer is written to flush L2 (outside the events).  W warm-up steps first.
+--impl reference times the fp64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HEADLINE = ("decode batch 1, context 8192 (new token at 8191 written by slot mapping), "
+            "24 q / 4 kv heads, d=256, BF16 N(0,1), block_size 832, shuffled 64-page pool")
+KV_BYTES_PER_TOKEN = 2 * workloads.HKV * workloads.HEAD_DIM * 2   # K+V, all KV heads
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--legs", default="all", help="comma list: sweep,bs784,batched,prefill or all/none")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+# ------------------------------------------------------------------------ distributed
+def dist_init(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the GPU legs run."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.proc = None
+        self.path = None
+        self.index = index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.f = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(busy),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ------------------------------------------------------------------------ timing
+def time_steps(step, steps, warmup, flush):
+    """Per-step device time (ms) of `step` with an L2 flush before each step."""
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def time_main_kernel(pa, call, steps, warmup, flush):
+    """Per-launch device time (ms) of the main kernel of `call` (decode split kernel or
+    prefill kernel), recorded by the library around that launch on its stream."""
+    for _ in range(warmup):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        pa.set_kernel_events(a, b)
+        call()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def graph_of(fn):
+    """Capture fn (a sequence of C-ABI calls on the current stream) as a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+# ------------------------------------------------------------------------ legs
+def decode_step_fn(pa, case, fused, max_seq_len=None):
+    """One decode step: slot mapping + fused write of the new token (if any) + decode."""
+    msl = int(case.seq_lens.max()) if max_seq_len is None else max_seq_len
+    S, hq, d = case.q.shape
+    out = torch.empty_like(case.q)
+    ws = torch.empty(max(256, pa.decode_workspace_size(S, hq, case.k_cache.shape[2], d,
+                                                        case.block_size, msl)),
+                     dtype=torch.uint8, device="cuda")
+    slots = torch.empty(S, dtype=torch.int64, device="cuda")
+
+    def attn_only():
+        pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                  case.scale, msl, out=out, workspace=ws)
+
+    def step():
+        if fused:
+            pa.slot_mapping(case.positions, case.block_table, case.block_size,
+                            seq_idx=case.seq_idx, out=slots)
+            pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                      case.scale, msl, out=out, workspace=ws, new_k=case.new_k,
+                      new_v=case.new_v, new_slots=slots)
+        else:
+            attn_only()
+    return step, attn_only, out
+
+
+def decode_leg(pa, case, steps, warmup, flush, peaks, fused):
+    step, attn_only, _ = decode_step_fn(pa, case, fused)
+    g = graph_of(step)
+    ms = time_steps(g.replay, steps, warmup, flush)
+    kms = time_main_kernel(pa, attn_only, steps, warmup, flush)
+    tokens = int(case.seq_lens.sum())
+    nbytes = tokens * KV_BYTES_PER_TOKEN
+    step_ms = statistics.mean(ms)
+    k_ms = statistics.mean(kms)
+    r = {"context_tokens": tokens, "kv_bytes": nbytes, "ms_per_step": step_ms,
+         "ms_per_step_min": min(ms), "kv_gbs": nbytes / (step_ms * 1e-3) / 1e9,
+         "split_kernel_ms": k_ms, "split_kernel_gbs": nbytes / (k_ms * 1e-3) / 1e9,
+         "tokens_per_s": case.q.shape[0] / (step_ms * 1e-3)}
+    r["kv_pct_of_hbm_peak"] = 100.0 * r["kv_gbs"] / peaks["hbm_gbs"]
+    r["split_kernel_pct_of_hbm_peak"] = 100.0 * r["split_kernel_gbs"] / peaks["hbm_gbs"]
+    return r, ms, kms
+
+
+PREFILL_FLOPS = 4.0 * workloads.HEAD_DIM * workloads.HQ * sum(4096 + i + 1 for i in range(4096))
+
+
+def prefill_leg(pa, steps, warmup, flush, peaks):
+    case = workloads.prefill_chunk("cuda")
+    out = torch.empty_like(case.q)
+    slots = torch.empty(case.positions.numel(), dtype=torch.int64, device="cuda")
+    bt0 = case.block_table[0].contiguous()
+
+    def attn():
+        pa.prefill_chunk(case.q, case.k_cache, case.v_cache, bt0, case.q_start, True,
+                         case.scale, out=out)
+
+    def step():
+        pa.slot_mapping(case.positions, case.block_table, case.block_size, out=slots)
+        pa.reshape_and_cache(case.new_k, case.new_v, case.k_cache, case.v_cache, slots)
+        attn()
+    g = graph_of(step)
+    ms = time_steps(g.replay, steps, warmup, flush)
+    kms = time_main_kernel(pa, attn, steps, warmup, flush)
+    step_ms, k_ms = statistics.mean(ms), statistics.mean(kms)
+    r = {"q_len": 4096, "q_start": 4096, "causal_flops": PREFILL_FLOPS,
+         "ms_per_step": step_ms, "step_tflops": PREFILL_FLOPS / (step_ms * 1e-3) / 1e12,
+         "kernel_ms": k_ms, "kernel_ms_min": min(kms),
+         "kernel_tflops": PREFILL_FLOPS / (k_ms * 1e-3) / 1e12}
+    peak = peaks["bf16_tflops"]
+    r["roofline"] = {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
+                     "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak, "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 dense burst"}
+    return r
+
+
+def e2e_leg(pa, case, steps, warmup, flush):
+    """The headline step through the public API with pinned host buffers: H2D of the
+    step's inputs (q, the new token's K/V, its position, the block table and seq_lens),
+    slot mapping + fused write + decode, D2H of the output."""
+    S, hq, d = case.q.shape
+    msl = int(case.seq_lens.max())
+    host = {k: getattr(case, k).cpu().pin_memory()
+            for k in ("q", "new_k", "new_v", "positions", "seq_idx", "block_table", "seq_lens")}
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    out_h = torch.empty((S, hq, d), dtype=torch.bfloat16).pin_memory()
+    out_d = torch.empty((S, hq, d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(256, pa.decode_workspace_size(S, hq, case.k_cache.shape[2], d,
+                                                        case.block_size, msl)),
+                     dtype=torch.uint8, device="cuda")
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        slots = pa.slot_mapping(dev["positions"], dev["block_table"], case.block_size,
+                                seq_idx=dev["seq_idx"])
+        pa.decode(dev["q"], case.k_cache, case.v_cache, dev["block_table"], dev["seq_lens"],
+                  case.scale, msl, out=out_d, workspace=ws, new_k=dev["new_k"],
+                  new_v=dev["new_v"], new_slots=slots)
+        out_h.copy_(out_d, non_blocking=True)
+    ms = time_steps(step, steps, warmup, flush)
+    return statistics.mean(ms), h2d, d2h
+
+
+# ------------------------------------------------------------------------ CPU oracle
+def oracle_step_fn(case_host):
+    import oracle
+    c = case_host
+
+    def step():
+        slots = oracle.slot_mapping(c["positions"], c["block_table"], c["block_size"],
+                                    c["seq_idx"])
+        oracle.reshape_and_cache(c["new_k"], c["new_v"], c["k"], c["v"], slots, c["block_size"])
+        oracle.decode(c["q"], c["k"], c["v"], c["block_table"], c["seq_lens"], c["scale"])
+    return step
+
+
+def host_case(case):
+    from workloads import bits
+    return dict(q=bits(case.q), k=bits(case.k_cache), v=bits(case.v_cache),
+                new_k=bits(case.new_k), new_v=bits(case.new_v),
+                positions=case.positions.cpu().numpy(), seq_idx=case.seq_idx.cpu().numpy(),
+                block_table=case.block_table.cpu().numpy(),
+                seq_lens=case.seq_lens.cpu().numpy(), block_size=case.block_size,
+                scale=case.scale)
+
+
+def cpu_oracle_timing(case_h, seconds, max_steps=None):
+    import oracle
+    step = oracle_step_fn(case_h)
+    step()  # builds / loads the oracle library, first touch of the pages
+    n, t0 = 0, time.perf_counter()
+    while True:
+        step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_steps and n >= max_steps):
+            break
+    return el / n, n, oracle.max_threads()
+
+
+def headline_case(device):
+    """The headline workload with the new token of position 8191 supplied for writing."""
+    return workloads.paged_case(1002, [8192], 832, 64, new_tokens=1, device=device)
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    torch.manual_seed(0)
+    case = headline_case("cpu")
+    ch = host_case(case)
+    per_step, n, threads = cpu_oracle_timing(ch, seconds=max(1.0, args.cpu_seconds),
+                                             max_steps=args.steps + args.warmup)
+    nbytes = 8192 * KV_BYTES_PER_TOKEN
+    v = nbytes / per_step / 1e9
+    line = {"impl": "reference", "metric": "paged decode KV GB/s (batch 1, ctx 8192, bs 832)",
+            "value": v, "unit": "GB/s", "n_gpus": args.gpus, "steps": n, "warmup": 1,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "block_size": 832, "context": 8192},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n} full decode steps (slot mapping + KV write + "
+                                       f"fp64 attention of 24 heads over 8192 keys)"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ main
+def main():
+    args = parse()
+    rank, ws = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+        return
+    import paged_kv_cache_09_gb300 as pa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    pa.load()
+    peaks = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+
+    # ---- headline: timed K steps, barrier + synchronize on both sides
+    case = headline_case("cuda")
+    step, attn_only, _ = decode_step_fn(pa, case, fused=True)
+    g = graph_of(step)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ms = time_steps(g.replay, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = max_over_ranks(sum(ms), ws)
+    nbytes_rank = 8192 * KV_BYTES_PER_TOKEN * args.steps
+    value = sum_over_ranks(nbytes_rank, ws) / (total_ms * 1e-3) / 1e9
+    kms = time_main_kernel(pa, attn_only, args.steps, args.warmup, flush)
+    k_ms = statistics.mean(kms)
+    kernel_gbs = 8192 * KV_BYTES_PER_TOKEN / (k_ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = e2e_leg(pa, case, args.steps, args.warmup, flush)
+    e2e_val = 8192 * KV_BYTES_PER_TOKEN / (e2e_ms * 1e-3) / 1e9
+    assert pa.device_errors() == 0, "device error word set during the headline leg"
+    del case, g
+
+    legs = {}
+    want = set() if args.legs == "none" else (
+        {"sweep", "bs784", "batched", "prefill"} if args.legs == "all" else set(args.legs.split(",")))
+    if rank == 0 and "sweep" in want:
+        sweep = {}
+        for ctx in (4096, 8192, 16384, 32768):
+            c = workloads.decode_sweep(ctx, "cuda")
+            r, _, _ = decode_leg(pa, c, args.steps, args.warmup, flush, peaks, fused=False)
+            sweep[str(ctx)] = r
+            del c
+            torch.cuda.empty_cache()
+        legs["decode_sweep_1gib_pool_peaked"] = sweep
+    if rank == 0 and "bs784" in want:
+        c = workloads.decode_8k(784, "cuda")
+        legs["decode_8k_bs784"], _, _ = decode_leg(pa, c, args.steps, args.warmup, flush, peaks,
+                                                   fused=False)
+        del c
+    if rank == 0 and "batched" in want:
+        c = workloads.batched_decode("cuda")
+        legs["batched_decode_16_fused_write"], _, _ = decode_leg(
+            pa, c, max(5, args.steps // 2), args.warmup, flush, peaks, fused=True)
+        del c
+        torch.cuda.empty_cache()
+    if rank == 0 and "prefill" in want:
+        legs["prefill_q4096_over_4096"] = prefill_leg(pa, max(5, args.steps // 4), args.warmup,
+                                                      flush, peaks)
+    assert pa.device_errors() == 0, "device error word set during the legs"
+    clk = clocks.stop() if clocks else None
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        c = headline_case("cpu")
+        per_step, n, threads = cpu_oracle_timing(host_case(c), seconds=args.cpu_seconds)
+        cv = 8192 * KV_BYTES_PER_TOKEN / per_step / 1e9
+        cpu = {"value": cv, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} full decode steps of the headline workload (slot mapping + KV "
+                         f"write + fp64 attention, 24 heads x 8192 keys), {per_step*1e3:.1f} ms each"}
+
+    if rank != 0:
+        return
+    step_ms = statistics.mean(ms)
+    line = {
+        "metric": "paged decode KV GB/s (% of HBM peak) at 4K-32K ctx; q=4096 prefill TFLOP/s",
+        "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": HEADLINE, "block_size": 832, "context": 8192,
+                   "step": "CUDA-graph replay of slot mapping + fused KV write + split decode "
+                           "+ LSE combine",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the "
+                         f"step events)",
+                   "kv_pct_of_hbm_peak": 100.0 * value / ws / peaks["hbm_gbs"],
+                   "parallelism": f"replica per GPU x{ws}"},
+        "clocks": clk,
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": kernel_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "decode_split_kernel",
+                     "algorithmic_bytes_per_launch": 8192 * KV_BYTES_PER_TOKEN,
+                     "kernel_ms": k_ms, "peak_source": f"{peaks['source']} hbm_gbs"},
+        "cpu_baseline": cpu,
+        "legs": legs,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -68,13 +68,15 @@ enum pa_device_error {
  * with p = positions[i] and s = seq_idx[i] (seq_idx may be NULL: every token belongs
  * to sequence 0).  block_table is int32 [num_seqs, bt_stride] row-major, of which the
  * first max_blocks entries of a row are valid.  slot_mapping is int64 [num_tokens].
- * A negative position is a padding token and gets slot -1.  A position whose logical
- * page is >= max_blocks, or whose block-table entry is negative, gets slot -1 and sets
- * PA_DEVERR_POSITION.  num_tokens == 0 is a no-op.
+ * A negative position is a padding token and gets slot -1.  A token whose sequence is
+ * outside [0, num_seqs), whose logical page is >= max_blocks, or whose block-table
+ * entry is negative gets slot -1 and sets PA_DEVERR_POSITION.  num_tokens == 0 is a
+ * no-op.
  */
 int pa_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
-                    const int32_t *block_table, int64_t bt_stride, int max_blocks,
-                    int num_tokens, int block_size, int64_t *slot_mapping, void *stream);
+                    const int32_t *block_table, int num_seqs, int64_t bt_stride,
+                    int max_blocks, int num_tokens, int block_size, int64_t *slot_mapping,
+                    void *stream);
 
 /*
  * pa_reshape_and_cache -- KV write of new tokens.  key and value are BF16
@@ -142,6 +144,16 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
  * and, if clear != 0, resets it to zero.
  */
 int pa_get_device_errors(unsigned int *bits, int clear, void *stream);
+
+/*
+ * pa_set_kernel_events -- measurement hook.  The next pa_decode or pa_prefill_chunk
+ * call made by this host thread records `start` on its stream immediately before it
+ * launches its main kernel (the split-context decode kernel, or the prefill kernel)
+ * and `stop` immediately after that launch, then forgets both.  The arguments are
+ * cudaEvent_t handles owned by the caller; passing NULL, NULL cancels a pending hook.
+ * Both or neither must be NULL.
+ */
+int pa_set_kernel_events(void *start, void *stop);
 
 /* Human-readable name of a pa_status value (static storage). */
 const char *pa_status_string(int status);

@@ -1,0 +1,219 @@
+"""Python binding of libpa.so: paged-KV GQA attention for one GB300 (sm_103a).
+
+This module only marshals arguments: it takes torch CUDA tensors, checks their dtype,
+device and layout, and passes raw pointers, sizes and the current CUDA stream to the
+C ABI declared in include/pa.h.  Every step of the computation runs in the library's
+CUDA kernels.  There is no CPU or PyTorch fallback: if libpa.so is missing or cannot be
+loaded, every call raises.
+
+Functions (names follow the C ABI):
+    slot_mapping(positions, block_table, block_size, seq_idx=None)    -> int64 slots
+    reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)     (in place)
+    decode_workspace_size(...), decode(q, k_cache, v_cache, block_table, seq_lens, ...)
+    prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale)
+    device_errors(clear=True)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = ["load", "build", "slot_mapping", "reshape_and_cache", "decode_workspace_size",
+           "decode", "prefill_chunk", "device_errors", "set_kernel_events", "build_info", "PAError",
+           "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION",
+           "LIB_PATH"]
+
+LIB_PATH = _build.LIB
+DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_POSITION = 1, 2, 4, 8, 16
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = _lib.pa_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {name}")
+
+
+def build(force: bool = False) -> str:
+    """Compile libpa.so (nvcc, sm_103a) in-tree."""
+    return _build.build(force=force)
+
+
+def load():
+    """Load libpa.so and declare the C signatures.  Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpa.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        sig = {
+            "pa_slot_mapping": ([P, P, P, i32, i64, i32, i32, i32, P, P], i32),
+            "pa_reshape_and_cache": ([P, P, P, P, i64, i64, P, i32, i32, i32, i32, P], i32),
+            "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+            "pa_decode": ([P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32, P, P,
+                           sz, P, P, P, P], i32),
+            "pa_prefill_chunk": ([P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                  P, P], i32),
+            "pa_get_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32, P], i32),
+            "pa_set_kernel_events": ([P, P], i32),
+            "pa_status_string": ([i32], ctypes.c_char_p),
+            "pa_build_info": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _check_cache(k_cache, v_cache):
+    for n, c in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(c, n, torch.bfloat16, 4)
+        if c.stride(3) != 1 or c.stride(2) != c.shape[3] or c.stride(1) != c.shape[2] * c.shape[3]:
+            raise ValueError(f"{n}: each page must be a contiguous [BS, Hkv, D] block")
+    if k_cache.shape != v_cache.shape or k_cache.stride(0) != v_cache.stride(0):
+        raise ValueError("k_cache and v_cache must have the same shape and page stride")
+    return k_cache.stride(0)
+
+
+def _raise(rc, where):
+    if rc != 0:
+        raise PAError(rc, where)
+
+
+def build_info() -> str:
+    return load().pa_build_info().decode()
+
+
+def slot_mapping(positions, block_table, block_size, seq_idx=None, max_blocks=None, out=None):
+    """int64 slot of each position (see pa_slot_mapping)."""
+    lib = load()
+    _check(positions, "positions", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32)
+    bt = block_table if block_table.dim() == 2 else block_table.view(1, -1)
+    if bt.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    if seq_idx is not None:
+        _check(seq_idx, "seq_idx", torch.int32, 1)
+    n = positions.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.int64, device=positions.device)
+    mb = bt.shape[1] if max_blocks is None else int(max_blocks)
+    _raise(lib.pa_slot_mapping(_ptr(positions.contiguous()), _ptr(seq_idx), _ptr(bt),
+                               bt.shape[0], bt.stride(0), mb, n, int(block_size), _ptr(out),
+                               _stream()), "pa_slot_mapping")
+    return out
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping_):
+    """Write key/value [T, Hkv, D] into the caches at slot_mapping_ (in place)."""
+    lib = load()
+    _check(key, "key", torch.bfloat16, 3)
+    _check(value, "value", torch.bfloat16, 3)
+    _check(slot_mapping_, "slot_mapping", torch.int64, 1)
+    ps = _check_cache(k_cache, v_cache)
+    key, value = key.contiguous(), value.contiguous()
+    T, hkv, d = key.shape
+    _raise(lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), ps,
+                                    k_cache.shape[0], _ptr(slot_mapping_), T, hkv, d,
+                                    k_cache.shape[1], _stream()), "pa_reshape_and_cache")
+
+
+def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                          max_seq_len) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               block_size, max_seq_len))
+
+
+def decode(q, k_cache, v_cache, block_table, seq_lens, scale, max_seq_len, out=None,
+           workspace=None, new_k=None, new_v=None, new_slots=None):
+    """q=1 paged decode (see pa_decode).  Returns out [S, Hq, D] BF16."""
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    ps = _check_cache(k_cache, v_cache)
+    q = q.contiguous()
+    S, hq, d = q.shape
+    _, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_size(S, hq, hkv, d, bs, max_seq_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if new_k is not None:
+        new_k, new_v = new_k.contiguous(), new_v.contiguous()
+    _raise(lib.pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
+                         _ptr(block_table), block_table.stride(0), _ptr(seq_lens), S,
+                         int(max_seq_len), hq, hkv, d, bs, float(scale), _ptr(out),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _ptr(new_k), _ptr(new_v), _ptr(new_slots), _stream()), "pa_decode")
+    return out
+
+
+def prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale, out=None):
+    """Causal (or full) chunk attention of one sequence (see pa_prefill_chunk)."""
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(block_table, "block_table", torch.int32)
+    ps = _check_cache(k_cache, v_cache)
+    q = q.contiguous()
+    bt = block_table.reshape(-1).contiguous()
+    q_len, hq, d = q.shape
+    _, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _raise(lib.pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
+                                _ptr(bt), q_len, int(q_start), int(bool(causal)), hq, hkv, d,
+                                bs, float(scale), _ptr(out), _stream()), "pa_prefill_chunk")
+    return out
+
+
+def set_kernel_events(start, stop):
+    """Measurement hook: the next decode / prefill_chunk call records these
+    torch.cuda.Event objects around its main kernel (see pa_set_kernel_events)."""
+    lib = load()
+    for e in (start, stop):
+        if not e.cuda_event:          # torch creates the CUDA event on first record
+            e.record()
+    _raise(lib.pa_set_kernel_events(ctypes.c_void_p(start.cuda_event),
+                                    ctypes.c_void_p(stop.cuda_event)), "pa_set_kernel_events")
+
+
+def device_errors(clear: bool = True) -> int:
+    """Waits for the current stream and returns (and by default clears) the error bits."""
+    lib = load()
+    v = ctypes.c_uint(0)
+    _raise(lib.pa_get_device_errors(ctypes.byref(v), int(clear), _stream()),
+           "pa_get_device_errors")
+    return int(v.value)

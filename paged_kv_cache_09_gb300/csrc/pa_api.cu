@@ -1,0 +1,402 @@
+// pa_api.cu -- the C ABI declared in include/pa.h: host-side argument checks, TMA
+// descriptor construction, the device error word and kernel dispatch.  No call
+// allocates device memory; every call is asynchronous on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pa.h"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace {
+
+// The library's device error word (one per device that loads the library).
+__device__ unsigned int g_pa_device_errors;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned *err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, looked up once with the device current.
+int device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0;
+        void *ptr = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (cudaGetSymbolAddress(&ptr, g_pa_device_errors) != cudaSuccess) return PA_ERR_CUDA;
+        d.num_sms = sms;
+        d.err = static_cast<unsigned *>(ptr);
+        d.ready = true;
+    }
+    *out = d;
+    return PA_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the library
+// does not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// K or V cache as a 4-D tensor {D, Hkv, rows, pages}; boxes of 64 dims x 1 head x
+// box_rows tokens x 1 page, 128-byte swizzle.  rows < block_size cuts the page short
+// (used for the last page of a sequence).
+bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_heads,
+                    int rows, int64_t num_pages, int64_t page_stride, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)rows,
+                          (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_kv_heads * head_dim * 2,
+                             (cuuint64_t)page_stride * 2};
+    cuuint32_t box[4] = {(cuuint32_t)pa::kChunkElems, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Query rows [q_len, Hq, D] as {D, Hq, q_len}; boxes of 64 dims x 1 head x box_rows.
+bool make_rows_map(CUtensorMap *m, const void *base, int head_dim, int num_heads, int rows,
+                   int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
+    cuuint32_t box[3] = {(cuuint32_t)pa::kChunkElems, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A small per-thread cache of decode descriptors: encoding costs host time and the
+// same cache pointers come back call after call.
+struct MapKey {
+    const void *base;
+    int head_dim, num_kv_heads, rows, box_rows;
+    int64_t num_pages, page_stride;
+    bool operator==(const MapKey &o) const {
+        return base == o.base && head_dim == o.head_dim && num_kv_heads == o.num_kv_heads &&
+               rows == o.rows && box_rows == o.box_rows && num_pages == o.num_pages &&
+               page_stride == o.page_stride;
+    }
+};
+
+bool cached_cache_map(CUtensorMap *m, const MapKey &k) {
+    struct Entry {
+        MapKey key;
+        CUtensorMap map;
+        bool used;
+    };
+    thread_local Entry entries[8] = {};
+    thread_local int next = 0;
+    for (auto &e : entries)
+        if (e.used && e.key == k) {
+            *m = e.map;
+            return true;
+        }
+    if (!make_cache_map(m, k.base, k.head_dim, k.num_kv_heads, k.rows, k.num_pages,
+                        k.page_stride, k.box_rows))
+        return false;
+    entries[next] = Entry{k, *m, true};
+    next = (next + 1) % 8;
+    return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pending measurement events of this host thread (pa_set_kernel_events).
+thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
+
+void take_kernel_events(cudaEvent_t *start, cudaEvent_t *stop) {
+    *start = t_ev_start;
+    *stop = t_ev_stop;
+    t_ev_start = t_ev_stop = nullptr;
+}
+
+bool diag_enabled() {
+    static int on = -1;
+    if (on < 0) {
+        const char *v = getenv("PA_DIAG");
+        on = (v && v[0] && v[0] != '0') ? 1 : 0;
+    }
+    return on == 1;
+}
+
+// Checks shared by the two attention calls.
+int check_attention_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int64_t num_pages, int64_t page_stride) {
+    if (num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 ||
+        num_pages < 1)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (num_q_heads > 65535 || num_kv_heads > 65535) return PA_ERR_INVALID_ARG;
+    if (page_stride < (int64_t)block_size * num_kv_heads * head_dim) return PA_ERR_INVALID_ARG;
+    if ((page_stride * 2) % 16) return PA_ERR_INVALID_ARG;
+    if (num_pages > 0x7fffffffLL) return PA_ERR_INVALID_ARG;
+    if (head_dim != pa::kHeadDim) return PA_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > pa::kDecMaxGroup) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+const char *pa_build_info(void) {
+    static char buf[256];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        snprintf(buf, sizeof buf,
+                 "paged_kv_cache_09_gb300: sm_103a; decode tile %d x %d stages, %d consumer "
+                 "warps; prefill %dx%d mma tiles; nvcc %d.%d",
+                 pa::kDecTile, pa::kDecStages, pa::kDecConsumers, pa::kPfQRows, pa::kPfKvTile,
+                 __CUDACC_VER_MAJOR__, __CUDACC_VER_MINOR__);
+    });
+    return buf;
+}
+
+int pa_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
+                    const int32_t *block_table, int num_seqs, int64_t bt_stride,
+                    int max_blocks, int num_tokens, int block_size, int64_t *slot_mapping,
+                    void *stream) {
+    if (num_tokens < 0 || block_size < 1 || max_blocks < 1 || bt_stride < max_blocks ||
+        num_seqs < 1)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!positions || !block_table || !slot_mapping) return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    cudaError_t e = pa::launch_slot_mapping(positions, seq_idx, block_table, num_seqs,
+                                            bt_stride, max_blocks, num_tokens, block_size,
+                                            slot_mapping,
+                                            dev.err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *k_cache,
+                         pa_bf16 *v_cache, int64_t page_stride, int64_t num_pages,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, void *stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_pages < 1)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (row % 8 || row > 0x7fffffffLL) return PA_ERR_INVALID_ARG;
+    if (page_stride < row * block_size || (page_stride * 2) % 16) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    cudaError_t e = pa::launch_reshape_and_cache(key, value, k_cache, v_cache, page_stride,
+                                                 num_pages, slot_mapping, num_tokens, (int)row,
+                                                 block_size, dev.err,
+                                                 static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_seq_len) {
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != pa::kHeadDim ||
+        block_size < 1 || max_seq_len < 1 || num_q_heads % num_kv_heads)
+        return 0;
+    DeviceInfo dev;
+    if (device_info(&dev)) return 0;
+    const pa::DecodePlan plan =
+        pa::plan_decode(num_seqs, num_kv_heads, block_size, max_seq_len, dev.num_sms);
+    return pa::decode_workspace_bytes(num_seqs, num_q_heads, plan);
+}
+
+int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+              int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+              int64_t bt_stride, const int32_t *seq_lens, int num_seqs, int max_seq_len,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+              pa_bf16 *out, void *workspace, size_t workspace_bytes, const pa_bf16 *new_k,
+              const pa_bf16 *new_v, const int64_t *new_slots, void *stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs < 1 || num_seqs > 65535 || max_seq_len < 1) return PA_ERR_INVALID_ARG;
+    if (int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
+                                       num_pages, page_stride))
+        return rc;
+    const int64_t max_blocks = ((int64_t)max_seq_len + block_size - 1) / block_size;
+    if (bt_stride < max_blocks) return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_INVALID_ARG;
+    const int nfused = (new_k != nullptr) + (new_v != nullptr) + (new_slots != nullptr);
+    if (nfused != 0 && nfused != 3) return PA_ERR_INVALID_ARG;
+    if (nfused == 3 && (!aligned16(new_k) || !aligned16(new_v))) return PA_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    const pa::DecodePlan plan =
+        pa::plan_decode(num_seqs, num_kv_heads, block_size, max_seq_len, dev.num_sms);
+    if (workspace_bytes < pa::decode_workspace_bytes(num_seqs, num_q_heads, plan))
+        return PA_ERR_INVALID_ARG;
+
+    CUtensorMap tk, tv;
+    if (!cached_cache_map(&tk, MapKey{k_cache, head_dim, num_kv_heads, block_size, pa::kDecTile,
+                                      num_pages, page_stride}) ||
+        !cached_cache_map(&tv, MapKey{v_cache, head_dim, num_kv_heads, block_size, pa::kDecTile,
+                                      num_pages, page_stride}))
+        return PA_ERR_CUDA;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (nfused == 3) {
+        cudaError_t e = pa::launch_reshape_and_cache(
+            new_k, new_v, const_cast<pa_bf16 *>(k_cache), const_cast<pa_bf16 *>(v_cache),
+            page_stride, num_pages, new_slots, num_seqs, num_kv_heads * head_dim, block_size,
+            dev.err, st);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    pa::DecodeArgs a;
+    a.q = q;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.max_seq_len = max_seq_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_q_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.out = out;
+    a.workspace = workspace;
+    a.err = dev.err;
+    take_kernel_events(&a.ev_start, &a.ev_stop);
+    if (diag_enabled())
+        fprintf(stderr, "[pa] decode: seqs=%d max_seq_len=%d bs=%d splits=%d tiles/split=%d\n",
+                num_seqs, max_seq_len, block_size, plan.num_splits, plan.tiles_per_split);
+    return pa::launch_decode(tk, tv, a, plan, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                     int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                     int q_len, int q_start, int causal, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, float scale, pa_bf16 *out, void *stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !out) return PA_ERR_INVALID_ARG;
+    if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > 0x7fffffffLL)
+        return PA_ERR_INVALID_ARG;
+    if (int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
+                                       num_pages, page_stride))
+        return rc;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    const int num_q_tiles = (q_len + pa::kPfQRows - 1) / pa::kPfQRows;
+    if (num_q_tiles > 0x7fffffff) return PA_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    const int seq_len_k = q_start + q_len;
+    const int last_page = (seq_len_k - 1) / block_size;
+    const int last_rows = seq_len_k - last_page * block_size;
+    CUtensorMap maps[5];
+    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, q_len, pa::kPfQRows) ||
+        !make_cache_map(&maps[1], k_cache, head_dim, num_kv_heads, block_size, num_pages,
+                        page_stride, pa::kPfKvTile) ||
+        !make_cache_map(&maps[2], v_cache, head_dim, num_kv_heads, block_size, num_pages,
+                        page_stride, pa::kPfKvTile) ||
+        !make_cache_map(&maps[3], k_cache, head_dim, num_kv_heads, last_rows, num_pages,
+                        page_stride, pa::kPfKvTile) ||
+        !make_cache_map(&maps[4], v_cache, head_dim, num_kv_heads, last_rows, num_pages,
+                        page_stride, pa::kPfKvTile))
+        return PA_ERR_CUDA;
+    pa::PrefillArgs a;
+    a.block_table = block_table;
+    a.q_len = q_len;
+    a.q_start = q_start;
+    a.causal = causal ? 1 : 0;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_q_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.last_page = last_page;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.out = out;
+    a.err = dev.err;
+    take_kernel_events(&a.ev_start, &a.ev_stop);
+    if (diag_enabled())
+        fprintf(stderr, "[pa] prefill: q_len=%d q_start=%d causal=%d bs=%d q_tiles=%d\n", q_len,
+                q_start, a.causal, block_size, num_q_tiles);
+    return pa::launch_prefill(maps, a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int pa_set_kernel_events(void *start, void *stop) {
+    if ((start == nullptr) != (stop == nullptr)) return PA_ERR_INVALID_ARG;
+    t_ev_start = static_cast<cudaEvent_t>(start);
+    t_ev_stop = static_cast<cudaEvent_t>(stop);
+    return PA_OK;
+}
+
+int pa_get_device_errors(unsigned int *bits, int clear, void *stream) {
+    if (!bits) return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, dev.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (clear && cudaMemset(dev.err, 0, sizeof v) != cudaSuccess) return PA_ERR_CUDA;
+    *bits = v;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// pa_cache.cu -- slot mapping and KV write of new tokens.
+//
+// Slot mapping follows the input-prep post §3.2 (slot = block_table[pos / bs] * bs +
+// pos % bs) and §5 (computed on the device from the resident block table, one launch).
+// The KV write copies each token's [Hkv, D] BF16 row, bit for bit, to its slot in the
+// page layout of the page832 post §4.  Both are pure integer / byte work.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+#include <atomic>
+
+namespace pa {
+
+cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
+    static std::atomic<unsigned long long> done[4];  // bit d: device d already set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const unsigned long long bit = 1ull << dev;
+    if (done[slot].load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[slot].fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ positions,
+                                    const int32_t *__restrict__ seq_idx,
+                                    const int32_t *__restrict__ block_table, int num_seqs,
+                                    int64_t bt_stride, int max_blocks, int num_tokens,
+                                    int block_size,
+                                    int64_t *__restrict__ slot_mapping, unsigned *err) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= num_tokens) return;
+    const int32_t pos = positions[i];
+    int64_t slot = -1;
+    if (pos >= 0) {
+        const int64_t s = seq_idx ? seq_idx[i] : 0;
+        const int logical_block = pos / block_size;
+        if (logical_block < max_blocks && s >= 0 && s < num_seqs) {
+            const int32_t block_number = block_table[s * bt_stride + logical_block];
+            if (block_number >= 0)
+                slot = (int64_t)block_number * block_size + pos % block_size;
+            else
+                atomicOr(err, kErrPosition);
+        } else {
+            atomicOr(err, kErrPosition);
+        }
+    }
+    slot_mapping[i] = slot;
+}
+
+cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
+                                const int32_t *block_table, int num_seqs, int64_t bt_stride,
+                                int max_blocks, int num_tokens, int block_size,
+                                int64_t *slot_mapping, unsigned *err, cudaStream_t stream) {
+    const int threads = 128;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks, threads, 0, stream>>>(positions, seq_idx, block_table,
+                                                        num_seqs, bt_stride, max_blocks,
+                                                        num_tokens,
+                                                        block_size, slot_mapping, err);
+    return cudaGetLastError();
+}
+
+// One warp-group per token row pair: each thread moves 16 bytes of K and 16 of V per
+// step.  Rows are row_elems BF16 long (Hkv * D, a multiple of 8).
+__global__ void __launch_bounds__(128) reshape_and_cache_kernel(
+    const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint16_t *k_cache,
+    uint16_t *v_cache, int64_t page_stride, int64_t num_pages,
+    const int64_t *__restrict__ slot_mapping, int num_tokens, int row_elems, int block_size,
+    unsigned *err) {
+    const int t = blockIdx.x;
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    const int64_t page = slot / block_size;
+    const int64_t offset = slot - page * block_size;
+    if (page >= num_pages) {
+        if (threadIdx.x == 0) atomicOr(err, kErrSlot);
+        return;
+    }
+    const int64_t dst = page * page_stride + offset * row_elems;  // in BF16 elements
+    uint4 *kd = reinterpret_cast<uint4 *>(k_cache + dst);
+    uint4 *vd = reinterpret_cast<uint4 *>(v_cache + dst);
+    const int vecs = row_elems / 8;
+    const uint4 *ks = key + (int64_t)t * vecs;
+    const uint4 *vs = value + (int64_t)t * vecs;
+    for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
+        const uint4 a = __ldg(ks + i);
+        const uint4 b = __ldg(vs + i);
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
+                                     uint16_t *k_cache, uint16_t *v_cache, int64_t page_stride,
+                                     int64_t num_pages, const int64_t *slot_mapping,
+                                     int num_tokens, int row_elems, int block_size,
+                                     unsigned *err, cudaStream_t stream) {
+    reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value), k_cache,
+        v_cache, page_stride, num_pages, slot_mapping, num_tokens, row_elems, block_size, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

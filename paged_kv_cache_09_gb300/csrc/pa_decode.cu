@@ -1,0 +1,399 @@
+// pa_decode.cu -- q=1 paged GQA decode: split-context kernel + log-sum-exp combine.
+//
+// What is computed (page832 post §5, §7): for sequence s and query head h,
+//     out[s, h] = softmax_t(scale * q[s, h] . k_t) . v_t,  t < seq_lens[s],
+// with k_t, v_t of KV head g = h / G read through the block table (page832 §1).
+//
+// How (GB300 design, not the pages' DCU design):
+//   * grid = (splits, KV heads, sequences).  A CTA owns a contiguous run of page-local
+//     16-token tiles of one (sequence, KV head) and all G <= 8 query heads of that KV
+//     head, so each K/V byte is read from HBM once for the whole group.
+//   * One producer warp walks the block table once per tile and issues TMA box loads
+//     (4 x 128-byte-swizzled boxes of 16 rows for K, 4 for V) into a 12-stage ring;
+//     tiles never straddle a page, and rows past the page end (block_size 784 leaves a
+//     16-token tail tile) come back as zeros and are masked.
+//   * Four consumer warps take tiles round-robin.  Per tile: S^T = K Q^T on the tensor
+//     cores (mma.m16n8k16, tokens as M, the group's heads as N), online softmax over
+//     tokens with warp shuffles, then O^T += V^T P^T with P split into a BF16 high part
+//     and a BF16 low part (two MMAs), which keeps P to ~16 significant bits.
+//   * At the end the four warps merge their (max, sum, acc) through shared memory and
+//     the CTA writes one fp32 partial per query head; the combine kernel merges the
+//     splits with a log-sum-exp and writes BF16.
+#include <math_constants.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kDecThreads = (kDecConsumers + 1) * 32;
+constexpr int kDecChunkBytes = kDecTile * 128;             // one 64-dim box: 16 rows x 128 B
+constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one tile: 8 KB
+constexpr int kDecStageBytes = 2 * kDecHalf;                // 16 KB
+constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 192 KB
+constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kHeadDim + 2) * 4;
+static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
+constexpr int kDecSmemBytes = 1024 + kDecRingBytes + 2 * kDecStages * 8;
+
+struct DecodeKParams {
+    const uint16_t *q;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    const int32_t *seq_lens;
+    int max_seq_len;
+    int num_q_heads;
+    int group;
+    int block_size;
+    int tiles_per_page;
+    int tiles_per_split;
+    int num_splits;
+    int64_t num_pages;
+    float scale_log2;   // scale * log2(e): scores are kept in base-2 units
+    float *part_o;      // [S, Hq, splits, D] unnormalised sums
+    float2 *part_ml;    // [S, Hq, splits] (running max in base-2 units, sum of weights)
+    uint16_t *out;
+    unsigned *err;
+};
+
+__device__ __forceinline__ int seq_tiles(int seq_len, int block_size, int tiles_per_page) {
+    const int full = seq_len / block_size;
+    const int rem = seq_len - full * block_size;
+    return full * tiles_per_page + (rem + kDecTile - 1) / kDecTile;
+}
+
+__device__ __forceinline__ int checked_seq_len(const DecodeKParams &p, int seq, bool report) {
+    int L = p.seq_lens[seq];
+    if (L < 1 || L > p.max_seq_len) {
+        if (report) atomicOr(p.err, kErrSeqLen);
+        L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    }
+    return L;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const DecodeKParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecRingBytes);
+    uint64_t *empty = full + kDecStages;
+
+    const int split = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int seq_len =
+        checked_seq_len(p, seq, threadIdx.x == 0 && split == 0 && g == 0);
+    const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
+    const int t0 = split * p.tiles_per_split;
+    const int t1 = min(ntiles, t0 + p.tiles_per_split);
+    if (t0 >= t1) return;  // this split has no tiles of this sequence
+    const int n = t1 - t0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDecStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kDecConsumers) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % kDecStages;
+                if (i >= kDecStages &&
+                    !mbar_wait(&empty[s], ((i / kDecStages) - 1) & 1, p.err))
+                    break;
+                const int j = t0 + i;
+                const int lp = j / p.tiles_per_page;
+                const int off = (j - lp * p.tiles_per_page) * kDecTile;
+                const int page = bt[lp];
+                // A page outside the pool is reported; the TMA box then lies outside the
+                // tensor and reads as zeros, so nothing faults.
+                if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrPage);
+                uint8_t *st = smem + s * kDecStageBytes;
+                mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    tma_load_4d(st + c * kDecChunkBytes, &tmk, &full[s], c * kChunkElems, g,
+                                off, page);
+                    tma_load_4d(st + kDecHalf + c * kDecChunkBytes, &tmv, &full[s],
+                                c * kChunkElems, g, off, page);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Q^T as the B operand: lane holds head n = lane/4 and dims 2(lane%4)+{0,1} (+8)
+    // of every 16-dim k-step.  Heads past the group are zero columns.
+    const int nh = lane >> 2;
+    const int qc = (lane & 3) * 2;
+    uint32_t qb[16][2];
+    {
+        const bool hv = nh < p.group;
+        const uint16_t *qrow =
+            p.q + ((int64_t)seq * p.num_q_heads + g * p.group + (hv ? nh : 0)) * kHeadDim;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            qb[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + qc) : 0u;
+            qb[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + qc + 8) : 0u;
+        }
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // heads qc, qc+1 (base-2 units)
+    float l0 = 0.f, l1 = 0.f;                        // this lane's share of the sums
+    const uint32_t sbase = smem_u32(smem);
+    const int r_lo = lane >> 2;  // token rows r_lo and r_lo + 8 of the tile
+
+    for (int i = warp; i < n; i += kDecConsumers) {
+        const int s = i % kDecStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kDecStages) & 1, p.err))) break;
+        const int j = t0 + i;
+        const int lp = j / p.tiles_per_page;
+        const int off = (j - lp * p.tiles_per_page) * kDecTile;
+        const int tok0 = lp * p.block_size + off;
+        const int nvalid = min(kDecTile, min(p.block_size - off, seq_len - tok0));
+        const uint32_t kb = sbase + s * kDecStageBytes;
+        const uint32_t vb = kb + kDecHalf;
+
+        if (nvalid < kDecTile) {
+            // Rows past the sequence end may hold anything (even NaN): zero them in V
+            // so that a zero weight cannot meet a NaN inside the MMA.
+            uint8_t *vp = smem + s * kDecStageBytes + kDecHalf;
+            const int per_chunk = (kDecTile - nvalid) * 8;
+            for (int u = lane; u < per_chunk * kChunks; u += 32) {
+                const int c = u / per_chunk;
+                const int r = nvalid + (u - c * per_chunk) / 8;
+                const int unit = u & 7;
+                *reinterpret_cast<uint4 *>(vp + c * kDecChunkBytes + r * 128 + unit * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // S^T (16 tokens x 8 heads) = K (16 x 256) . Q^T (256 x 8)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int uhi = lane >> 4;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(swz128(kb + (kk >> 2) * kDecChunkBytes, row, (kk & 3) * 2 + uhi), a0,
+                        a1, a2, a3);
+                mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            }
+        }
+
+        // Online softmax over the tile's tokens, per head.
+        const bool v0 = r_lo < nvalid, v1 = r_lo + 8 < nvalid;
+        const float x00 = v0 ? sc[0] * p.scale_log2 : -CUDART_INF_F;
+        const float x01 = v0 ? sc[1] * p.scale_log2 : -CUDART_INF_F;
+        const float x10 = v1 ? sc[2] * p.scale_log2 : -CUDART_INF_F;
+        const float x11 = v1 ? sc[3] * p.scale_log2 : -CUDART_INF_F;
+        float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+        const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+        const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+        const float p00 = exp2f(x00 - mu0), p01 = exp2f(x01 - mu1);
+        const float p10 = exp2f(x10 - mu0), p11 = exp2f(x11 - mu1);
+        l0 = l0 * al0 + (p00 + p10);
+        l1 = l1 * al1 + (p01 + p11);
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+
+        // P^T as the B operand: the S^T fragment holds (token, head pair); the 8x8
+        // transpose turns it into (head, token pair).  High and low BF16 parts.
+        const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);
+        const uint32_t e0 = pack_bf16x2(p00 - bf16_lo(h0), p01 - bf16_hi(h0));
+        const uint32_t e1 = pack_bf16x2(p10 - bf16_lo(h1), p11 - bf16_hi(h1));
+        const uint32_t bh0 = movmatrix_t(h0), bh1 = movmatrix_t(h1);
+        const uint32_t bl0 = movmatrix_t(e0), bl1 = movmatrix_t(e1);
+
+        // O^T (256 dims x 8 heads) += V^T (256 x 16 tokens) . P^T (16 x 8)
+        {
+            const int jm = lane >> 3;
+            const int row = (lane & 7) + (jm >> 1) * 8;
+            const int ulo = jm & 1;
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(swz128(vb + (mt >> 2) * kDecChunkBytes, row, (mt & 3) * 2 + ulo), a0,
+                          a1, a2, a3);
+                mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+                mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+    }
+
+    // ---------------------------------------------------------------- CTA merge
+    named_bar_sync(1, kDecConsumers * 32);  // every tile consumed: the ring is free
+    float *red_o = reinterpret_cast<float *>(smem);                 // [warp][head][D]
+    float *red_m = red_o + kDecConsumers * kDecMaxGroup * kHeadDim;  // [warp][head]
+    float *red_l = red_m + kDecConsumers * kDecMaxGroup;
+    if (lane < 4) {
+        red_m[warp * kDecMaxGroup + qc] = m0;
+        red_m[warp * kDecMaxGroup + qc + 1] = m1;
+        red_l[warp * kDecMaxGroup + qc] = l0;
+        red_l[warp * kDecMaxGroup + qc + 1] = l1;
+    }
+    {
+        float *w0 = red_o + (warp * kDecMaxGroup + qc) * kHeadDim;
+        float *w1 = w0 + kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            const int d = mt * 16 + r_lo;
+            w0[d] = o[mt][0];
+            w1[d] = o[mt][1];
+            w0[d + 8] = o[mt][2];
+            w1[d + 8] = o[mt][3];
+        }
+    }
+    named_bar_sync(1, kDecConsumers * 32);
+    for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += kDecConsumers * 32) {
+        const int c = idx / kHeadDim, d = idx - c * kHeadDim;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, red_m[w * kDecMaxGroup + c]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kDecConsumers; ++w) {
+                const float e = exp2f(red_m[w * kDecMaxGroup + c] - M);
+                L += e * red_l[w * kDecMaxGroup + c];
+                O += e * red_o[(w * kDecMaxGroup + c) * kHeadDim + d];
+            }
+        }
+        const int64_t pi =
+            ((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split;
+        p.part_o[pi * kHeadDim + d] = O;
+        if (d == 0) p.part_ml[pi] = make_float2(M, L);
+    }
+}
+
+// One CTA per (query head, sequence); thread d owns output dim d.
+__global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodeKParams p) {
+    const int h = blockIdx.x, seq = blockIdx.y, d = threadIdx.x;
+    const int seq_len = checked_seq_len(p, seq, false);
+    const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
+    const int nsplit = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.num_splits;
+    float M = -CUDART_INF_F;
+    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, p.part_ml[base + j].x);
+    float L = 0.f, O = 0.f;
+    if (M != -CUDART_INF_F) {
+        for (int j = 0; j < nsplit; ++j) {
+            const float2 ml = p.part_ml[base + j];
+            const float e = exp2f(ml.x - M);
+            L += e * ml.y;
+            O += e * p.part_o[(base + j) * kHeadDim + d];
+        }
+    }
+    const float r = L > 0.f ? O / L : 0.f;
+    const __nv_bfloat16 b = __float2bfloat16_rn(r);
+    p.out[((int64_t)seq * p.num_q_heads + h) * kHeadDim + d] =
+        *reinterpret_cast<const uint16_t *>(&b);
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int num_seqs, int num_kv_heads, int block_size, int max_seq_len,
+                       int num_sms) {
+    DecodePlan pl;
+    pl.tiles_per_page = (block_size + kDecTile - 1) / kDecTile;
+    const int full = max_seq_len / block_size;
+    const int rem = max_seq_len - full * block_size;
+    pl.max_tiles = full * pl.tiles_per_page + (rem + kDecTile - 1) / kDecTile;
+    const long long pairs = (long long)num_seqs * num_kv_heads;
+    // One CTA per SM across all (sequence, KV head) pairs, at least one tile per warp.
+    long long want = (num_sms + pairs - 1) / pairs;
+    if (want < 1) want = 1;
+    int tps = (int)((pl.max_tiles + want - 1) / want);
+    if (tps < kDecConsumers) tps = kDecConsumers;
+    pl.tiles_per_split = tps;
+    pl.num_splits = (pl.max_tiles + tps - 1) / tps;
+    return pl;
+}
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, const DecodePlan &plan) {
+    const size_t parts = (size_t)num_seqs * num_q_heads * plan.num_splits;
+    const size_t o_bytes = (parts * kHeadDim * sizeof(float) + 255) & ~size_t(255);
+    const size_t ml_bytes = (parts * sizeof(float2) + 255) & ~size_t(255);
+    return o_bytes + ml_bytes;
+}
+
+cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                          const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_split_kernel),
+                                  kDecSmemBytes, 0);
+    if (e != cudaSuccess) return e;
+    DecodeKParams p;
+    p.q = a.q;
+    p.block_table = a.block_table;
+    p.bt_stride = a.bt_stride;
+    p.seq_lens = a.seq_lens;
+    p.max_seq_len = a.max_seq_len;
+    p.num_q_heads = a.num_q_heads;
+    p.group = a.group;
+    p.block_size = a.block_size;
+    p.tiles_per_page = plan.tiles_per_page;
+    p.tiles_per_split = plan.tiles_per_split;
+    p.num_splits = plan.num_splits;
+    p.num_pages = a.num_pages;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const size_t parts = (size_t)a.num_seqs * a.num_q_heads * plan.num_splits;
+    const size_t o_bytes = (parts * kHeadDim * sizeof(float) + 255) & ~size_t(255);
+    p.part_o = static_cast<float *>(a.workspace);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(a.workspace) + o_bytes);
+    p.out = a.out;
+    p.err = a.err;
+    const dim3 grid(plan.num_splits, a.num_kv_heads, a.num_seqs);
+    if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
+    decode_split_kernel<<<grid, kDecThreads, kDecSmemBytes, stream>>>(tmap_k, tmap_v, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, stream)) != cudaSuccess) return e;
+    decode_combine_kernel<<<dim3(a.num_q_heads, a.num_seqs), kHeadDim, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,86 @@
+// pa_internal.h -- host-side declarations shared between the C-ABI layer (pa_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel slot, device), so that
+// later launches (possibly under stream capture) make no attribute call.
+cudaError_t set_smem_once(const void *kernel, int bytes, int slot);
+
+// ----------------------------------------------------------------- cache write
+cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
+                                const int32_t *block_table, int num_seqs, int64_t bt_stride,
+                                int max_blocks,
+                                int num_tokens, int block_size, int64_t *slot_mapping,
+                                unsigned *err, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
+                                     uint16_t *k_cache, uint16_t *v_cache, int64_t page_stride,
+                                     int64_t num_pages, const int64_t *slot_mapping,
+                                     int num_tokens, int row_elems, int block_size,
+                                     unsigned *err, cudaStream_t stream);
+
+// ----------------------------------------------------------------- decode
+constexpr int kDecTile = 16;       // tokens per pipeline stage (page-local)
+constexpr int kDecStages = 12;     // shared-memory ring depth
+constexpr int kDecConsumers = 4;   // consumer warps per CTA (plus one producer warp)
+constexpr int kDecMaxGroup = 8;    // query heads per KV head handled by one MMA column tile
+
+struct DecodePlan {
+    int tiles_per_page;   // ceil(block_size / kDecTile)
+    int max_tiles;        // tiles of the longest allowed sequence
+    int tiles_per_split;  // tiles one CTA processes
+    int num_splits;       // CTAs per (sequence, KV head)
+};
+
+DecodePlan plan_decode(int num_seqs, int num_kv_heads, int block_size, int max_seq_len,
+                       int num_sms);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, const DecodePlan &plan);
+
+struct DecodeArgs {
+    const uint16_t *q;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    const int32_t *seq_lens;
+    int num_seqs, max_seq_len;
+    int num_q_heads, num_kv_heads, group;
+    int block_size;
+    int64_t num_pages;
+    float scale;
+    uint16_t *out;
+    void *workspace;
+    unsigned *err;
+    cudaEvent_t ev_start, ev_stop;  // optional: recorded around the split kernel
+};
+
+cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                          const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+
+// ----------------------------------------------------------------- prefill
+constexpr int kPfQRows = 64;       // query rows per CTA (16 per consumer warp)
+constexpr int kPfKvTile = 64;      // keys per pipeline stage (page-local)
+constexpr int kPfStages = 2;
+
+struct PrefillArgs {
+    const int32_t *block_table;
+    int q_len, q_start, causal;
+    int num_q_heads, num_kv_heads, group;
+    int block_size;
+    int last_page;        // logical index of the sequence's last page
+    int64_t num_pages;
+    float scale;
+    uint16_t *out;
+    unsigned *err;
+    cudaEvent_t ev_start, ev_stop;  // optional: recorded around the prefill kernel
+};
+
+// tmaps: Q, K, V, K of the last page, V of the last page.
+cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream);
+
+}  // namespace pa

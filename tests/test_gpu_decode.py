@@ -1,0 +1,192 @@
+"""q=1 paged decode on the GPU vs the fp64 oracle, on the pages' workloads at full size
+and on edge cases (page tails, sequence ends on and around page boundaries, unbind
+views, group sizes, bad inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._util import assert_attention_close
+from workloads import bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_decode(case, k_host=None, v_host=None):
+    return oracle.decode(bits(case.q), bits(case.k_cache) if k_host is None else k_host,
+                         bits(case.v_cache) if v_host is None else v_host,
+                         case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(),
+                         case.scale)
+
+
+def _gpu_decode(pa, case, max_seq_len=None, **kw):
+    msl = int(case.seq_lens.max()) if max_seq_len is None else max_seq_len
+    return pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                     case.scale, msl, **kw)
+
+
+def test_tiny_decode_with_fused_new_token_write(cuda_lib):
+    pa = cuda_lib
+    case = workloads.tiny_decode("cuda")
+    slots = pa.slot_mapping(case.positions, case.block_table, case.block_size,
+                            seq_idx=case.seq_idx)
+    out = _gpu_decode(pa, case, new_k=case.new_k, new_v=case.new_v, new_slots=slots)
+    torch.cuda.synchronize()
+    k_host, v_host = bits(case.k_cache), bits(case.v_cache)
+    # The oracle writes the new token into its own copy of the caches (which still have
+    # the NaN at that slot, since the GPU copy is read back after the fused write) ...
+    k_ref, v_ref = k_host.copy(), v_host.copy()
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_ref, v_ref,
+                             oracle.slot_mapping(case.positions.cpu().numpy(),
+                                                 case.block_table.cpu().numpy(), 832,
+                                                 case.seq_idx.cpu().numpy()), 832)
+    assert np.array_equal(k_ref, k_host) and np.array_equal(v_ref, v_host)
+    ref = _oracle_decode(case, k_ref, v_ref)
+    e = assert_attention_close(out, ref, "tiny decode")
+    assert e["rel_l2"] < 5e-3
+    assert pa.device_errors() == 0
+
+
+@pytest.mark.parametrize("bs", [832, 784])
+def test_decode_8k(cuda_lib, bs):
+    pa = cuda_lib
+    case = workloads.decode_8k(bs, "cuda")
+    out = _gpu_decode(pa, case)
+    assert_attention_close(out, _oracle_decode(case), f"decode 8K bs={bs}")
+    assert pa.device_errors() == 0
+
+
+@pytest.mark.parametrize("context", [4096, 8192, 16384, 32768])
+def test_decode_sweep_peaked_1gib_pool(cuda_lib, context):
+    pa = cuda_lib
+    case = workloads.decode_sweep(context, "cuda")
+    out = _gpu_decode(pa, case)
+    assert_attention_close(out, _oracle_decode(case), f"sweep {context}")
+    assert pa.device_errors() == 0
+
+
+def test_batched_decode_fused_write(cuda_lib):
+    pa = cuda_lib
+    case = workloads.batched_decode("cuda")
+    k_before, v_before = bits(case.k_cache), bits(case.v_cache)
+    slots = pa.slot_mapping(case.positions, case.block_table, case.block_size,
+                            seq_idx=case.seq_idx)
+    out = _gpu_decode(pa, case, new_k=case.new_k, new_v=case.new_v, new_slots=slots)
+    torch.cuda.synchronize()
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_before, v_before,
+                             oracle.slot_mapping(case.positions.cpu().numpy(),
+                                                 case.block_table.cpu().numpy(),
+                                                 case.block_size, case.seq_idx.cpu().numpy()),
+                             case.block_size)
+    ref = _oracle_decode(case, k_before, v_before)
+    assert_attention_close(out, ref, "batched decode")
+    assert pa.device_errors() == 0
+
+
+EDGE_LENS = [1, 15, 16, 17, 63, 64, 65, 783, 784, 785, 831, 832, 833, 1700]
+
+
+@pytest.mark.parametrize("bs", [784, 832, 64, 16])
+def test_decode_edge_lengths_in_one_batch(cuda_lib, bs):
+    pa = cuda_lib
+    npg = sum(-(-L // bs) for L in EDGE_LENS) + 3
+    case = workloads.paged_case(77 + bs, EDGE_LENS, bs, npg, device="cuda")
+    out = _gpu_decode(pa, case)
+    assert_attention_close(out, _oracle_decode(case), f"edge lengths bs={bs}")
+    # seq_len 1 returns that token's value row (up to BF16 rounding of an exact copy).
+    v = case.v_cache[int(case.block_table[0, 0]), 0]          # [Hkv, D]
+    want = v.repeat_interleave(case.q.shape[1] // v.shape[0], dim=0)
+    assert torch.equal(out[0], want)
+    assert pa.device_errors() == 0
+
+
+def test_decode_max_seq_len_above_actual_lengths(cuda_lib):
+    # The split plan is made for max_seq_len; shorter sequences leave splits empty.
+    pa = cuda_lib
+    case = workloads.paged_case(5, [100, 5000, 1], 832, 12, device="cuda", max_blocks=40)
+    out = _gpu_decode(pa, case, max_seq_len=40 * 832)
+    assert_attention_close(out, _oracle_decode(case), "max_seq_len slack")
+
+
+def test_decode_unbind_view_page_stride(cuda_lib):
+    pa = cuda_lib
+    case = workloads.decode_8k(832, "cuda")
+    kv = torch.stack([case.k_cache, case.v_cache], dim=1)       # [pages, 2, BS, Hkv, D]
+    k_view, v_view = kv.unbind(1)
+    out = pa.decode(case.q, k_view, v_view, case.block_table, case.seq_lens, case.scale, 8192)
+    ref_out = _gpu_decode(pa, case)
+    assert torch.equal(out, ref_out)
+    assert_attention_close(out, _oracle_decode(case), "unbind view")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 2), (8, 1), (12, 4)])
+def test_decode_other_group_sizes(cuda_lib, hq, hkv):
+    pa = cuda_lib
+    case = workloads.paged_case(900 + hq, [700, 2000], 64, 48, hq=hq, hkv=hkv, device="cuda")
+    out = _gpu_decode(pa, case)
+    assert_attention_close(out, _oracle_decode(case), f"group {hq}/{hkv}")
+
+
+def test_decode_is_deterministic(cuda_lib):
+    pa = cuda_lib
+    case = workloads.decode_sweep(16384, "cuda")
+    a = _gpu_decode(pa, case)
+    b = _gpu_decode(pa, case)
+    assert torch.equal(a, b)
+
+
+def test_decode_block_size_784_vs_832_close(cuda_lib):
+    # Same logical tokens, two page sizes: both match the oracle; the oracle itself gives
+    # identical results for both (the definition does not depend on the page size).
+    pa = cuda_lib
+    T = 3000
+    g = torch.Generator(device="cuda").manual_seed(3)
+    kc = torch.randn(T, 4, 256, generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(T, 4, 256, generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn(1, 24, 256, generator=g, device="cuda").to(torch.bfloat16)
+    outs, refs = [], []
+    for bs in (784, 832):
+        npg = -(-T // bs)
+        k_cache = torch.zeros(npg + 2, bs, 4, 256, dtype=torch.bfloat16, device="cuda")
+        v_cache = torch.zeros_like(k_cache)
+        perm = torch.randperm(npg + 2, generator=torch.Generator().manual_seed(bs))[:npg]
+        bt = perm.to(torch.int32).view(1, -1).cuda()
+        slots = pa.slot_mapping(torch.arange(T, dtype=torch.int32, device="cuda"), bt, bs)
+        pa.reshape_and_cache(kc, vc, k_cache, v_cache, slots)
+        sl = torch.tensor([T], dtype=torch.int32, device="cuda")
+        outs.append(pa.decode(q, k_cache, v_cache, bt, sl, 1 / 16, T))
+        refs.append(oracle.decode(bits(q), bits(k_cache), bits(v_cache), bt.cpu().numpy(),
+                                  np.array([T], np.int32), 1 / 16))
+    assert np.array_equal(refs[0], refs[1])
+    for o in outs:
+        assert_attention_close(o, refs[0], "bs invariance")
+
+
+def test_decode_bad_page_is_reported_not_faulted(cuda_lib):
+    pa = cuda_lib
+    case = workloads.paged_case(9, [2000], 832, 6, device="cuda")
+    case.block_table[0, 1] = case.num_pages + 3       # outside the pool: reads zeros
+    out = _gpu_decode(pa, case)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert pa.device_errors() & pa.DEVERR_PAGE
+    assert pa.device_errors() == 0
+
+
+def test_decode_seq_len_above_max_is_reported(cuda_lib):
+    pa = cuda_lib
+    case = workloads.paged_case(10, [900], 832, 4, device="cuda", max_blocks=2)
+    case.seq_lens[0] = 5000                            # above max_seq_len = 1664
+    out = _gpu_decode(pa, case, max_seq_len=1664)
+    torch.cuda.synchronize()
+    assert pa.device_errors() & pa.DEVERR_SEQLEN
+    assert out.shape == case.q.shape
+
+
+def test_decode_workspace_too_small_is_rejected(cuda_lib):
+    pa = cuda_lib
+    case = workloads.decode_8k(832, "cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PAError):
+        _gpu_decode(pa, case, workspace=ws)

@@ -1,0 +1,120 @@
+"""Chunked causal prefill on the GPU vs the fp64 oracle: small shapes compared on every
+element (several query and key tiles, ragged tails, page sizes 784/832/64/16), and the
+q=4096 chunk over 4096 prior tokens at full size on sampled (row, head) outputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._util import assert_attention_close
+from workloads import bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _write_chunk(pa, case):
+    """The chunk's own K/V go into the cache first, through the library."""
+    slots = pa.slot_mapping(case.positions, case.block_table, case.block_size,
+                            seq_idx=case.seq_idx)
+    pa.reshape_and_cache(case.new_k, case.new_v, case.k_cache, case.v_cache, slots)
+    return slots
+
+
+def _oracle_caches_after_write(case, k_host, v_host):
+    sl = oracle.slot_mapping(case.positions.cpu().numpy(), case.block_table.cpu().numpy(),
+                             case.block_size)
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_host, v_host, sl,
+                             case.block_size)
+    return k_host, v_host
+
+
+@pytest.mark.parametrize("bs,q_len,q_start", [
+    (832, 1, 0), (832, 64, 0), (832, 65, 3), (832, 200, 100), (832, 130, 1000),
+    (784, 300, 700), (784, 64, 784), (64, 129, 63), (16, 77, 40), (16, 1, 500),
+])
+def test_prefill_small_every_element(cuda_lib, bs, q_len, q_start):
+    pa = cuda_lib
+    npg = -(-(q_start + q_len) // bs) + 3
+    case = workloads.paged_case(300 + q_len + q_start, [q_start + q_len], bs, npg,
+                                q_rows=q_len, q_start=q_start, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                           True, case.scale)
+    ref = oracle.prefill(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                         q_start, True, case.scale)
+    assert_attention_close(out, ref, f"prefill bs={bs} q={q_len}@{q_start}")
+    assert pa.device_errors() == 0
+
+
+@pytest.mark.parametrize("bs,q_len,q_start", [(832, 100, 900), (64, 70, 0)])
+def test_prefill_non_causal(cuda_lib, bs, q_len, q_start):
+    pa = cuda_lib
+    npg = -(-(q_start + q_len) // bs) + 2
+    case = workloads.paged_case(500 + q_len, [q_start + q_len], bs, npg, q_rows=q_len,
+                                q_start=q_start, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                           False, case.scale)
+    ref = oracle.prefill(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                         q_start, False, case.scale)
+    assert_attention_close(out, ref, "non-causal")
+
+
+def test_prefill_chunk_4096_over_4096_sampled(cuda_lib):
+    pa = cuda_lib
+    case = workloads.prefill_chunk("cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
+                           case.q_start, True, case.scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    # The GPU's copy of the cache after its own write is the oracle's copy, bit for bit.
+    assert np.array_equal(bits(case.k_cache), k_host)
+    assert np.array_equal(bits(case.v_cache), v_host)
+    rng = np.random.default_rng(4096)
+    rows = np.concatenate([[0, 1, 63, 64, 65, 127, 128, 2047, 2048, 4032, 4094, 4095],
+                           rng.integers(0, 4096, 180)]).astype(np.int32)
+    heads = rng.integers(0, 24, rows.size).astype(np.int32)
+    heads[:12] = np.arange(12) * 2 + 1
+    ref = oracle.prefill_rows(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                              case.q_start, True, case.scale, rows, heads)
+    got = out[torch.from_numpy(rows).long().cuda(), torch.from_numpy(heads).long().cuda()]
+    assert_attention_close(got, ref, "q=4096 chunk (sampled)")
+    assert pa.device_errors() == 0
+    again = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
+                             case.q_start, True, case.scale)
+    assert torch.equal(out, again)                         # deterministic
+
+
+def test_prefill_unbind_views(cuda_lib):
+    pa = cuda_lib
+    q_len, q_start, bs = 150, 900, 832
+    case = workloads.paged_case(42, [q_start + q_len], bs, 5, q_rows=q_len, q_start=q_start,
+                                device="cuda")
+    _write_chunk(pa, case)
+    kv = torch.stack([case.k_cache, case.v_cache], dim=1)
+    kview, vview = kv.unbind(1)
+    a = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                         True, case.scale)
+    b = pa.prefill_chunk(case.q, kview, vview, case.block_table[0], q_start, True, case.scale)
+    assert torch.equal(a, b)
+
+
+def test_prefill_row_equals_decode_of_its_prefix(cuda_lib):
+    # The last chunk row at position p attends to the same keys as a decode with p+1 keys.
+    pa = cuda_lib
+    q_len, q_start, bs = 40, 1200, 832
+    case = workloads.paged_case(43, [q_start + q_len], bs, 6, q_rows=q_len, q_start=q_start,
+                                device="cuda")
+    _write_chunk(pa, case)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                           True, case.scale)
+    sl = torch.tensor([q_start + q_len], dtype=torch.int32, device="cuda")
+    dec = pa.decode(case.q[-1:].contiguous(), case.k_cache, case.v_cache, case.block_table, sl,
+                    case.scale, q_start + q_len)
+    d = (out[-1].float() - dec[0].float()).abs().max().item()
+    assert d <= 1e-2
