@@ -202,13 +202,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             o[nt][3] *= al_b;
         }
 
-        // O (16 x 256) += P (16 x 64) . V (64 x 256)
+        // O (16 x 256) += P (16 x 64) . V (64 x 256), with P = P_hi + P_lo in two BF16
+        // parts: a single BF16 P carries a relative error up to 2^-8 per weight, which
+        // rows with few or peaked keys turn into output errors above the tolerance.
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
-            const uint32_t a0 = pack_bf16x2(sacc[2 * kt][0], sacc[2 * kt][1]);
-            const uint32_t a1 = pack_bf16x2(sacc[2 * kt][2], sacc[2 * kt][3]);
-            const uint32_t a2 = pack_bf16x2(sacc[2 * kt + 1][0], sacc[2 * kt + 1][1]);
-            const uint32_t a3 = pack_bf16x2(sacc[2 * kt + 1][2], sacc[2 * kt + 1][3]);
+            uint32_t ah[4], al[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float x0 = sacc[2 * kt + (r >> 1)][(r & 1) * 2];
+                const float x1 = sacc[2 * kt + (r >> 1)][(r & 1) * 2 + 1];
+                ah[r] = pack_bf16x2(x0, x1);
+                al[r] = pack_bf16x2(x0 - bf16_lo(ah[r]), x1 - bf16_hi(ah[r]));
+            }
 #pragma unroll
             for (int dp = 0; dp < 16; ++dp) {
                 uint32_t b0, b1, b2, b3;
@@ -216,8 +222,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                  kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8,
                                  (dp & 3) * 2 + (lane >> 4)),
                           b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * dp], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+                mma_bf16_16816(o[2 * dp], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                mma_bf16_16816(o[2 * dp + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
+                mma_bf16_16816(o[2 * dp], al[0], al[1], al[2], al[3], b0, b1);
+                mma_bf16_16816(o[2 * dp + 1], al[0], al[1], al[2], al[3], b2, b3);
             }
         }
         __syncwarp();
