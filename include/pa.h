@@ -124,6 +124,37 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
               void *stream);
 
 /*
+ * pa_decode_noalloc -- the same decode as pa_decode (without the fused write), for
+ * callers that cannot allocate device memory on the decode path: for example a serving
+ * runtime that gives almost all device memory to its KV-cache pool at start-up and
+ * allows no allocation afterwards, or plain C code with no device allocator at hand.
+ * The pages describe nothing like it; it exists only for such callers.
+ *
+ * Instead of a caller-provided workspace it uses one fixed scratch array of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES (4 MiB) that is part of the library's device image:
+ * every GPU that loads the library holds that memory until the process exits.  The call
+ * allocates and frees nothing.  The caller still passes all inputs and the output.
+ *   - Problems whose split partials need more than that (pa_decode_workspace_size >
+ *     PA_DECODE_NOALLOC_SCRATCH_BYTES; about 160 sequences of 24 heads, or fewer with
+ *     long contexts on few sequences) are refused with PA_ERR_UNSUPPORTED and nothing
+ *     is queued.  Other bad arguments return what pa_decode returns for them.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current) and keeps it; make that first call before any stream capture.
+ *   - All calls on a device share the one array, and it keeps whatever the last call
+ *     wrote.  Nothing in it needs to start at zero: every value a call reads from it was
+ *     written earlier in the same call.  Calls whose work overlaps on the GPU (different
+ *     streams, or different host threads, without ordering between them) race on the
+ *     array and can produce wrong outputs; order them, e.g. on one stream.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+int pa_decode_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                      int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                      int64_t bt_stride, const int32_t *seq_lens, int num_seqs,
+                      int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, float scale, pa_bf16 *out, void *stream);
+
+/*
  * pa_prefill_chunk -- attention of a chunk of q_len query rows of ONE sequence over
  * that sequence's paged cache [page832 §6].  Row i sits at absolute position
  * q_start + i; with causal != 0 it sees keys 0..q_start+i (diagonal included),
