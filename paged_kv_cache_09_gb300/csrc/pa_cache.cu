@@ -31,6 +31,8 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ positions,
                                     int block_size,
                                     int64_t *__restrict__ slot_mapping, unsigned *err) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     if (i >= num_tokens) return;
     const int32_t pos = positions[i];
     int64_t slot = -1;
@@ -56,11 +58,9 @@ cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx
                                 int64_t *slot_mapping, unsigned *err, cudaStream_t stream) {
     const int threads = 128;
     const int blocks = (num_tokens + threads - 1) / threads;
-    slot_mapping_kernel<<<blocks, threads, 0, stream>>>(positions, seq_idx, block_table,
-                                                        num_seqs, bt_stride, max_blocks,
-                                                        num_tokens,
-                                                        block_size, slot_mapping, err);
-    return cudaGetLastError();
+    return launch_pdl(slot_mapping_kernel, dim3(blocks), dim3(threads), 0, stream, positions,
+                      seq_idx, block_table, num_seqs, bt_stride, max_blocks, num_tokens,
+                      block_size, slot_mapping, err);
 }
 
 // One warp-group per token row pair: each thread moves 16 bytes of K and 16 of V per
@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     const int64_t *__restrict__ slot_mapping, int num_tokens, int row_elems, int block_size,
     unsigned *err) {
     const int t = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     if (t >= num_tokens) return;
     const int64_t slot = slot_mapping[t];
     if (slot < 0) return;
@@ -99,10 +101,10 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
                                      int64_t num_pages, const int64_t *slot_mapping,
                                      int num_tokens, int row_elems, int block_size,
                                      unsigned *err, cudaStream_t stream) {
-    reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value), k_cache,
-        v_cache, page_stride, num_pages, slot_mapping, num_tokens, row_elems, block_size, err);
-    return cudaGetLastError();
+    return launch_pdl(reshape_and_cache_kernel, dim3(num_tokens), dim3(128), 0, stream,
+                      reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value),
+                      k_cache, v_cache, page_stride, num_pages, slot_mapping, num_tokens,
+                      row_elems, block_size, err);
 }
 
 }  // namespace pa

@@ -9,16 +9,18 @@
 //     16-token tiles of one (sequence, KV head) and all G <= 8 query heads of that KV
 //     head, so each K/V byte is read from HBM once for the whole group.
 //   * One producer warp walks the block table once per tile and issues TMA box loads
-//     (4 x 128-byte-swizzled boxes of 16 rows for K, 4 for V) into a 12-stage ring;
+//     (4 x 128-byte-swizzled boxes of 16 rows for K, 4 for V) into a 14-stage ring;
 //     tiles never straddle a page, and rows past the page end (block_size 784 leaves a
 //     16-token tail tile) come back as zeros and are masked.
-//   * Four consumer warps take tiles round-robin.  Per tile: S^T = K Q^T on the tensor
-//     cores (mma.m16n8k16, tokens as M, the group's heads as N), online softmax over
-//     tokens with warp shuffles, then O^T += V^T P^T with P split into a BF16 high part
-//     and a BF16 low part (two MMAs), which keeps P to ~16 significant bits.
-//   * At the end the four warps merge their (max, sum, acc) through shared memory and
-//     the CTA writes one fp32 partial per query head; the combine kernel merges the
-//     splits with a log-sum-exp and writes BF16.
+//   * Seven consumer warps take tiles round-robin (tile i -> warp i % 7, stage i % 14).
+//     Per tile: S^T = K Q^T on the tensor cores (mma.m16n8k16, tokens as M, the group's
+//     heads as N, two accumulator chains), online softmax over tokens with warp
+//     shuffles, then O^T += V^T P^T with P split into a BF16 high part and a BF16 low
+//     part (two MMAs), which keeps P to ~16 significant bits.
+//   * At the end the warps merge their (max, sum, acc) through shared memory and the
+//     CTA writes one fp32 partial per query head; the combine kernel merges the splits
+//     with a log-sum-exp and writes BF16.  Both kernels use programmatic dependent
+//     launch, so the combine's launch overlaps the split kernel's tail.
 #include <math_constants.h>
 
 #include "pa_device.cuh"
@@ -32,10 +34,11 @@ constexpr int kDecThreads = (kDecConsumers + 1) * 32;
 constexpr int kDecChunkBytes = kDecTile * 128;             // one 64-dim box: 16 rows x 128 B
 constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one tile: 8 KB
 constexpr int kDecStageBytes = 2 * kDecHalf;                // 16 KB
-constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 192 KB
+constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 224 KB
 constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kHeadDim + 2) * 4;
 static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
 constexpr int kDecSmemBytes = 1024 + kDecRingBytes + 2 * kDecStages * 8;
+constexpr int kCombineThreads = kHeadDim;
 
 struct DecodeKParams {
     const uint16_t *q;
@@ -88,14 +91,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int split = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int seq_len =
-        checked_seq_len(p, seq, threadIdx.x == 0 && split == 0 && g == 0);
-    const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
-    const int t0 = split * p.tiles_per_split;
-    const int t1 = min(ntiles, t0 + p.tiles_per_split);
-    if (t0 >= t1) return;  // this split has no tiles of this sequence
-    const int n = t1 - t0;
-
+    // Prologue that touches no memory written by earlier work on the stream.
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
@@ -103,13 +99,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         fence_mbar_init();
     }
+    if (warp == kDecConsumers && lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    const int seq_len = checked_seq_len(p, seq, threadIdx.x == 0 && split == 0 && g == 0);
+    const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
+    const int t0 = split * p.tiles_per_split;
+    const int t1 = min(ntiles, t0 + p.tiles_per_split);
+    if (t0 >= t1) return;  // this split has no tiles of this sequence (CTA-uniform)
+    const int n = t1 - t0;
 
     if (warp == kDecConsumers) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
             const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
             for (int i = 0; i < n; ++i) {
                 const int s = i % kDecStages;
@@ -189,26 +196,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             __syncwarp();
         }
 
-        // S^T (16 tokens x 8 heads) = K (16 x 256) . Q^T (256 x 8)
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T (16 tokens x 8 heads) = K (16 x 256) . Q^T (256 x 8), two chains.
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         {
             const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int uhi = lane >> 4;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                uint32_t a0, a1, a2, a3;
+            for (int kk = 0; kk < 16; kk += 2) {
+                uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
                 ldsm_x4(swz128(kb + (kk >> 2) * kDecChunkBytes, row, (kk & 3) * 2 + uhi), a0,
                         a1, a2, a3);
-                mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                ldsm_x4(swz128(kb + ((kk + 1) >> 2) * kDecChunkBytes, row,
+                               ((kk + 1) & 3) * 2 + uhi),
+                        c0, c1, c2, c3);
+                mma_bf16_16816(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                mma_bf16_16816(sb, c0, c1, c2, c3, qb[kk + 1][0], qb[kk + 1][1]);
             }
         }
 
         // Online softmax over the tile's tokens, per head.
         const bool v0 = r_lo < nvalid, v1 = r_lo + 8 < nvalid;
-        const float x00 = v0 ? sc[0] * p.scale_log2 : -CUDART_INF_F;
-        const float x01 = v0 ? sc[1] * p.scale_log2 : -CUDART_INF_F;
-        const float x10 = v1 ? sc[2] * p.scale_log2 : -CUDART_INF_F;
-        const float x11 = v1 ? sc[3] * p.scale_log2 : -CUDART_INF_F;
+        const float x00 = v0 ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
+        const float x01 = v0 ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
+        const float x10 = v1 ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
+        const float x11 = v1 ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
         float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
@@ -223,15 +234,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float p10 = exp2f(x10 - mu0), p11 = exp2f(x11 - mu1);
         l0 = l0 * al0 + (p00 + p10);
         l1 = l1 * al1 + (p01 + p11);
+        // Rescale the accumulators only when some head's running max moved.
+        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
         m0 = mn0;
         m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < 16; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-        }
 
         // P^T as the B operand: the S^T fragment holds (token, head pair); the 8x8
         // transpose turns it into (head, token pair).  High and low BF16 parts.
@@ -310,24 +324,48 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
 }
 
-// One CTA per (query head, sequence); thread d owns output dim d.
-__global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodeKParams p) {
+__device__ __forceinline__ float block_reduce(float v, float *red, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, sh);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int w = 1; w < kCombineThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    __syncthreads();
+    return r;
+}
+
+// One CTA per (query head, sequence); thread d owns output dim d.  The split weights
+// are computed once into shared memory, then every thread sums its dim over the splits.
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeKParams p) {
+    __shared__ float wsplit[kDecMaxSplits];
+    __shared__ float red[kCombineThreads / 32];
     const int h = blockIdx.x, seq = blockIdx.y, d = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int seq_len = checked_seq_len(p, seq, false);
     const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
     const int nsplit = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
     const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.num_splits;
-    float M = -CUDART_INF_F;
-    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, p.part_ml[base + j].x);
-    float L = 0.f, O = 0.f;
-    if (M != -CUDART_INF_F) {
-        for (int j = 0; j < nsplit; ++j) {
-            const float2 ml = p.part_ml[base + j];
-            const float e = exp2f(ml.x - M);
-            L += e * ml.y;
-            O += e * p.part_o[(base + j) * kHeadDim + d];
-        }
+    float mx = -CUDART_INF_F;
+    for (int j = d; j < nsplit; j += kCombineThreads) mx = fmaxf(mx, p.part_ml[base + j].x);
+    const float M = block_reduce(mx, red, true);
+    float ls = 0.f;
+    for (int j = d; j < nsplit; j += kCombineThreads) {
+        const float2 ml = p.part_ml[base + j];
+        const float e = M == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
+        wsplit[j] = e;
+        ls += e * ml.y;
     }
+    const float L = block_reduce(ls, red, false);  // its barrier also publishes wsplit
+    float O = 0.f;
+    const float *po = p.part_o + base * kHeadDim + d;
+#pragma unroll 8
+    for (int j = 0; j < nsplit; ++j) O += wsplit[j] * po[(int64_t)j * kHeadDim];
     const float r = L > 0.f ? O / L : 0.f;
     const __nv_bfloat16 b = __float2bfloat16_rn(r);
     p.out[((int64_t)seq * p.num_q_heads + h) * kHeadDim + d] =
@@ -349,6 +387,8 @@ DecodePlan plan_decode(int num_seqs, int num_kv_heads, int block_size, int max_s
     if (want < 1) want = 1;
     int tps = (int)((pl.max_tiles + want - 1) / want);
     if (tps < kDecConsumers) tps = kDecConsumers;
+    if ((pl.max_tiles + tps - 1) / tps > kDecMaxSplits)
+        tps = (pl.max_tiles + kDecMaxSplits - 1) / kDecMaxSplits;
     pl.tiles_per_split = tps;
     pl.num_splits = (pl.max_tiles + tps - 1) / tps;
     return pl;
@@ -388,12 +428,12 @@ cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
     p.err = a.err;
     const dim3 grid(plan.num_splits, a.num_kv_heads, a.num_seqs);
     if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
-    decode_split_kernel<<<grid, kDecThreads, kDecSmemBytes, stream>>>(tmap_k, tmap_v, p);
-    e = cudaGetLastError();
+    e = launch_pdl(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream, tmap_k,
+                   tmap_v, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, stream)) != cudaSuccess) return e;
-    decode_combine_kernel<<<dim3(a.num_q_heads, a.num_seqs), kHeadDim, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(decode_combine_kernel, dim3(a.num_q_heads, a.num_seqs),
+                      dim3(kCombineThreads), 0, stream, p);
 }
 
 }  // namespace pa

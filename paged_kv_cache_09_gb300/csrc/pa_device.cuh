@@ -31,6 +31,17 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Wait until the previous grid on the stream has completed and its writes are visible
+// (a no-op when the kernel was launched without programmatic serialization).
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid on the stream to be scheduled (it still waits in pdl_wait()).
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

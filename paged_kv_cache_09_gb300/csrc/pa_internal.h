@@ -13,6 +13,26 @@ namespace pa {
 // later launches (possibly under stream capture) make no attribute call.
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot);
 
+// Launches a kernel with programmatic dependent launch allowed: it may start while the
+// previous kernel on the stream is still running.  Every library kernel calls
+// pdl_wait() before it reads memory that earlier work on the stream may produce, and
+// pdl_trigger() once its own dependents may start their prologue.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ----------------------------------------------------------------- cache write
 cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
                                 const int32_t *block_table, int num_seqs, int64_t bt_stride,
@@ -28,8 +48,14 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
 
 // ----------------------------------------------------------------- decode
 constexpr int kDecTile = 16;       // tokens per pipeline stage (page-local)
-constexpr int kDecStages = 12;     // shared-memory ring depth
-constexpr int kDecConsumers = 4;   // consumer warps per CTA (plus one producer warp)
+constexpr int kDecStages = 14;     // shared-memory ring depth
+constexpr int kDecConsumers = 7;   // consumer warps per CTA (plus one producer warp)
+// Tile i uses stage i % kDecStages and is consumed by warp i % kDecConsumers.  An
+// mbarrier wait only tells the last two phases apart, so every stage must always be
+// consumed by the same warp (which then waits on it in order): the ring depth is a
+// multiple of the consumer count.
+static_assert(kDecStages % kDecConsumers == 0, "stage -> warp mapping must be fixed");
+constexpr int kDecMaxSplits = 1024;  // upper bound on CTAs per (sequence, KV head)
 constexpr int kDecMaxGroup = 8;    // query heads per KV head handled by one MMA column tile
 
 struct DecodePlan {
