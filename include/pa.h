@@ -108,10 +108,15 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  *   seq_lens     int32 [num_seqs], device; each in [1, max_seq_len]
  *   workspace    device scratch of >= pa_decode_workspace_size(...) bytes, 256-byte
  *                aligned; its contents on entry do not matter.
- * Optional fused write of each sequence's newest token (config of a serving step):
- * when new_k, new_v and new_slots are all non-NULL, new_k / new_v ([num_seqs, Hkv, D])
- * are first written at new_slots (int64 [num_seqs]) exactly as pa_reshape_and_cache
- * does, and the attention then includes them.  Pass all three NULL to skip.
+ * Optional fused write of each sequence's newest token (a serving step): when new_k,
+ * new_v and new_slots are all non-NULL, the token being decoded -- position
+ * seq_lens[s] - 1 of sequence s -- is written into the caches from new_k / new_v
+ * ([num_seqs, Hkv, D]) at new_slots[s] (int64 [num_seqs], as pa_slot_mapping gives it),
+ * bit for bit as pa_reshape_and_cache would, and the attention includes it.  The
+ * write happens inside the decode kernel, by the CTA that reads that token's tile, just
+ * before it loads the tile.  A negative new_slots[s] is skipped (padding).  A slot that
+ * is not the one the block table gives for position seq_lens[s] - 1 is not written and
+ * sets PA_DEVERR_SLOT.  Pass all three NULL to skip.
  * The split-context kernel processes page-local tiles of 16 tokens, so any block_size
  * works (784 leaves a 16-token tail tile per page, 832 does not).
  */

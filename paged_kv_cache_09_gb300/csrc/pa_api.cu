@@ -293,14 +293,13 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
         return PA_ERR_CUDA;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (nfused == 3) {
-        cudaError_t e = pa::launch_reshape_and_cache(
-            new_k, new_v, const_cast<pa_bf16 *>(k_cache), const_cast<pa_bf16 *>(v_cache),
-            page_stride, num_pages, new_slots, num_seqs, num_kv_heads * head_dim, block_size,
-            dev.err, st);
-        if (e != cudaSuccess) return PA_ERR_CUDA;
-    }
     pa::DecodeArgs a;
+    a.k_cache_w = nfused == 3 ? const_cast<pa_bf16 *>(k_cache) : nullptr;
+    a.v_cache_w = nfused == 3 ? const_cast<pa_bf16 *>(v_cache) : nullptr;
+    a.new_k = nfused == 3 ? new_k : nullptr;
+    a.new_v = nfused == 3 ? new_v : nullptr;
+    a.new_slots = nfused == 3 ? new_slots : nullptr;
+    a.page_stride = page_stride;
     a.q = q;
     a.block_table = block_table;
     a.bt_stride = bt_stride;

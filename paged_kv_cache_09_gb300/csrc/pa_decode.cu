@@ -37,7 +37,7 @@ constexpr int kDecStageBytes = 2 * kDecHalf;                // 16 KB
 constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 224 KB
 constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kHeadDim + 2) * 4;
 static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
-constexpr int kDecSmemBytes = 1024 + kDecRingBytes + 2 * kDecStages * 8;
+constexpr int kDecSmemBytes = 1024 + kDecRingBytes + (2 * kDecStages + 1) * 8;
 constexpr int kCombineThreads = kHeadDim;
 
 struct DecodeKParams {
@@ -58,7 +58,45 @@ struct DecodeKParams {
     float2 *part_ml;    // [S, Hq, splits] (running max in base-2 units, sum of weights)
     uint16_t *out;
     unsigned *err;
+    // Fused write of the token being decoded (new_slots == nullptr: none).
+    uint16_t *k_cache_w, *v_cache_w;
+    const uint16_t *new_k, *new_v;   // [S, Hkv, D]
+    const int64_t *new_slots;        // [S]
+    int64_t page_stride;
+    int num_kv_heads;
 };
+
+// Fused write of the token being decoded, done by one consumer warp of the CTA that owns
+// sequence `seq`'s last tile as soon as the CTA starts: each lane copies 16 bytes of
+// the K row and 16 of the V row of KV head g, every lane fences its stores against the
+// async proxy, and after the warp has converged lane 0 arrives on `written`.  The
+// producer waits on `written` before it issues the TMA load of that last tile.  Only a
+// slot that matches the block table's slot for position seq_len - 1 is written.
+__device__ __forceinline__ void write_newest_token(const DecodeKParams &p, const int32_t *bt,
+                                                   int seq, int g, int seq_len, int lane,
+                                                   uint64_t *written) {
+    const int64_t slot = p.new_slots[seq];
+    const int pos = seq_len - 1;
+    const int lp = pos / p.block_size;
+    const int off = pos - lp * p.block_size;
+    const int page = bt[lp];
+    if (slot >= 0) {  // a negative slot is padding
+        if (page >= 0 && page < p.num_pages && slot == (int64_t)page * p.block_size + off) {
+            const int64_t src = ((int64_t)seq * p.num_kv_heads + g) * kHeadDim;
+            const int64_t dst =
+                page * p.page_stride + ((int64_t)off * p.num_kv_heads + g) * kHeadDim;
+            const uint4 k = reinterpret_cast<const uint4 *>(p.new_k + src)[lane];
+            const uint4 v = reinterpret_cast<const uint4 *>(p.new_v + src)[lane];
+            reinterpret_cast<uint4 *>(p.k_cache_w + dst)[lane] = k;
+            reinterpret_cast<uint4 *>(p.v_cache_w + dst)[lane] = v;
+        } else if (lane == 0) {
+            atomicOr(p.err, kErrSlot);
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(written);
+}
 
 __device__ __forceinline__ int seq_tiles(int seq_len, int block_size, int tiles_per_page) {
     const int full = seq_len / block_size;
@@ -87,6 +125,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecRingBytes);
     uint64_t *empty = full + kDecStages;
+    uint64_t *written = empty + kDecStages;  // the fused write of the newest token is done
 
     const int split = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,6 +136,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(written, 1);
         fence_mbar_init();
     }
     if (warp == kDecConsumers && lane == 0) {
@@ -113,11 +153,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int t1 = min(ntiles, t0 + p.tiles_per_split);
     if (t0 >= t1) return;  // this split has no tiles of this sequence (CTA-uniform)
     const int n = t1 - t0;
+    const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
+    // This CTA holds the tile of the token being decoded and has to write that token.
+    const bool writes_newest = p.new_slots != nullptr && t1 == ntiles;
 
     if (warp == kDecConsumers) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
             for (int i = 0; i < n; ++i) {
                 const int s = i % kDecStages;
                 if (i >= kDecStages &&
@@ -126,6 +168,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 const int j = t0 + i;
                 const int lp = j / p.tiles_per_page;
                 const int off = (j - lp * p.tiles_per_page) * kDecTile;
+                // The last tile holds the token being decoded: wait until it is written.
+                if (writes_newest && i == n - 1 && !mbar_wait(written, 0, p.err)) break;
                 const int page = bt[lp];
                 // A page outside the pool is reported; the TMA box then lies outside the
                 // tensor and reads as zeros, so nothing faults.
@@ -145,6 +189,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
 
     // ---------------------------------------------------------------- consumers
+    if (writes_newest && warp == kDecConsumers - 1)
+        write_newest_token(p, bt, seq, g, seq_len, lane, written);
+
     // Q^T as the B operand: lane holds head n = lane/4 and dims 2(lane%4)+{0,1} (+8)
     // of every 16-dim k-step.  Heads past the group are zero columns.
     const int nh = lane >> 2;
@@ -339,12 +386,17 @@ __device__ __forceinline__ float block_reduce(float v, float *red, bool is_max) 
     return r;
 }
 
-// One CTA per (query head, sequence); thread d owns output dim d.  The split weights
-// are computed once into shared memory, then every thread sums its dim over the splits.
+// One CTA per (query head, sequence).  The split weights exp2(m_j - M) are computed once
+// into shared memory; then warp w sums splits w, w+8, ... with each lane owning 8
+// consecutive dims (two 16-byte loads per split, all issued together), and the eight
+// warp sums are added through shared memory.
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeKParams p) {
+    constexpr int kWarps = kCombineThreads / 32;
     __shared__ float wsplit[kDecMaxSplits];
     __shared__ float red[kCombineThreads / 32];
-    const int h = blockIdx.x, seq = blockIdx.y, d = threadIdx.x;
+    __shared__ __align__(16) float part[kWarps][kHeadDim];
+    const int h = blockIdx.x, seq = blockIdx.y, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     pdl_wait();
     pdl_trigger();
     const int seq_len = checked_seq_len(p, seq, false);
@@ -352,23 +404,35 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     const int nsplit = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
     const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.num_splits;
     float mx = -CUDART_INF_F;
-    for (int j = d; j < nsplit; j += kCombineThreads) mx = fmaxf(mx, p.part_ml[base + j].x);
+    for (int j = tid; j < nsplit; j += kCombineThreads) mx = fmaxf(mx, p.part_ml[base + j].x);
     const float M = block_reduce(mx, red, true);
     float ls = 0.f;
-    for (int j = d; j < nsplit; j += kCombineThreads) {
+    for (int j = tid; j < nsplit; j += kCombineThreads) {
         const float2 ml = p.part_ml[base + j];
         const float e = M == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
         wsplit[j] = e;
         ls += e * ml.y;
     }
     const float L = block_reduce(ls, red, false);  // its barrier also publishes wsplit
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float4 *po = reinterpret_cast<const float4 *>(p.part_o + base * kHeadDim) + lane * 2;
+#pragma unroll 4
+    for (int j = warp; j < nsplit; j += kWarps) {
+        const float w = wsplit[j];
+        const float4 a = po[(int64_t)j * (kHeadDim / 4)];
+        const float4 b = po[(int64_t)j * (kHeadDim / 4) + 1];
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+    reinterpret_cast<float4 *>(&part[warp][lane * 8])[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4 *>(&part[warp][lane * 8])[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncthreads();
     float O = 0.f;
-    const float *po = p.part_o + base * kHeadDim + d;
-#pragma unroll 8
-    for (int j = 0; j < nsplit; ++j) O += wsplit[j] * po[(int64_t)j * kHeadDim];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) O += part[w][tid];
     const float r = L > 0.f ? O / L : 0.f;
     const __nv_bfloat16 b = __float2bfloat16_rn(r);
-    p.out[((int64_t)seq * p.num_q_heads + h) * kHeadDim + d] =
+    p.out[((int64_t)seq * p.num_q_heads + h) * kHeadDim + tid] =
         *reinterpret_cast<const uint16_t *>(&b);
 }
 
@@ -426,6 +490,13 @@ cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
     p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(a.workspace) + o_bytes);
     p.out = a.out;
     p.err = a.err;
+    p.k_cache_w = a.k_cache_w;
+    p.v_cache_w = a.v_cache_w;
+    p.new_k = a.new_k;
+    p.new_v = a.new_v;
+    p.new_slots = a.new_slots;
+    p.page_stride = a.page_stride;
+    p.num_kv_heads = a.num_kv_heads;
     const dim3 grid(plan.num_splits, a.num_kv_heads, a.num_seqs);
     if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
     e = launch_pdl(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream, tmap_k,

@@ -83,6 +83,11 @@ struct DecodeArgs {
     void *workspace;
     unsigned *err;
     cudaEvent_t ev_start, ev_stop;  // optional: recorded around the split kernel
+    // Optional fused write of each sequence's newest token (all NULL when unused).
+    uint16_t *k_cache_w, *v_cache_w;
+    const uint16_t *new_k, *new_v;
+    const int64_t *new_slots;
+    int64_t page_stride;            // elements between consecutive pages
 };
 
 cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,

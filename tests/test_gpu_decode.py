@@ -190,3 +190,29 @@ def test_decode_workspace_too_small_is_rejected(cuda_lib):
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(pa.PAError):
         _gpu_decode(pa, case, workspace=ws)
+
+
+def test_fused_write_checks_the_slot_of_the_newest_token(cuda_lib):
+    # The fused write only lands at the slot the block table gives for position
+    # seq_len - 1; any other slot is refused (error bit, nothing written), and a negative
+    # slot is padding.
+    pa = cuda_lib
+    case = workloads.paged_case(71, [900, 1500], 832, 8, new_tokens=1, device="cuda")
+    good = pa.slot_mapping(case.positions, case.block_table, 832, seq_idx=case.seq_idx)
+    bad = good.clone()
+    bad[0] += 1                       # one slot too far for sequence 0
+    bad[1] = -1                       # sequence 1: padding, skipped
+    before = bits(case.k_cache).copy()
+    pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
+              1500, new_k=case.new_k, new_v=case.new_v, new_slots=bad)
+    torch.cuda.synchronize()
+    assert pa.device_errors() == pa.DEVERR_SLOT
+    assert np.array_equal(bits(case.k_cache), before)      # nothing was written
+    pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
+              1500, new_k=case.new_k, new_v=case.new_v, new_slots=good)
+    torch.cuda.synchronize()
+    assert pa.device_errors() == 0
+    k_ref, v_ref = before.copy(), bits(case.v_cache).copy()
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_ref, v_ref,
+                             good.cpu().numpy(), 832)
+    assert np.array_equal(bits(case.k_cache), k_ref)
