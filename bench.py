@@ -499,7 +499,8 @@ def main():
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 4 * args.steps,
+        # per step: slot mapping, split decode (with the fused KV write), LSE combine
+        "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": kernel_gbs / peaks["hbm_gbs"] if kernel_gbs else None,
                      "traffic": None,

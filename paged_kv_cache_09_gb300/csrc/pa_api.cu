@@ -197,7 +197,7 @@ const char *pa_build_info(void) {
     std::call_once(once, [] {
         snprintf(buf, sizeof buf,
                  "paged_kv_cache_09_gb300: sm_103a; decode tile %d x %d stages, %d consumer "
-                 "warps; prefill %dx%d mma tiles; nvcc %d.%d",
+                 "warps; prefill %dx%d tcgen05 tiles; nvcc %d.%d",
                  pa::kDecTile, pa::kDecStages, pa::kDecConsumers, pa::kPfQRows, pa::kPfKvTile,
                  __CUDACC_VER_MAJOR__, __CUDACC_VER_MINOR__);
     });
@@ -346,15 +346,16 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
     CUtensorMap maps[5];
     if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, q_len, pa::kPfQRows) ||
         !make_cache_map(&maps[1], k_cache, head_dim, num_kv_heads, block_size, num_pages,
-                        page_stride, pa::kPfKvTile) ||
+                        page_stride, pa::kPfBlock) ||
         !make_cache_map(&maps[2], v_cache, head_dim, num_kv_heads, block_size, num_pages,
-                        page_stride, pa::kPfKvTile) ||
+                        page_stride, pa::kPfBlock) ||
         !make_cache_map(&maps[3], k_cache, head_dim, num_kv_heads, last_rows, num_pages,
-                        page_stride, pa::kPfKvTile) ||
+                        page_stride, pa::kPfBlock) ||
         !make_cache_map(&maps[4], v_cache, head_dim, num_kv_heads, last_rows, num_pages,
-                        page_stride, pa::kPfKvTile))
+                        page_stride, pa::kPfBlock))
         return PA_ERR_CUDA;
     pa::PrefillArgs a;
+    a.q = q;
     a.block_table = block_table;
     a.q_len = q_len;
     a.q_start = q_start;
@@ -368,6 +369,7 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
     a.scale = scale;
     a.out = out;
     a.err = dev.err;
+    a.num_sms = dev.num_sms;
     take_kernel_events(&a.ev_start, &a.ev_stop);
     if (diag_enabled())
         fprintf(stderr, "[pa] prefill: q_len=%d q_start=%d causal=%d bs=%d q_tiles=%d\n", q_len,

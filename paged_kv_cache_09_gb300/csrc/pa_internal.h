@@ -94,11 +94,13 @@ cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
 
 // ----------------------------------------------------------------- prefill
-constexpr int kPfQRows = 64;       // query rows per CTA (16 per consumer warp)
-constexpr int kPfKvTile = 64;      // keys per pipeline stage (page-local)
-constexpr int kPfStages = 2;
+constexpr int kPfQRows = 128;      // query rows per work item (one TMEM lane each)
+constexpr int kPfKvTile = 256;     // keys per K/V tile: four page-local blocks
+constexpr int kPfBlock = 64;       // keys per TMA box (one page-local block)
+constexpr int kPfRing = 5;         // 32 KB K/V unit slots in the shared-memory ring
 
 struct PrefillArgs {
+    const uint16_t *q;    // [q_len, Hq, D]
     const int32_t *block_table;
     int q_len, q_start, causal;
     int num_q_heads, num_kv_heads, group;
@@ -109,6 +111,7 @@ struct PrefillArgs {
     uint16_t *out;
     unsigned *err;
     cudaEvent_t ev_start, ev_stop;  // optional: recorded around the prefill kernel
+    int num_sms;                    // persistent grid size bound
 };
 
 // tmaps: Q, K, V, K of the last page, V of the last page.

@@ -1,18 +1,44 @@
-// pa_prefill.cu -- chunked-prefill attention of one sequence over its paged cache.
+// pa_prefill.cu -- chunked-prefill attention of one sequence over its paged cache, on
+// the tcgen05 tensor cores with TMEM accumulators.
 //
 // What is computed (page832 post §6): query row i of the chunk sits at absolute
 // position q_start + i and, with causal masking, attends to keys 0..q_start+i of the
 // same sequence (earlier chunks and the chunk itself, already written to the cache);
 // without it, to all q_start + q_len keys.  K/V are read through the block table
-// (page832 §1) in page-local 64-token tiles.
+// (page832 §1) in page-local blocks of 64 keys; four blocks form a 256-key tile.
 //
-// Kernel shape: one CTA per (64-row query tile, query head); the longest (latest)
-// query tiles are launched first.  A producer warp loads the query tile once and
-// streams K/V tiles with TMA into a 2-stage ring.  Keys of the sequence's last page
-// are read through tensor maps whose row extent ends at the sequence's last token, so
-// rows past it arrive as zeros (never stale or NaN data).  Four consumer warps each own
-// 16 query rows: S = Q K^T and O += P V on mma.m16n8k16 tensor-core tiles, online
-// softmax in registers, fp32 accumulation, BF16 output.
+// Shape choices.  A tcgen05.mma with M=128 and K=16 occupies the tensor core for about
+// the same time for any N up to 256, so every MMA here has N = 256: S = Q K^T runs over
+// 256 keys at a time, and O += P V covers all 256 output dims in one MMA per 16 keys.
+// With O (256 columns) and S (256 columns) TMEM is full, so S is single-buffered.  To
+// keep the tensor core busy while the softmax runs, P is handed over in 64-key quarters:
+// the PV of quarter q runs while the softmax of quarter q+1 is computed, and the tensor
+// core only waits for the softmax of each tile's first quarter.
+//
+// Work item = (128 query rows of one head).  Persistent CTAs, one per SM, walk the items
+// longest first in a snake order (item k of CTA b: k*G + b for even k, k*G + G-1-b for
+// odd k), which evens out the causal imbalance between early and late query rows.
+//
+// Warp roles (192 threads):
+//   warp 0    TMA producer: the item's Q tile (4 boxes of 64 dims x 128 rows, 64 KB),
+//             then per tile four K units (one 64-dim chunk x 256 keys, 32 KB each) and
+//             four V units (64 keys x 256 dims) into a 5-slot ring of 32 KB.  Boxes are
+//             64 keys of one page; keys of the sequence's last page come through tensor
+//             maps cut at the last token, so rows past it (and past a page end) are zeros.
+//   warp 1    MMA issuer (one thread) and TMEM owner: S = Q K^T (A, B K-major in shared
+//             memory), then O += P V per 64-key quarter (A = P from TMEM, B = V unit
+//             MN-major, 8 KB between 64-dim atoms).
+//   warps 2-5 thread t owns query row t (TMEM lane t).  Per quarter it reads 64 S
+//             values, masks (page end, sequence end, causal) where the quarter needs it,
+//             keeps a running max that moves only when it grows by more than 8 (log2
+//             units; then its O row is rescaled in TMEM), and writes P = P_hi + P_lo (two
+//             BF16 parts, so that P keeps ~16 significant bits) over that quarter of S.
+//             At the end it normalises O and stores BF16.
+// TMEM columns: O [0, 256), S [256, 512); P of quarter q: hi at 256+64q, lo at +32.
+//
+// Every wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT, flags the CTA to
+// stop, and the CTA drains its tensor-core work and frees TMEM before it returns.
+#include <float.h>
 #include <math_constants.h>
 
 #include "pa_device.cuh"
@@ -22,254 +48,446 @@ namespace pa {
 
 namespace {
 
-constexpr int kPfConsumers = kPfQRows / 16;
-constexpr int kPfThreads = (kPfConsumers + 1) * 32;
-constexpr int kPfQChunk = kPfQRows * 128;       // one 64-dim box of the query tile
-constexpr int kPfQBytes = kChunks * kPfQChunk;  // 32 KB
-constexpr int kPfKvChunk = kPfKvTile * 128;
-constexpr int kPfHalf = kChunks * kPfKvChunk;   // K (or V) of one tile: 32 KB
-constexpr int kPfStageBytes = 2 * kPfHalf;
-constexpr int kPfSmemBytes = 1024 + kPfQBytes + kPfStages * kPfStageBytes + 64;
+constexpr int kBM = kPfQRows;                 // 128 query rows
+constexpr int kBN = kPfKvTile;                // 256 keys per tile
+constexpr int kBlk = 64;                      // keys per TMA box (page-local block)
+constexpr int kBlkBytes = kBlk * 128;         // one box: 64 rows x 128 B = 8 KB
+constexpr int kUnit = 4 * kBlkBytes;          // 32 KB ring slot
+constexpr int kQChunk = kBM * 128;            // 64 dims x 128 rows: 16 KB
+constexpr int kQBytes = kChunks * kQChunk;    // 64 KB
+constexpr int kRing = kPfRing;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 256;
+static_assert(kBN == 4 * kBlk && kBN == 256, "tile = four 64-key blocks");
 
-struct PfKParams {
+// Shared memory (offsets from the 1024-byte-aligned base).
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kQBytes;
+constexpr int kOffBars = kOffRing + kRing * kUnit;
+enum Bar {
+    kRingFull = 0,
+    kRingEmpty = kRingFull + kRing,
+    kQFull = kRingEmpty + kRing,
+    kQEmpty,
+    kSFull,
+    kPFull,               // [4] quarters
+    kPvDone = kPFull + 4, // [4] quarters
+    kOEmpty = kPvDone + 4,
+    kDrain,
+    kNumBars
+};
+constexpr int kSmemBytes = 1024 + kOffBars + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct TcParams {
     const int32_t *block_table;
     int q_len, q_start, causal, seq_len_k;
     int num_q_heads, group;
-    int block_size, tiles_per_page, last_page, num_q_tiles;
+    int block_size, blocks_per_page, last_page, num_q_tiles, num_items;
     int64_t num_pages;
-    float scale_log2;
+    float sc;             // |scale| * log2(e), at least FLT_MIN
+    int neg;              // scale < 0
     uint16_t *out;
     unsigned *err;
 };
 
-struct PfMaps {
+struct TcMaps {
     CUtensorMap q, k, v, k_last, v_last;
 };
 
-__global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_kernel(const __grid_constant__ PfMaps maps, const PfKParams p) {
+struct Item {
+    int h, g, r0, rows, nblocks, n;  // head, KV head, first row, rows present, blocks, tiles
+};
+
+__device__ __forceinline__ bool item_of(const TcParams &p, int k, Item &it) {
+    const int G = gridDim.x, b = blockIdx.x;
+    const int idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
+    if (idx >= p.num_items) return false;
+    const int qt = p.num_q_tiles - 1 - idx / p.num_q_heads;
+    it.h = idx % p.num_q_heads;
+    it.g = it.h / p.group;
+    it.r0 = qt * kBM;
+    it.rows = min(kBM, p.q_len - it.r0);
+    const int nkeys = p.causal ? p.q_start + it.r0 + it.rows : p.seq_len_k;
+    const int full = nkeys / p.block_size;
+    const int rem = nkeys - full * p.block_size;
+    it.nblocks = full * p.blocks_per_page + (rem + kBlk - 1) / kBlk;
+    it.n = (it.nblocks + 3) / 4;
+    return true;
+}
+
+// Bounded wait that also gives up at once when another role of the CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, unsigned *err,
+                                              volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qs = smem;
-    uint8_t *ring = smem + kPfQBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kPfStages * kPfStageBytes);
-    uint64_t *qbar = bars;
-    uint64_t *full = bars + 1;
-    uint64_t *empty = full + kPfStages;
+    uint8_t *qs = smem + kOffQ;
+    uint8_t *ring = smem + kOffRing;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    const int qt = p.num_q_tiles - 1 - blockIdx.x;  // latest rows (most keys) first
-    const int h = blockIdx.y;
-    const int g = h / p.group;
-    const int row0 = qt * kPfQRows;
-    const int rows_here = min(kPfQRows, p.q_len - row0);
-    const int nkeys = p.causal ? p.q_start + row0 + rows_here : p.seq_len_k;
-    const int full_pages = nkeys / p.block_size;
-    const int rem = nkeys - full_pages * p.block_size;
-    const int ntiles = full_pages * p.tiles_per_page + (rem + kPfKvTile - 1) / kPfKvTile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // ---------------------------------------------------------------- prologue
     if (threadIdx.x == 0) {
-        mbar_init(qbar, 1);
-        for (int s = 0; s < kPfStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kPfConsumers);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&bars[kRingFull + i], 1);
+            mbar_init(&bars[kRingEmpty + i], 1);
         }
+        mbar_init(&bars[kQFull], 1);
+        mbar_init(&bars[kQEmpty], 1);
+        mbar_init(&bars[kSFull], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&bars[kPFull + i], 128);
+            mbar_init(&bars[kPvDone + i], 1);
+        }
+        mbar_init(&bars[kOEmpty], 128);
+        mbar_init(&bars[kDrain], 1);
+        *abort = 0;
         fence_mbar_init();
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(&maps.v);
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
 
-    if (warp == kPfConsumers) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(qbar, kPfQBytes);
+            uint32_t u = 0;
+            Item it;
+            bool stop = false;
+            for (int k = 0; !stop && item_of(p, k, it); ++k) {
+                if (k > 0 && !wait_or_abort(&bars[kQEmpty], (k - 1) & 1, p.err, abort)) break;
+                mbar_arrive_expect_tx(&bars[kQFull], kQBytes);
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                tma_load_3d(qs + c * kPfQChunk, &maps.q, qbar, c * kChunkElems, h, row0);
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % kPfStages;
-                if (i >= kPfStages && !mbar_wait(&empty[s], ((i / kPfStages) - 1) & 1, p.err))
-                    break;
-                const int lp = i / p.tiles_per_page;
-                const int off = (i - lp * p.tiles_per_page) * kPfKvTile;
-                const int page = p.block_table[lp];
-                if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrPage);
-                const CUtensorMap *mk = lp == p.last_page ? &maps.k_last : &maps.k;
-                const CUtensorMap *mv = lp == p.last_page ? &maps.v_last : &maps.v;
-                uint8_t *st = ring + s * kPfStageBytes;
-                mbar_arrive_expect_tx(&full[s], kPfStageBytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(qs + c * kQChunk, &maps.q, &bars[kQFull], c * kChunkElems, it.h,
+                                it.r0);
+                for (int j = 0; j < it.n && !stop; ++j) {
+                    // Page, offset and map of each of the tile's four blocks; blocks past the
+                    // item's last are read from outside the pool (zeros) and masked.
+                    int pg[4], of[4];
+                    const CUtensorMap *mk[4], *mv[4];
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    tma_load_4d(st + c * kPfKvChunk, mk, &full[s], c * kChunkElems, g, off, page);
-                    tma_load_4d(st + kPfHalf + c * kPfKvChunk, mv, &full[s], c * kChunkElems, g,
-                                off, page);
+                    for (int bb = 0; bb < 4; ++bb) {
+                        const int kb = 4 * j + bb;
+                        const int lp = kb / p.blocks_per_page;
+                        of[bb] = (kb - lp * p.blocks_per_page) * kBlk;
+                        if (kb < it.nblocks) {
+                            pg[bb] = p.block_table[lp];
+                            if (pg[bb] < 0 || pg[bb] >= p.num_pages) atomicOr(p.err, kErrPage);
+                            mk[bb] = lp == p.last_page ? &maps.k_last : &maps.k;
+                            mv[bb] = lp == p.last_page ? &maps.v_last : &maps.v;
+                        } else {
+                            pg[bb] = (int)p.num_pages;
+                            of[bb] = 0;
+                            mk[bb] = &maps.k;
+                            mv[bb] = &maps.v;
+                        }
+                    }
+                    // 4 K units (dim chunk c: the four blocks stacked), then 4 V units
+                    // (block bb: the four dim chunks side by side).
+                    for (int x = 0; x < 8; ++x, ++u) {
+                        const int s = u % kRing;
+                        if (u >= kRing &&
+                            !wait_or_abort(&bars[kRingEmpty + s], ((u / kRing) - 1) & 1, p.err,
+                                           abort)) {
+                            stop = true;
+                            break;
+                        }
+                        uint8_t *dst = ring + s * kUnit;
+                        mbar_arrive_expect_tx(&bars[kRingFull + s], kUnit);
+                        if (x < 4) {
+#pragma unroll
+                            for (int bb = 0; bb < 4; ++bb)
+                                tma_load_4d(dst + bb * kBlkBytes, mk[bb], &bars[kRingFull + s],
+                                            x * kChunkElems, it.g, of[bb], pg[bb]);
+                        } else {
+                            const int bb = x - 4;
+#pragma unroll
+                            for (int c = 0; c < kChunks; ++c)
+                                tma_load_4d(dst + c * kBlkBytes, mv[bb], &bars[kRingFull + s],
+                                            c * kChunkElems, it.g, of[bb], pg[bb]);
+                        }
+                    }
                 }
             }
         }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    const int wr = warp * 16;                // this warp's rows within the tile
-    const int ra = lane >> 2;                // fragment rows ra and ra + 8
-    const int qpos_a = p.q_start + row0 + wr + ra;
-    const int qpos_b = qpos_a + 8;
-    const uint32_t qbase = smem_u32(qs);
-    const uint32_t rbase = smem_u32(ring);
-
-    float o[32][4];
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = umma_idesc_bf16(kBM, kBN, 0, 0);
+            constexpr uint32_t kIdPV = umma_idesc_bf16(kBM, kHeadDim, 0, 1);
+            const uint32_t q_addr = smem_u32(qs), ring_addr = smem_u32(ring);
+            const uint32_t sbuf = tmem + kColS, obuf = tmem + kColO;
+            uint32_t u = 0, jt = 0;
+            Item it;
+            bool stop = false;
+            for (int k = 0; !stop && item_of(p, k, it); ++k) {
+                if (!wait_or_abort(&bars[kQFull], k & 1, p.err, abort)) break;
+                tc_fence_after();
+                for (int j = 0; j < it.n && !stop; ++j) {
+                    // S = Q K^T over the tile's 256 keys.
+                    for (int c = 0; c < kChunks; ++c, ++u) {
+                        const int s = u % kRing;
+                        if (!wait_or_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-    for (int nt = 0; nt < 32; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F, l_a = 0.f, l_b = 0.f;
-
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, p.err));
-    for (int i = 0; ok && i < ntiles; ++i) {
-        const int s = i % kPfStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kPfStages) & 1, p.err))) break;
-        const int lp = i / p.tiles_per_page;
-        const int off = (i - lp * p.tiles_per_page) * kPfKvTile;
-        const int tok0 = lp * p.block_size + off;
-        const uint32_t kb = rbase + s * kPfStageBytes;
-        const uint32_t vb = kb + kPfHalf;
-
-        // S (16 rows x 64 keys) = Q (16 x 256) . K^T (256 x 64)
-        float sacc[8][4];
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            umma_ss(sbuf, umma_sdesc_sw128(q_addr + c * kQChunk + k4 * 32),
+                                    umma_sdesc_sw128(ring_addr + s * kUnit + k4 * 32), kIdQK,
+                                    (c | k4) != 0);
+                        umma_commit(&bars[kRingEmpty + s]);
+                    }
+                    if (stop) break;
+                    if (j == it.n - 1) umma_commit(&bars[kQEmpty]);
+                    umma_commit(&bars[kSFull]);
+                    // O += P V, one 64-key quarter (one V unit) at a time.
+                    for (int qq = 0; qq < 4; ++qq, ++u) {
+                        if (!wait_or_abort(&bars[kPFull + qq], (jt + j) & 1, p.err, abort)) {
+                            stop = true;
+                            break;
+                        }
+                        if (j == 0 && qq == 0 && k > 0 &&
+                            !wait_or_abort(&bars[kOEmpty], (k - 1) & 1, p.err, abort)) {
+                            stop = true;
+                            break;
+                        }
+                        const int s = u % kRing;
+                        if (!wait_or_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t phi = sbuf + 64 * qq;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const int c = kk >> 2;
-            const int u0 = (kk & 3) * 2;
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(swz128(qbase + c * kPfQChunk, wr + (lane & 7) + ((lane >> 3) & 1) * 8,
-                           u0 + (lane >> 4)),
-                    a0, a1, a2, a3);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(swz128(kb + c * kPfKvChunk, np * 16 + (lane & 7) + (lane >> 4) * 8,
-                               u0 + ((lane >> 3) & 1)),
-                        b0, b1, b2, b3);
-                mma_bf16_16816(sacc[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(sacc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                        for (int ks = 0; ks < kBlk / 16; ++ks) {
+                            const uint64_t vd =
+                                umma_sdesc_sw128(ring_addr + s * kUnit + ks * 2048, kBlkBytes);
+                            umma_ts(obuf, phi + 8 * ks, vd, kIdPV, (j | qq | ks) != 0);
+                            umma_ts(obuf, phi + 32 + 8 * ks, vd, kIdPV, 1);
+                        }
+                        umma_commit(&bars[kRingEmpty + s]);
+                        umma_commit(&bars[kPvDone + qq]);
+                    }
+                }
+                jt += it.n;
             }
+            // Drain: every tensor-core operation issued by this thread is complete before
+            // the CTA frees TMEM.
+            umma_commit(&bars[kDrain]);
+            mbar_wait(&bars[kDrain], 0, p.err);
         }
-
-        // Mask (page tail, sequence end, causal) and online softmax per row.
-        float mx_a = -CUDART_INF_F, mx_b = -CUDART_INF_F;
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t obase = tmem + lane_off + kColO;
+        const uint32_t sbase = tmem + lane_off + kColS;
+        uint32_t jt = 0;
+        Item it;
+        bool stop = false;
+        for (int k = 0; !stop && item_of(p, k, it); ++k) {
+            const int qpos = p.q_start + it.r0 + row;
+            float m_used = -CUDART_INF_F, l = 0.f;
+            for (int j = 0; j < it.n && !stop; ++j) {
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(&bars[kSFull], (jt + j) & 1, p.err, abort))) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
+                for (int qq = 0; qq < 4; ++qq) {
+                    float x[64];
+                    {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(sbase + 64 * qq, r0);
+                        tmem_ld32(sbase + 64 * qq + 32, r1);
+                        tc_wait_ld();
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+                        for (int i = 0; i < 32; ++i) {
+                            x[i] = __uint_as_float(r0[i]);
+                            x[32 + i] = __uint_as_float(r1[i]);
+                        }
+                    }
+                    if (p.neg) {  // a negative scale reverses the order of the raw scores
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = nt * 8 + (lane & 3) * 2 + (e & 1);
-                const int t = tok0 + col;
-                const int qpos = (e >> 1) ? qpos_b : qpos_a;
-                const bool valid = (off + col < p.block_size) && (t < p.seq_len_k) &&
-                                   (!p.causal || t <= qpos);
-                const float x = valid ? sacc[nt][e] * p.scale_log2 : -CUDART_INF_F;
-                sacc[nt][e] = x;
-                if (e >> 1) mx_b = fmaxf(mx_b, x); else mx_a = fmaxf(mx_a, x);
+                        for (int i = 0; i < 64; ++i) x[i] = -x[i];
+                    }
+                    // The quarter is one 64-key block; its valid keys form a prefix [0, lim).
+                    // Only quarters with a page tail, the sequence end or the causal
+                    // diagonal in them need the mask.
+                    const int kb = 4 * j + qq;
+                    int lim = 0;
+                    if (kb < it.nblocks) {
+                        const int lp = kb / p.blocks_per_page;
+                        const int off = (kb - lp * p.blocks_per_page) * kBlk;
+                        const int tok0 = lp * p.block_size + off;
+                        lim = min(kBlk, min(p.block_size - off, p.seq_len_k - tok0));
+                        if (p.causal) lim = min(lim, qpos - tok0 + 1);
+                    }
+                    if (!__all_sync(0xffffffffu, lim >= kBlk)) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) x[i] = i < lim ? x[i] : -CUDART_INF_F;
+                    }
+                    float mp[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mp[i] = fmaxf(fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24])),
+                                      fmaxf(fmaxf(x[i + 32], x[i + 40]), fmaxf(x[i + 48], x[i + 56])));
+                    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) *
+                                     p.sc;
+                    const float m_new = fmaxf(m_used, mx);
+                    const bool need = m_new > m_used + 8.f;  // also true for the first finite max
+                    const float alpha =
+                        !need ? 1.f
+                              : (m_used == -CUDART_INF_F ? 0.f : ex2_approx(m_used - m_new));
+                    if (need) {
+                        l *= alpha;
+                        m_used = m_new;
+                    }
+                    const float nmu = m_used == -CUDART_INF_F ? 0.f : -m_used;
+                    float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = ex2_approx(fmaf(x[32 * c + 2 * i], p.sc, nmu));
+                            const float p1 = ex2_approx(fmaf(x[32 * c + 2 * i + 1], p.sc, nmu));
+                            sp[i & 7] += p0 + p1;
+                            hi[i] = pack_bf16x2(p0, p1);
+                            lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+                        }
+                        tmem_st16(sbase + 64 * qq + 16 * c, hi);
+                        tmem_st16(sbase + 64 * qq + 32 + 16 * c, lo);
+                    }
+                    l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+                    // Moving the running max rescales this row of O, which the PVs of the
+                    // tile's earlier quarters may still be accumulating: wait for them first
+                    // (their completion covers every earlier tensor op).  At quarter 0 no
+                    // wait is needed: S_j being ready means every tensor op issued before
+                    // QK_j has completed.  Either way the parity wait is never two phases
+                    // behind its barrier.
+                    if ((j > 0 || qq > 0) && __any_sync(0xffffffffu, need)) {
+                        const bool ok =
+                            qq == 0 || wait_or_abort(&bars[kPvDone + qq - 1], (jt + j) & 1, p.err,
+                                                     abort);
+                        if (!__all_sync(0xffffffffu, ok)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < kHeadDim / 32; ++c) {
+                            uint32_t r[32];
+                            tmem_ld32(obase + 32 * c, r);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(obase + 32 * c, r);
+                        }
+                    }
+                    tc_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars[kPFull + qq]);
+                }
             }
-        }
+            if (stop) break;
+            // epilogue: wait for the item's last PV, normalise, store BF16.
+            if (!__all_sync(0xffffffffu, wait_or_abort(&bars[kPvDone + 3], (jt + it.n - 1) & 1,
+                                                       p.err, abort)))
+                break;
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint16_t *dst =
+                p.out + ((int64_t)(it.r0 + row) * p.num_q_heads + it.h) * kHeadDim;
+#pragma unroll 1
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(obase + 32 * c, r);
+                tc_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-        for (int sh = 1; sh < 4; sh <<= 1) {
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, sh));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, sh));
-        }
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-        const float mu_a = mn_a == -CUDART_INF_F ? 0.f : mn_a;
-        const float mu_b = mn_b == -CUDART_INF_F ? 0.f : mn_b;
-        const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
-        m_a = mn_a;
-        m_b = mn_b;
-        float rs_a = 0.f, rs_b = 0.f;
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv,
+                                        __uint_as_float(r[2 * i + 1]) * inv);
+                if (row < it.rows) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            sacc[nt][0] = exp2f(sacc[nt][0] - mu_a);
-            sacc[nt][1] = exp2f(sacc[nt][1] - mu_a);
-            sacc[nt][2] = exp2f(sacc[nt][2] - mu_b);
-            sacc[nt][3] = exp2f(sacc[nt][3] - mu_b);
-            rs_a += sacc[nt][0] + sacc[nt][1];
-            rs_b += sacc[nt][2] + sacc[nt][3];
-        }
-        l_a = l_a * al_a + rs_a;
-        l_b = l_b * al_b + rs_b;
-#pragma unroll
-        for (int nt = 0; nt < 32; ++nt) {
-            o[nt][0] *= al_a;
-            o[nt][1] *= al_a;
-            o[nt][2] *= al_b;
-            o[nt][3] *= al_b;
-        }
-
-        // O (16 x 256) += P (16 x 64) . V (64 x 256), with P = P_hi + P_lo in two BF16
-        // parts: a single BF16 P carries a relative error up to 2^-8 per weight, which
-        // rows with few or peaked keys turn into output errors above the tolerance.
-#pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-            uint32_t ah[4], al[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float x0 = sacc[2 * kt + (r >> 1)][(r & 1) * 2];
-                const float x1 = sacc[2 * kt + (r >> 1)][(r & 1) * 2 + 1];
-                ah[r] = pack_bf16x2(x0, x1);
-                al[r] = pack_bf16x2(x0 - bf16_lo(ah[r]), x1 - bf16_hi(ah[r]));
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        d4[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
+                                            pk[4 * q4 + 3]);
+                }
             }
-#pragma unroll
-            for (int dp = 0; dp < 16; ++dp) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(swz128(vb + (dp >> 2) * kPfKvChunk,
-                                 kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8,
-                                 (dp & 3) * 2 + (lane >> 4)),
-                          b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * dp], ah[0], ah[1], ah[2], ah[3], b0, b1);
-                mma_bf16_16816(o[2 * dp + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
-                mma_bf16_16816(o[2 * dp], al[0], al[1], al[2], al[3], b0, b1);
-                mma_bf16_16816(o[2 * dp + 1], al[0], al[1], al[2], al[3], b2, b3);
-            }
+            tc_fence_before();
+            mbar_arrive(&bars[kOEmpty]);
+            jt += it.n;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-#pragma unroll
-    for (int sh = 1; sh < 4; sh <<= 1) {
-        l_a += __shfl_xor_sync(0xffffffffu, l_a, sh);
-        l_b += __shfl_xor_sync(0xffffffffu, l_b, sh);
-    }
-    const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
-    const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
-    const int row_a = row0 + wr + ra, row_b = row_a + 8;
-    const int dc = (lane & 3) * 2;
-    if (row_a < p.q_len) {
-        uint16_t *dst = p.out + ((int64_t)row_a * p.num_q_heads + h) * kHeadDim + dc;
-#pragma unroll
-        for (int nt = 0; nt < 32; ++nt)
-            *reinterpret_cast<uint32_t *>(dst + nt * 8) =
-                pack_bf16x2(o[nt][0] * inv_a, o[nt][1] * inv_a);
-    }
-    if (row_b < p.q_len) {
-        uint16_t *dst = p.out + ((int64_t)row_b * p.num_q_heads + h) * kHeadDim + dc;
-#pragma unroll
-        for (int nt = 0; nt < 32; ++nt)
-            *reinterpret_cast<uint32_t *>(dst + nt * 8) =
-                pack_bf16x2(o[nt][2] * inv_b, o[nt][3] * inv_b);
-    }
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream) {
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(prefill_kernel),
-                                  kPfSmemBytes, 1);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(prefill_tc_kernel), kSmemBytes, 1);
     if (e != cudaSuccess) return e;
-    PfMaps maps;
+    TcMaps maps;
     maps.q = tmaps[0];
     maps.k = tmaps[1];
     maps.v = tmaps[2];
     maps.k_last = tmaps[3];
     maps.v_last = tmaps[4];
-    PfKParams p;
+    TcParams p;
     p.block_table = a.block_table;
     p.q_len = a.q_len;
     p.q_start = a.q_start;
@@ -278,17 +496,18 @@ cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaS
     p.num_q_heads = a.num_q_heads;
     p.group = a.group;
     p.block_size = a.block_size;
-    p.tiles_per_page = (a.block_size + kPfKvTile - 1) / kPfKvTile;
+    p.blocks_per_page = (a.block_size + kBlk - 1) / kBlk;
     p.last_page = a.last_page;
-    p.num_q_tiles = (a.q_len + kPfQRows - 1) / kPfQRows;
+    p.num_q_tiles = (a.q_len + kBM - 1) / kBM;
+    p.num_items = p.num_q_tiles * a.num_q_heads;
     p.num_pages = a.num_pages;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.sc = fmaxf(fabsf(a.scale) * 1.4426950408889634f, FLT_MIN);
+    p.neg = a.scale < 0.f;
     p.out = a.out;
     p.err = a.err;
-    const dim3 grid(p.num_q_tiles, a.num_q_heads);
+    const int grid = min(p.num_items, a.num_sms > 0 ? a.num_sms : 1);
     if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
-    prefill_kernel<<<grid, kPfThreads, kPfSmemBytes, stream>>>(maps, p);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, maps, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
     return e;
