@@ -35,7 +35,9 @@ constexpr int kDecChunkBytes = kDecTile * 128;             // one 64-dim box: 16
 constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one tile: 8 KB
 constexpr int kDecStageBytes = 2 * kDecHalf;                // 16 KB
 constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 224 KB
-constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kHeadDim + 2) * 4;
+// per warp and head: O row, max, sum, weight; per head: CTA max and sum
+constexpr int kDecMergeBytes =
+    (kDecConsumers * kDecMaxGroup * (kHeadDim + 3) + 2 * kDecMaxGroup) * 4;
 static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
 constexpr int kDecSmemBytes = 1024 + kDecRingBytes + (2 * kDecStages + 1) * 8;
 constexpr int kCombineThreads = kHeadDim;
@@ -147,13 +149,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     pdl_wait();
     pdl_trigger();
 
+    const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
+    const int t0 = split * p.tiles_per_split;
     const int seq_len = checked_seq_len(p, seq, threadIdx.x == 0 && split == 0 && g == 0);
     const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
-    const int t0 = split * p.tiles_per_split;
     const int t1 = min(ntiles, t0 + p.tiles_per_split);
     if (t0 >= t1) return;  // this split has no tiles of this sequence (CTA-uniform)
     const int n = t1 - t0;
-    const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
     // This CTA holds the tile of the token being decoded and has to write that token.
     const bool writes_newest = p.new_slots != nullptr && t1 == ntiles;
 
@@ -350,51 +352,49 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
     }
     named_bar_sync(1, kDecConsumers * 32);
-    for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += kDecConsumers * 32) {
-        const int c = idx / kHeadDim, d = idx - c * kHeadDim;
+    // The CTA's running max per head and each warp's weight exp2(m_w - M), once per head.
+    float *red_e = red_l + kDecConsumers * kDecMaxGroup;  // [warp][head]
+    float *cta_m = red_e + kDecConsumers * kDecMaxGroup;  // [head]
+    float *cta_l = cta_m + kDecMaxGroup;                  // [head]
+    if (threadIdx.x < p.group) {
+        const int c = threadIdx.x;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, red_m[w * kDecMaxGroup + c]);
-        float L = 0.f, O = 0.f;
-        if (M != -CUDART_INF_F) {
+        float L = 0.f;
 #pragma unroll
-            for (int w = 0; w < kDecConsumers; ++w) {
-                const float e = exp2f(red_m[w * kDecMaxGroup + c] - M);
-                L += e * red_l[w * kDecMaxGroup + c];
-                O += e * red_o[(w * kDecMaxGroup + c) * kHeadDim + d];
-            }
+        for (int w = 0; w < kDecConsumers; ++w) {
+            const float e = M == -CUDART_INF_F ? 0.f : exp2f(red_m[w * kDecMaxGroup + c] - M);
+            red_e[w * kDecMaxGroup + c] = e;
+            L += e * red_l[w * kDecMaxGroup + c];
         }
+        cta_m[c] = M;
+        cta_l[c] = L;
+    }
+    named_bar_sync(1, kDecConsumers * 32);
+    for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += kDecConsumers * 32) {
+        const int c = idx / kHeadDim, d = idx - c * kHeadDim;
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecConsumers; ++w)
+            O += red_e[w * kDecMaxGroup + c] * red_o[(w * kDecMaxGroup + c) * kHeadDim + d];
         const int64_t pi =
             ((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split;
         p.part_o[pi * kHeadDim + d] = O;
-        if (d == 0) p.part_ml[pi] = make_float2(M, L);
+        if (d == 0) p.part_ml[pi] = make_float2(cta_m[c], cta_l[c]);
     }
 }
 
-__device__ __forceinline__ float block_reduce(float v, float *red, bool is_max) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, v, sh);
-        v = is_max ? fmaxf(v, o) : v + o;
-    }
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float r = red[0];
-    for (int w = 1; w < kCombineThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-    __syncthreads();
-    return r;
-}
-
-// One CTA per (query head, sequence).  The split weights exp2(m_j - M) are computed once
-// into shared memory; then warp w sums splits w, w+8, ... with each lane owning 8
-// consecutive dims (two 16-byte loads per split, all issued together), and the eight
-// warp sums are added through shared memory.
+// One CTA per (query head, sequence); warp w merges splits w, w+8, w+16, ... against its
+// own running max, with each lane owning 8 consecutive dims (two 16-byte loads per
+// split).  The loads of a batch of up to 32 splits per warp are issued before any of
+// their weights is known, so the kernel waits for global memory about once.  The eight
+// warp results are then merged through shared memory with one more log-sum-exp step.
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeKParams p) {
     constexpr int kWarps = kCombineThreads / 32;
-    __shared__ float wsplit[kDecMaxSplits];
-    __shared__ float red[kCombineThreads / 32];
+    constexpr int kBatch = 8;  // splits per warp whose loads are in flight together
     __shared__ __align__(16) float part[kWarps][kHeadDim];
+    __shared__ float wm[kWarps], wl[kWarps];
     const int h = blockIdx.x, seq = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     pdl_wait();
@@ -403,34 +403,66 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
     const int nsplit = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
     const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.num_splits;
-    float mx = -CUDART_INF_F;
-    for (int j = tid; j < nsplit; j += kCombineThreads) mx = fmaxf(mx, p.part_ml[base + j].x);
-    const float M = block_reduce(mx, red, true);
-    float ls = 0.f;
-    for (int j = tid; j < nsplit; j += kCombineThreads) {
-        const float2 ml = p.part_ml[base + j];
-        const float e = M == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
-        wsplit[j] = e;
-        ls += e * ml.y;
-    }
-    const float L = block_reduce(ls, red, false);  // its barrier also publishes wsplit
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const float4 *po = reinterpret_cast<const float4 *>(p.part_o + base * kHeadDim) + lane * 2;
-#pragma unroll 4
-    for (int j = warp; j < nsplit; j += kWarps) {
-        const float w = wsplit[j];
-        const float4 a = po[(int64_t)j * (kHeadDim / 4)];
-        const float4 b = po[(int64_t)j * (kHeadDim / 4) + 1];
-        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    float M = -CUDART_INF_F, L = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // Split j of this warp's k-th batch element: warp + kWarps * (b0 + k).
+    for (int b0 = 0; warp + kWarps * b0 < nsplit; b0 += kBatch) {
+        float4 va[kBatch], vb[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int j = warp + kWarps * (b0 + k);
+            if (j < nsplit) {
+                va[k] = po[(int64_t)j * (kHeadDim / 4)];
+                vb[k] = po[(int64_t)j * (kHeadDim / 4) + 1];
+            } else {
+                va[k] = vb[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        // Lane k < kBatch holds the (max, sum) of the batch's k-th split.
+        const int jl = warp + kWarps * (b0 + lane);
+        const float2 ml = lane < kBatch && jl < nsplit ? p.part_ml[base + jl]
+                                                       : make_float2(-CUDART_INF_F, 0.f);
+        float bm = ml.x;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, sh));
+        const float mn = fmaxf(M, bm);
+        const float f = M == -CUDART_INF_F ? 0.f : exp2f(M - mn);  // rescale of the old sums
+        const float e = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - mn);
+        float el = e * ml.y;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) el += __shfl_xor_sync(0xffffffffu, el, sh);
+        L = L * f + el;
+        M = mn;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= f;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float w = __shfl_sync(0xffffffffu, e, k);
+            acc[0] += w * va[k].x; acc[1] += w * va[k].y; acc[2] += w * va[k].z; acc[3] += w * va[k].w;
+            acc[4] += w * vb[k].x; acc[5] += w * vb[k].y; acc[6] += w * vb[k].z; acc[7] += w * vb[k].w;
+        }
     }
     reinterpret_cast<float4 *>(&part[warp][lane * 8])[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     reinterpret_cast<float4 *>(&part[warp][lane * 8])[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (lane == 0) {
+        wm[warp] = M;
+        wl[warp] = L;
+    }
     __syncthreads();
-    float O = 0.f;
+    float Mt = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) O += part[w][tid];
-    const float r = L > 0.f ? O / L : 0.f;
+    for (int w = 0; w < kWarps; ++w) Mt = fmaxf(Mt, wm[w]);
+    float O = 0.f, Lt = 0.f;
+    if (Mt != -CUDART_INF_F) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float e = wm[w] == -CUDART_INF_F ? 0.f : exp2f(wm[w] - Mt);
+            O += e * part[w][tid];
+            Lt += e * wl[w];
+        }
+    }
+    const float r = Lt > 0.f ? O / Lt : 0.f;
     const __nv_bfloat16 b = __float2bfloat16_rn(r);
     p.out[((int64_t)seq * p.num_q_heads + h) * kHeadDim + tid] =
         *reinterpret_cast<const uint16_t *>(&b);
