@@ -175,6 +175,25 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
                      int head_dim, int block_size, float scale, pa_bf16 *out, void *stream);
 
 /*
+ * pa_prefill_plan -- the static work assignment pa_prefill_chunk uses, for inspection.
+ * The pages have no counterpart: it describes how this library spreads one chunk over
+ * the GPU, not what the attention computes.  Host only; touches no device.
+ *
+ * Work item i (0 <= i < ceil(q_len / 128) * num_q_heads) is the 128 query rows of tile
+ * ceil(q_len / 128) - 1 - i / num_q_heads (the longest first) of head i % num_q_heads.
+ * Its cost is the number of 256-key tiles it reads (64-key page-local blocks, four per
+ * tile) plus one.  pa_prefill_chunk runs min(num_ctas, items) persistent CTAs, with
+ * num_ctas = the device's SM count.
+ *   cta_of_item  int32 [items] (host) or NULL: the CTA each item runs on
+ *   num_items    (host, or NULL) the item count
+ *   max_cost     (host, or NULL) the largest per-CTA total cost
+ * Returns PA_ERR_INVALID_ARG for bad sizes, PA_ERR_UNSUPPORTED when the problem has more
+ * than 6144 items or 256 CTAs (pa_prefill_chunk then walks the items in a fixed order).
+ */
+int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads, int block_size,
+                    int num_ctas, int32_t *cta_of_item, int *num_items, int *max_cost);
+
+/*
  * pa_get_device_errors -- waits for `stream`, then returns in *bits the device error
  * word of the current device (PA_DEVERR_* bits set by any call since the last clear)
  * and, if clear != 0, resets it to zero.

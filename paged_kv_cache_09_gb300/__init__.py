@@ -11,6 +11,7 @@ Functions (names follow the C ABI):
     reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)     (in place)
     decode_workspace_size(...), decode(q, k_cache, v_cache, block_table, seq_lens, ...)
     prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale)
+    prefill_plan(q_len, q_start, causal, num_q_heads, block_size, num_ctas)  (host only)
     device_errors(clear=True)
 """
 from __future__ import annotations
@@ -24,7 +25,7 @@ import torch
 from . import _build
 
 __all__ = ["load", "build", "slot_mapping", "reshape_and_cache", "decode_workspace_size",
-           "decode", "prefill_chunk", "device_errors", "set_kernel_events", "build_info", "PAError",
+           "decode", "prefill_chunk", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
            "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION",
            "LIB_PATH"]
 
@@ -66,6 +67,7 @@ def load():
                            sz, P, P, P, P], i32),
             "pa_prefill_chunk": ([P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                   P, P], i32),
+            "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, P, P, P], i32),
             "pa_get_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32, P], i32),
             "pa_set_kernel_events": ([P, P], i32),
             "pa_status_string": ([i32], ctypes.c_char_p),
@@ -197,6 +199,21 @@ def prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale, out=
                                 _ptr(bt), q_len, int(q_start), int(bool(causal)), hq, hkv, d,
                                 bs, float(scale), _ptr(out), _stream()), "pa_prefill_chunk")
     return out
+
+
+def prefill_plan(q_len, q_start, causal, num_q_heads, block_size, num_ctas):
+    """The static work assignment of prefill_chunk (see pa_prefill_plan): returns
+    (cta_of_item, max_cost) with cta_of_item a list indexed by work item."""
+    lib = load()
+    n = ctypes.c_int(0)
+    mc = ctypes.c_int(0)
+    _raise(lib.pa_prefill_plan(q_len, q_start, int(bool(causal)), num_q_heads, block_size,
+                               num_ctas, None, ctypes.byref(n), None), "pa_prefill_plan")
+    cta = (ctypes.c_int32 * n.value)()
+    _raise(lib.pa_prefill_plan(q_len, q_start, int(bool(causal)), num_q_heads, block_size,
+                               num_ctas, cta, ctypes.byref(n), ctypes.byref(mc)),
+           "pa_prefill_plan")
+    return list(cta), mc.value
 
 
 def set_kernel_events(start, stop):

@@ -354,7 +354,13 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
         !make_cache_map(&maps[4], v_cache, head_dim, num_kv_heads, last_rows, num_pages,
                         page_stride, pa::kPfBlock))
         return PA_ERR_CUDA;
+    // The static work assignment (cached per shape); problems too large for its arrays
+    // run without one.
+    static thread_local pa::PrefillSchedule sched;
+    const bool planned = pa::plan_prefill(q_len, q_start, causal ? 1 : 0, num_q_heads,
+                                          block_size, dev.num_sms, &sched, nullptr);
     pa::PrefillArgs a;
+    a.sched = planned ? &sched : nullptr;
     a.q = q;
     a.block_table = block_table;
     a.q_len = q_len;

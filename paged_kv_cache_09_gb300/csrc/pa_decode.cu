@@ -35,9 +35,12 @@ constexpr int kDecChunkBytes = kDecTile * 128;             // one 64-dim box: 16
 constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one tile: 8 KB
 constexpr int kDecStageBytes = 2 * kDecHalf;                // 16 KB
 constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 224 KB
-// per warp and head: O row, max, sum, weight; per head: CTA max and sum
+// Merge buffers, per warp and head: O row (padded by 4 floats, so that the 4 head
+// columns a warp stores at once fall in different banks), max, sum, weight; per head:
+// CTA max and sum.
+constexpr int kDecMergeRow = kHeadDim + 4;
 constexpr int kDecMergeBytes =
-    (kDecConsumers * kDecMaxGroup * (kHeadDim + 3) + 2 * kDecMaxGroup) * 4;
+    (kDecConsumers * kDecMaxGroup * (kDecMergeRow + 3) + 2 * kDecMaxGroup) * 4;
 static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
 constexpr int kDecSmemBytes = 1024 + kDecRingBytes + (2 * kDecStages + 1) * 8;
 constexpr int kCombineThreads = kHeadDim;
@@ -330,8 +333,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     // ---------------------------------------------------------------- CTA merge
     named_bar_sync(1, kDecConsumers * 32);  // every tile consumed: the ring is free
-    float *red_o = reinterpret_cast<float *>(smem);                 // [warp][head][D]
-    float *red_m = red_o + kDecConsumers * kDecMaxGroup * kHeadDim;  // [warp][head]
+    float *red_o = reinterpret_cast<float *>(smem);                     // [warp][head][row]
+    float *red_m = red_o + kDecConsumers * kDecMaxGroup * kDecMergeRow;  // [warp][head]
     float *red_l = red_m + kDecConsumers * kDecMaxGroup;
     if (lane < 4) {
         red_m[warp * kDecMaxGroup + qc] = m0;
@@ -340,8 +343,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         red_l[warp * kDecMaxGroup + qc + 1] = l1;
     }
     {
-        float *w0 = red_o + (warp * kDecMaxGroup + qc) * kHeadDim;
-        float *w1 = w0 + kHeadDim;
+        float *w0 = red_o + (warp * kDecMaxGroup + qc) * kDecMergeRow;
+        float *w1 = w0 + kDecMergeRow;
 #pragma unroll
         for (int mt = 0; mt < 16; ++mt) {
             const int d = mt * 16 + r_lo;
@@ -377,7 +380,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         float O = 0.f;
 #pragma unroll
         for (int w = 0; w < kDecConsumers; ++w)
-            O += red_e[w * kDecMaxGroup + c] * red_o[(w * kDecMaxGroup + c) * kHeadDim + d];
+            O += red_e[w * kDecMaxGroup + c] * red_o[(w * kDecMaxGroup + c) * kDecMergeRow + d];
         const int64_t pi =
             ((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split;
         p.part_o[pi * kHeadDim + d] = O;

@@ -99,7 +99,36 @@ constexpr int kPfKvTile = 256;     // keys per K/V tile: four page-local blocks
 constexpr int kPfBlock = 64;       // keys per TMA box (one page-local block)
 constexpr int kPfRing = 5;         // 32 KB K/V unit slots in the shared-memory ring
 
+// Keys one work item (kPfQRows query rows of one head) reads, counted in kPfKvTile-key
+// tiles of page-local kPfBlock-key blocks: what the kernel streams for that item.
+__host__ __device__ inline int prefill_item_tiles(int q_len, int q_start, int causal, int r0,
+                                                  int block_size) {
+    const int rows = q_len - r0 < kPfQRows ? q_len - r0 : kPfQRows;
+    const int nkeys = causal ? q_start + r0 + rows : q_start + q_len;
+    const int blocks_per_page = (block_size + kPfBlock - 1) / kPfBlock;
+    const int full = nkeys / block_size;
+    const int rem = nkeys - full * block_size;
+    const int nblocks = full * blocks_per_page + (rem + kPfBlock - 1) / kPfBlock;
+    return (nblocks + kPfKvTile / kPfBlock - 1) / (kPfKvTile / kPfBlock);
+}
+
+// Static assignment of prefill work items to the persistent CTAs.  Item index i stands
+// for query tile (num_q_tiles - 1 - i / Hq) of head i % Hq (the longest items first).
+constexpr int kPfSchedMaxCtas = 256;
+constexpr int kPfSchedMaxItems = 6144;
+struct PrefillSchedule {
+    int num_ctas;                        // 0: none (the kernel walks a snake order)
+    uint16_t off[kPfSchedMaxCtas + 1];   // CTA b runs items[off[b] .. off[b+1]) in order
+    uint16_t items[kPfSchedMaxItems];
+};
+
+// Plans the schedule (cached per shape); false when the problem exceeds the arrays.
+// max_cost (optional): the largest per-CTA cost, in tiles plus one per item.
+bool plan_prefill(int q_len, int q_start, int causal, int num_q_heads, int block_size,
+                  int num_ctas, PrefillSchedule *s, int *max_cost);
+
 struct PrefillArgs {
+    const PrefillSchedule *sched;  // host copy, passed to the kernel by value (or NULL)
     const uint16_t *q;    // [q_len, Hq, D]
     const int32_t *block_table;
     int q_len, q_start, causal;

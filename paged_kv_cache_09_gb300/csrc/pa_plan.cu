@@ -1,0 +1,179 @@
+// pa_plan.cu -- static work assignment for the persistent prefill kernel (host only).
+//
+// The causal chunk's work items (128 query rows of one head) differ in length: row tile
+// r of a chunk at q_start reads q_start + r*128 + 128 keys.  With about five items per
+// CTA, walking them in a fixed order leaves some CTAs well above the mean (the q=4096
+// chunk over 4096 prior tokens: 138 tiles on the busiest CTA against a mean of 123.8).
+// This planner assigns items to CTAs up front:
+//   1. cost of an item = its K/V tiles + 1 (the per-item Q load and epilogue);
+//   2. longest-processing-time first: items by decreasing cost, each to the CTA with the
+//      least cost so far;
+//   3. local search: while some move of one item off the most loaded CTA, or swap of one
+//      of its items with a cheaper item of another CTA, lowers that CTA's cost without
+//      raising the other one's to the same level, apply the best such change.
+// Each CTA then runs its items longest first.  Plans are cached per shape, since a
+// serving loop prefills chunks of the same few shapes over and over.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+struct PlanKey {
+    int q_len, q_start, causal, hq, bs, ctas;
+    bool operator==(const PlanKey &o) const {
+        return q_len == o.q_len && q_start == o.q_start && causal == o.causal && hq == o.hq &&
+               bs == o.bs && ctas == o.ctas;
+    }
+};
+
+struct CachedPlan {
+    PlanKey key;
+    int max_cost;
+    std::vector<uint16_t> off, items;
+};
+
+constexpr int kPlanCacheSize = 8;
+std::mutex g_plan_mu;
+std::vector<CachedPlan> g_plan_cache;  // most recently used last
+
+void compute_plan(const PlanKey &k, CachedPlan &out) {
+    const int nqt = (k.q_len + kPfQRows - 1) / kPfQRows;
+    const int n = nqt * k.hq;
+    const int G = std::min(k.ctas, n);
+    std::vector<int> cost(n);
+    for (int i = 0; i < n; ++i) {
+        const int qt = nqt - 1 - i / k.hq;
+        cost[i] = prefill_item_tiles(k.q_len, k.q_start, k.causal, qt * kPfQRows, k.bs) + 1;
+    }
+    // 2. LPT.
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int b) { return cost[a] > cost[b]; });
+    std::vector<std::vector<int>> bins(G);
+    std::vector<long long> load(G, 0);
+    using Slot = std::pair<long long, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int b = 0; b < G; ++b) heap.push({0, b});
+    for (int i : order) {
+        const int b = heap.top().second;
+        heap.pop();
+        bins[b].push_back(i);
+        load[b] += cost[i];
+        heap.push({load[b], b});
+    }
+    // 3. Local search on the most loaded CTA (bounded; each step lowers the sum of the
+    // squared loads, so it ends well before the bound on any input).
+    for (int step = 0; step < 4 * n + 64; ++step) {
+        int i = 0;
+        for (int b = 1; b < G; ++b)
+            if (load[b] > load[i]) i = b;
+        const long long Li = load[i];
+        long long best_nm = Li;
+        int bj = -1, ba = -1, bb = -1;
+        for (int j = 0; j < G; ++j) {
+            const long long Lj = load[j];
+            if (j == i || Lj >= Li - 1) continue;
+            for (int ai = 0; ai < (int)bins[i].size(); ++ai) {
+                const int ca = cost[bins[i][ai]];
+                if (Lj + ca < Li) {  // move
+                    const long long nm = std::max(Li - ca, Lj + ca);
+                    if (nm < best_nm) best_nm = nm, bj = j, ba = ai, bb = -1;
+                }
+                for (int bi = 0; bi < (int)bins[j].size(); ++bi) {  // swap
+                    const int d = ca - cost[bins[j][bi]];
+                    if (d <= 0 || Lj + d >= Li) continue;
+                    const long long nm = std::max(Li - d, Lj + d);
+                    if (nm < best_nm) best_nm = nm, bj = j, ba = ai, bb = bi;
+                }
+            }
+        }
+        if (bj < 0) break;
+        const int a = bins[i][ba];
+        bins[i].erase(bins[i].begin() + ba);
+        if (bb >= 0) {
+            const int b = bins[bj][bb];
+            bins[bj].erase(bins[bj].begin() + bb);
+            bins[i].push_back(b);
+            load[i] += cost[b];
+            load[bj] -= cost[b];
+        }
+        bins[bj].push_back(a);
+        load[i] -= cost[a];
+        load[bj] += cost[a];
+    }
+    out.key = k;
+    out.max_cost = (int)*std::max_element(load.begin(), load.end());
+    out.off.assign(G + 1, 0);
+    out.items.clear();
+    out.items.reserve(n);
+    for (int b = 0; b < G; ++b) {
+        std::stable_sort(bins[b].begin(), bins[b].end(), [&](int x, int y) {
+            return cost[x] != cost[y] ? cost[x] > cost[y] : x < y;
+        });
+        for (int x : bins[b]) out.items.push_back((uint16_t)x);
+        out.off[b + 1] = (uint16_t)out.items.size();
+    }
+}
+
+}  // namespace
+
+bool plan_prefill(int q_len, int q_start, int causal, int num_q_heads, int block_size,
+                  int num_ctas, PrefillSchedule *s, int *max_cost) {
+    const long long nqt = (q_len + kPfQRows - 1) / kPfQRows;
+    const long long n = nqt * num_q_heads;
+    if (q_len < 1 || q_start < 0 || num_q_heads < 1 || block_size < 1 || num_ctas < 1 ||
+        n > kPfSchedMaxItems || std::min<long long>(num_ctas, n) > kPfSchedMaxCtas)
+        return false;
+    const PlanKey key{q_len, q_start, causal ? 1 : 0, num_q_heads, block_size, num_ctas};
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = std::find_if(g_plan_cache.begin(), g_plan_cache.end(),
+                           [&](const CachedPlan &c) { return c.key == key; });
+    if (it == g_plan_cache.end()) {
+        CachedPlan fresh;
+        compute_plan(key, fresh);
+        if ((int)g_plan_cache.size() == kPlanCacheSize) g_plan_cache.erase(g_plan_cache.begin());
+        g_plan_cache.push_back(std::move(fresh));
+        it = g_plan_cache.end() - 1;
+    } else if (it != g_plan_cache.end() - 1) {
+        std::rotate(it, it + 1, g_plan_cache.end());  // mark as most recently used
+        it = g_plan_cache.end() - 1;
+    }
+    if (s) {
+        const int G = (int)it->off.size() - 1;
+        s->num_ctas = G;
+        std::memcpy(s->off, it->off.data(), (G + 1) * sizeof(uint16_t));
+        std::memcpy(s->items, it->items.data(), it->items.size() * sizeof(uint16_t));
+    }
+    if (max_cost) *max_cost = it->max_cost;
+    return true;
+}
+
+}  // namespace pa
+
+extern "C" int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads,
+                               int block_size, int num_ctas, int32_t *cta_of_item,
+                               int *num_items, int *max_cost) {
+    if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > INT32_MAX || num_q_heads < 1 ||
+        block_size < 1 || num_ctas < 1)
+        return PA_ERR_INVALID_ARG;
+    static thread_local pa::PrefillSchedule s;
+    int mc = 0;
+    if (!pa::plan_prefill(q_len, q_start, causal, num_q_heads, block_size, num_ctas, &s, &mc))
+        return PA_ERR_UNSUPPORTED;
+    const int n = s.off[s.num_ctas];
+    if (num_items) *num_items = n;
+    if (max_cost) *max_cost = mc;
+    if (cta_of_item)
+        for (int b = 0; b < s.num_ctas; ++b)
+            for (int x = s.off[b]; x < s.off[b + 1]; ++x) cta_of_item[s.items[x]] = b;
+    return PA_OK;
+}

@@ -15,9 +15,11 @@
 // the PV of quarter q runs while the softmax of quarter q+1 is computed, and the tensor
 // core only waits for the softmax of each tile's first quarter.
 //
-// Work item = (128 query rows of one head).  Persistent CTAs, one per SM, walk the items
-// longest first in a snake order (item k of CTA b: k*G + b for even k, k*G + G-1-b for
-// odd k), which evens out the causal imbalance between early and late query rows.
+// Work item = (128 query rows of one head).  Persistent CTAs, one per SM, run the items
+// the host planner assigned to them (a static schedule that balances the causal items'
+// unequal lengths across CTAs, passed in the kernel parameters), longest first.
+// Problems too large for the schedule arrays walk the items longest first in a snake
+// order instead (item k of CTA b: k*G + b for even k, k*G + G-1-b for odd k).
 //
 // Warp roles (192 threads):
 //   warp 0    TMA producer: the item's Q tile (4 boxes of 64 dims x 128 rows, 64 KB),
@@ -40,6 +42,7 @@
 // stop, and the CTA drains its tensor-core work and frees TMEM before it returns.
 #include <float.h>
 #include <math_constants.h>
+#include <string.h>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -90,6 +93,7 @@ struct TcParams {
     int neg;              // scale < 0
     uint16_t *out;
     unsigned *err;
+    PrefillSchedule sched;  // static item -> CTA assignment (num_ctas 0: snake order)
 };
 
 struct TcMaps {
@@ -102,8 +106,15 @@ struct Item {
 
 __device__ __forceinline__ bool item_of(const TcParams &p, int k, Item &it) {
     const int G = gridDim.x, b = blockIdx.x;
-    const int idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
-    if (idx >= p.num_items) return false;
+    int idx;
+    if (p.sched.num_ctas) {
+        const int x = p.sched.off[b] + k;
+        if (x >= p.sched.off[b + 1]) return false;
+        idx = p.sched.items[x];
+    } else {
+        idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
+        if (idx >= p.num_items) return false;
+    }
     const int qt = p.num_q_tiles - 1 - idx / p.num_q_heads;
     it.h = idx % p.num_q_heads;
     it.g = it.h / p.group;
@@ -135,7 +146,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, un
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -505,7 +516,16 @@ cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaS
     p.neg = a.scale < 0.f;
     p.out = a.out;
     p.err = a.err;
-    const int grid = min(p.num_items, a.num_sms > 0 ? a.num_sms : 1);
+    int grid = min(p.num_items, a.num_sms > 0 ? a.num_sms : 1);
+    if (a.sched && a.sched->num_ctas > 0) {
+        const int G = a.sched->num_ctas;
+        p.sched.num_ctas = G;
+        memcpy(p.sched.off, a.sched->off, (G + 1) * sizeof(uint16_t));
+        memcpy(p.sched.items, a.sched->items, a.sched->off[G] * sizeof(uint16_t));
+        grid = G;
+    } else {
+        p.sched.num_ctas = 0;
+    }
     if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
     e = launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, maps, p);
     if (e != cudaSuccess) return e;

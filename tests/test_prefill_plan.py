@@ -1,0 +1,92 @@
+"""Host-only checks of the prefill kernel's static work assignment (pa_prefill_plan).
+
+The plan decides which persistent CTA runs which work item (128 query rows of one head);
+it does not change what is computed, so it is checked for validity and balance, with
+the item costs recomputed here from the kernel's streaming rule: an item reads the keys
+up to its last row (causal) or all keys, in page-local blocks of 64 keys, four blocks
+per 256-key tile, and costs its tile count plus one.
+"""
+import math
+
+import pytest
+
+from test_abi_host import lib  # noqa: F401  (builds and loads libpa.so)
+
+
+def item_costs(q_len, q_start, causal, hq, bs):
+    nqt = math.ceil(q_len / 128)
+    bpp = math.ceil(bs / 64)
+    costs = []
+    for i in range(nqt * hq):
+        qt = nqt - 1 - i // hq
+        r0 = qt * 128
+        rows = min(128, q_len - r0)
+        nkeys = q_start + r0 + rows if causal else q_start + q_len
+        full, rem = divmod(nkeys, bs)
+        nblocks = full * bpp + math.ceil(rem / 64)
+        costs.append(math.ceil(nblocks / 4) + 1)
+    return costs
+
+
+def snake_max(costs, G):
+    load = [0] * G
+    for idx, c in enumerate(costs):
+        k, b = divmod(idx, G)
+        load[b if k % 2 == 0 else G - 1 - b] += c
+    return max(load)
+
+
+SHAPES = [
+    (4096, 4096, True, 24, 832, 152),   # the q=4096 chunk over 4096 prior tokens
+    (4096, 0, True, 24, 832, 152),      # first chunk of a prompt
+    (1685, 12288, True, 24, 832, 152),  # a tail chunk
+    (4096, 4096, True, 24, 784, 152),   # ragged 16-token page tails
+    (4096, 4096, False, 24, 832, 152),  # non-causal: all items equal
+    (130, 900, True, 24, 832, 152),     # fewer items than CTAs
+    (2048, 4096, True, 8, 64, 148),
+]
+
+
+@pytest.mark.parametrize("q_len,q_start,causal,hq,bs,G", SHAPES)
+def test_every_item_runs_exactly_once_on_a_valid_cta(lib, q_len, q_start, causal, hq, bs, G):
+    import paged_kv_cache_09_gb300 as pa
+    cta, max_cost = pa.prefill_plan(q_len, q_start, causal, hq, bs, G)
+    costs = item_costs(q_len, q_start, causal, hq, bs)
+    assert len(cta) == len(costs)
+    ctas = min(G, len(costs))
+    assert all(0 <= b < ctas for b in cta)
+    load = [0] * ctas
+    for i, b in enumerate(cta):
+        load[b] += costs[i]
+    assert max(load) == max_cost
+    assert min(load) > 0  # no CTA is left idle
+    # Never worse than the fixed snake order, never below the obvious lower bounds.
+    assert max_cost <= snake_max(costs, ctas)
+    assert max_cost >= max(max(costs), math.ceil(sum(costs) / ctas))
+
+
+def test_headline_chunk_is_balanced_to_the_lower_bound(lib):
+    import paged_kv_cache_09_gb300 as pa
+    costs = item_costs(4096, 4096, True, 24, 832)
+    _, max_cost = pa.prefill_plan(4096, 4096, True, 24, 832, 152)
+    lb = math.ceil(sum(costs) / 152)
+    assert max_cost <= lb + 1
+    assert snake_max(costs, 152) - max_cost >= 5  # 143 -> 129 in cost units
+
+
+def test_plan_is_deterministic_and_cached(lib):
+    import paged_kv_cache_09_gb300 as pa
+    a = pa.prefill_plan(4096, 4096, True, 24, 832, 152)
+    pa.prefill_plan(2048, 0, True, 24, 832, 152)
+    b = pa.prefill_plan(4096, 4096, True, 24, 832, 152)
+    assert a == b
+
+
+def test_plan_refuses_bad_sizes_and_oversized_problems(lib):
+    import paged_kv_cache_09_gb300 as pa
+    with pytest.raises(pa.PAError):
+        pa.prefill_plan(0, 0, True, 24, 832, 152)
+    with pytest.raises(pa.PAError):
+        pa.prefill_plan(128, -1, True, 24, 832, 152)
+    with pytest.raises(pa.PAError):  # 33000 rows x 24 heads: 6192 items > 6144
+        pa.prefill_plan(33000, 0, True, 24, 832, 152)
