@@ -60,6 +60,7 @@ enum pa_device_error {
     PA_DEVERR_SLOT = 4u,      /* slot (or its page) outside the pool */
     PA_DEVERR_TIMEOUT = 8u,   /* a bounded wait inside a kernel ran out */
     PA_DEVERR_POSITION = 16u, /* a position past the block table's capacity */
+    PA_DEVERR_LAYOUT = 32u,   /* a kernel found its shared memory misaligned; it did nothing */
 };
 
 /*
@@ -118,7 +119,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * is not the one the block table gives for position seq_lens[s] - 1 is not written and
  * sets PA_DEVERR_SLOT.  Pass all three NULL to skip.
  * The split-context kernel processes page-local tiles of 16 tokens, so any block_size
- * works (784 leaves a 16-token tail tile per page, 832 does not).
+ * works (one that is not a multiple of 16 leaves a ragged tile at each page end; 784
+ * and 832 are both multiples of 16).
  */
 int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
               int64_t page_stride, int64_t num_pages, const int32_t *block_table,

@@ -26,11 +26,12 @@ from . import _build
 
 __all__ = ["load", "build", "slot_mapping", "reshape_and_cache", "decode_workspace_size",
            "decode", "prefill_chunk", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
-           "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION",
+           "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION", "DEVERR_LAYOUT",
            "LIB_PATH"]
 
 LIB_PATH = _build.LIB
 DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_POSITION = 1, 2, 4, 8, 16
+DEVERR_LAYOUT = 32
 
 _lib = None
 _lock = threading.Lock()

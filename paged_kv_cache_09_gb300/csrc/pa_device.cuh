@@ -16,7 +16,7 @@ constexpr int kChunks = kHeadDim / kChunkElems;
 
 // Bits of the device error word (same values as PA_DEVERR_* in pa.h).
 constexpr unsigned kErrPage = 1u, kErrSeqLen = 2u, kErrSlot = 4u, kErrTimeout = 8u,
-                   kErrPosition = 16u;
+                   kErrPosition = 16u, kErrLayout = 32u;
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -267,6 +267,42 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Paired fp32 arithmetic (one instruction for two lanes' worth of values; PTX f32x2,
+// sm_100 and later), each result rounded to nearest like the scalar operation.
+// (d0, d1) = (a0, a1) * b + c
+__device__ __forceinline__ void fma2_bc(float &d0, float &d1, float a0, float a1, float b,
+                                        float c) {
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) = (a0, a1) + (b0, b1)
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, float b0,
+                                     float b1) {
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (d0, d1) = (a0, a1) - (b0, b1)
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0,
+                                     float b1) {
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(a, b, c) in one instruction (NaN-free inputs).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // ---------------------------------------------------------------- BF16 packing

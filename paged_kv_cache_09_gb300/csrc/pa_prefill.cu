@@ -21,7 +21,7 @@
 // Problems too large for the schedule arrays walk the items longest first in a snake
 // order instead (item k of CTA b: k*G + b for even k, k*G + G-1-b for odd k).
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0    TMA producer: the item's Q tile (4 boxes of 64 dims x 128 rows, 64 KB),
 //             then per tile four K units (one 64-dim chunk x 256 keys, 32 KB each) and
 //             four V units (64 keys x 256 dims) into a 5-slot ring of 32 KB.  Boxes are
@@ -30,12 +30,16 @@
 //   warp 1    MMA issuer (one thread) and TMEM owner: S = Q K^T (A, B K-major in shared
 //             memory), then O += P V per 64-key quarter (A = P from TMEM, B = V unit
 //             MN-major, 8 KB between 64-dim atoms).
-//   warps 2-5 thread t owns query row t (TMEM lane t).  Per quarter it reads 64 S
-//             values, masks (page end, sequence end, causal) where the quarter needs it,
-//             keeps a running max that moves only when it grows by more than 8 (log2
-//             units; then its O row is rescaled in TMEM), and writes P = P_hi + P_lo (two
-//             BF16 parts, so that P keeps ~16 significant bits) over that quarter of S.
-//             At the end it normalises O and stores BF16.
+//   warps 2-9 softmax: warps w and w+4 share query rows 32*(w%4) .. +31 (TMEM lanes),
+//             one thread per row, and split each 64-key quarter into two 32-key halves
+//             (and O into two 128-column halves).  Per quarter each warp reads its 32 S
+//             values, masks (page end, sequence end, causal) where needed, and the pair
+//             agrees on the quarter's row max through shared memory.  The running max
+//             moves only when it grows by more than 8 (log2 units; then both warps
+//             rescale their half of the O row in TMEM).  Each warp writes P = P_hi + P_lo
+//             (two BF16 parts, so that P keeps ~16 significant bits) for its keys over
+//             that quarter of S.  At the end the pair adds its two partial row sums and
+//             each warp normalises and stores its half of O as BF16.
 // TMEM columns: O [0, 256), S [256, 512); P of quarter q: hi at 256+64q, lo at +32.
 //
 // Every wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT, flags the CTA to
@@ -59,15 +63,20 @@ constexpr int kUnit = 4 * kBlkBytes;          // 32 KB ring slot
 constexpr int kQChunk = kBM * 128;            // 64 dims x 128 rows: 16 KB
 constexpr int kQBytes = kChunks * kQChunk;    // 64 KB
 constexpr int kRing = kPfRing;
-constexpr int kThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 8;              // two per TMEM lane quarter
+constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;
 static_assert(kBN == 4 * kBlk && kBN == 256, "tile = four 64-key blocks");
 
-// Shared memory (offsets from the 1024-byte-aligned base).
+// Shared memory.  Its dynamic part starts 1024-byte aligned on this GPU (right after the
+// 1 KB the hardware reserves per block), which the 128-byte swizzle of the TMA tiles
+// needs; the kernel checks this and reports PA_DEVERR_LAYOUT rather than run otherwise.
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kQBytes;
-constexpr int kOffBars = kOffRing + kRing * kUnit;
+constexpr int kOffXchg = kOffRing + kRing * kUnit;  // row maxima / sums of warp pairs
+constexpr int kXchgBytes = 4 * 2 * 2 * 32 * 4;      // [lane quarter][phase][half][lane]
+constexpr int kOffBars = kOffXchg + kXchgBytes;
 enum Bar {
     kRingFull = 0,
     kRingEmpty = kRingFull + kRing,
@@ -78,9 +87,10 @@ enum Bar {
     kPvDone = kPFull + 4, // [4] quarters
     kOEmpty = kPvDone + 4,
     kDrain,
-    kNumBars
+    kPair,                // [4] the two softmax warps of a lane quarter meet here
+    kNumBars = kPair + 4
 };
-constexpr int kSmemBytes = 1024 + kOffBars + kNumBars * 8 + 16;
+constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct TcParams {
@@ -147,11 +157,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, un
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(16) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // CTA-uniform; nothing has been set up yet
+        if (threadIdx.x == 0) atomicOr(p.err, kErrLayout);
+        return;
+    }
     uint8_t *qs = smem + kOffQ;
     uint8_t *ring = smem + kOffRing;
+    float *xchg = reinterpret_cast<float *>(smem + kOffXchg);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -168,10 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[kQEmpty], 1);
         mbar_init(&bars[kSFull], 1);
         for (int i = 0; i < 4; ++i) {
-            mbar_init(&bars[kPFull + i], 128);
+            mbar_init(&bars[kPFull + i], kSoftmaxWarps * 32);
             mbar_init(&bars[kPvDone + i], 1);
+            mbar_init(&bars[kPair + i], 64);
         }
-        mbar_init(&bars[kOEmpty], 128);
+        mbar_init(&bars[kOEmpty], kSoftmaxWarps * 32);
         mbar_init(&bars[kDrain], 1);
         *abort = 0;
         fence_mbar_init();
@@ -328,11 +342,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t obase = tmem + lane_off + kColO;
+        // Two warps per TMEM lane quarter: warp sw (0..7) owns rows 32*(warp % 4) + lane
+        // and half hf = sw / 4 of every 64-key quarter (keys 32*hf .. 32*hf + 31) and of
+        // the O columns (128*hf .. 128*hf + 127).  The pair agrees on each quarter's row
+        // max through shared memory and its kPair barrier.
+        const int lq = warp & 3;
+        const int hf = (warp - 2) >> 2;
+        const int row = lq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
+        const uint32_t obase = tmem + lane_off + kColO + 128 * hf;
         const uint32_t sbase = tmem + lane_off + kColS;
+        float *xq = xchg + lq * 128;  // [phase][half][lane]
+        uint64_t *pair = &bars[kPair + lq];
+        uint32_t pc = 0;  // exchanges done by this pair (both warps count alike)
+        // Publishes v, meets the partner warp, returns the partner's value.  The meeting
+        // also orders each warp's (completed) TMEM loads of its S half before the
+        // partner's P stores, which land partly in those columns.
+        auto exchange = [&](float v, bool &ok) -> float {
+            const uint32_t ph = pc & 1;
+            xq[ph * 64 + hf * 32 + lane] = v;
+            tc_fence_before();
+            mbar_arrive(pair);
+            ok = wait_or_abort(pair, ph, p.err, abort);
+            tc_fence_after();
+            ++pc;
+            return xq[ph * 64 + (hf ^ 1) * 32 + lane];
+        };
         uint32_t jt = 0;
         Item it;
         bool stop = false;
@@ -347,21 +382,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 for (int qq = 0; qq < 4; ++qq) {
-                    float x[64];
+                    float x[32];
                     {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld32(sbase + 64 * qq, r0);
-                        tmem_ld32(sbase + 64 * qq + 32, r1);
+                        uint32_t r[32];
+                        tmem_ld32(sbase + 64 * qq + 32 * hf, r);
                         tc_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            x[i] = __uint_as_float(r0[i]);
-                            x[32 + i] = __uint_as_float(r1[i]);
-                        }
+                        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
                     }
                     if (p.neg) {  // a negative scale reverses the order of the raw scores
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) x[i] = -x[i];
+                        for (int i = 0; i < 32; ++i) x[i] = -x[i];
                     }
                     // The quarter is one 64-key block; its valid keys form a prefix [0, lim).
                     // Only quarters with a page tail, the sequence end or the causal
@@ -375,18 +406,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lim = min(kBlk, min(p.block_size - off, p.seq_len_k - tok0));
                         if (p.causal) lim = min(lim, qpos - tok0 + 1);
                     }
-                    if (!__all_sync(0xffffffffu, lim >= kBlk)) {
+                    lim -= 32 * hf;  // valid keys of this warp's half
+                    if (!__all_sync(0xffffffffu, lim >= 32)) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) x[i] = i < lim ? x[i] : -CUDART_INF_F;
+                        for (int i = 0; i < 32; ++i) x[i] = i < lim ? x[i] : -CUDART_INF_F;
                     }
-                    float mp[8];
+                    float mp[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        mp[i] = fmaxf(fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24])),
-                                      fmaxf(fmaxf(x[i + 32], x[i + 40]), fmaxf(x[i + 48], x[i + 56])));
-                    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) *
-                                     p.sc;
+                    for (int i = 0; i < 4; ++i)
+                        mp[i] = fmax3(fmax3(x[i], x[i + 4], x[i + 8]),
+                                      fmax3(x[i + 12], x[i + 16], x[i + 20]),
+                                      fmaxf(x[i + 24], x[i + 28]));
+                    float mh = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+                    bool ok = true;
+                    mh = fmaxf(mh, exchange(mh, ok));
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        stop = true;
+                        break;
+                    }
+                    const float mx = mh * p.sc;
                     const float m_new = fmaxf(m_used, mx);
                     const bool need = m_new > m_used + 8.f;  // also true for the first finite max
                     const float alpha =
@@ -397,39 +435,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_used = m_new;
                     }
                     const float nmu = m_used == -CUDART_INF_F ? 0.f : -m_used;
-                    float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t hi[16], lo[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float p0 = ex2_approx(fmaf(x[32 * c + 2 * i], p.sc, nmu));
-                            const float p1 = ex2_approx(fmaf(x[32 * c + 2 * i + 1], p.sc, nmu));
-                            sp[i & 7] += p0 + p1;
-                            hi[i] = pack_bf16x2(p0, p1);
-                            lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
-                        }
-                        tmem_st16(sbase + 64 * qq + 16 * c, hi);
-                        tmem_st16(sbase + 64 * qq + 32 + 16 * c, lo);
+                    for (int i = 0; i < 16; ++i) {
+                        float e0, e1;
+                        fma2_bc(e0, e1, x[2 * i], x[2 * i + 1], p.sc, nmu);
+                        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+                        add2(sa[i & 3], sb[i & 3], sa[i & 3], sb[i & 3], p0, p1);
+                        hi[i] = pack_bf16x2(p0, p1);
+                        float r0, r1;
+                        sub2(r0, r1, p0, p1, bf16_lo(hi[i]), bf16_hi(hi[i]));
+                        lo[i] = pack_bf16x2(r0, r1);
                     }
-                    l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-                    // Moving the running max rescales this row of O, which the PVs of the
-                    // tile's earlier quarters may still be accumulating: wait for them first
-                    // (their completion covers every earlier tensor op).  At quarter 0 no
-                    // wait is needed: S_j being ready means every tensor op issued before
-                    // QK_j has completed.  Either way the parity wait is never two phases
-                    // behind its barrier.
+                    tmem_st16(sbase + 64 * qq + 16 * hf, hi);
+                    tmem_st16(sbase + 64 * qq + 32 + 16 * hf, lo);
+                    l += ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+                    // Moving the running max rescales this row of O (this warp's half of the
+                    // columns), which the PVs of the tile's earlier quarters may still be
+                    // accumulating: wait for them first (their completion covers every
+                    // earlier tensor op).  At quarter 0 no wait is needed: S_j being ready
+                    // means every tensor op issued before QK_j has completed.  Either way
+                    // the parity wait is never two phases behind its barrier.
                     if ((j > 0 || qq > 0) && __any_sync(0xffffffffu, need)) {
-                        const bool ok =
-                            qq == 0 || wait_or_abort(&bars[kPvDone + qq - 1], (jt + j) & 1, p.err,
-                                                     abort);
+                        ok = qq == 0 || wait_or_abort(&bars[kPvDone + qq - 1], (jt + j) & 1,
+                                                      p.err, abort);
                         if (!__all_sync(0xffffffffu, ok)) {
                             stop = true;
                             break;
                         }
                         tc_fence_after();
 #pragma unroll 1
-                        for (int c = 0; c < kHeadDim / 32; ++c) {
+                        for (int c = 0; c < 4; ++c) {
                             uint32_t r[32];
                             tmem_ld32(obase + 32 * c, r);
                             tc_wait_ld();
@@ -445,16 +482,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (stop) break;
-            // epilogue: wait for the item's last PV, normalise, store BF16.
-            if (!__all_sync(0xffffffffu, wait_or_abort(&bars[kPvDone + 3], (jt + it.n - 1) & 1,
-                                                       p.err, abort)))
+            // epilogue: the row sum is the pair's two partial sums; wait for the item's
+            // last PV, normalise this warp's half of the row and store it as BF16.
+            bool ok = true;
+            const float lt = l + exchange(l, ok);
+            if (!__all_sync(0xffffffffu, ok &&
+                                             wait_or_abort(&bars[kPvDone + 3], (jt + it.n - 1) & 1,
+                                                           p.err, abort)))
                 break;
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint16_t *dst =
-                p.out + ((int64_t)(it.r0 + row) * p.num_q_heads + it.h) * kHeadDim;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            uint16_t *dst = p.out + ((int64_t)(it.r0 + row) * p.num_q_heads + it.h) * kHeadDim +
+                            128 * hf;
 #pragma unroll 1
-            for (int c = 0; c < kHeadDim / 32; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
                 tmem_ld32(obase + 32 * c, r);
                 tc_wait_ld();
