@@ -13,8 +13,10 @@ time (K+V of 4 KV heads x 256 dims x 2 bytes).
 
 Other legs, each timed the same way and reported under "legs": the 4K/8K/16K/32K sweep
 (1 GiB pool, 5% of K rows x8), block_size 784 at 8K, batched decode (16 sequences,
-4K-32K, fused write), and the q=4096 prefill chunk over 4096 prior tokens (chunk KV
-write + prefill; TFLOP/s counts the causal work 4*D*Hq*sum_i(4096+i+1) = 6.185e11).
+4K-32K, fused write), the q=4096 prefill chunk over 4096 prior tokens (chunk KV write +
+prefill; TFLOP/s counts the causal work 4*D*Hq*sum_i(4096+i+1) = 6.185e11), and two more
+chunk shapes of the same prompt: the q=1685 tail chunk over 12288 prior tokens and the
+q=4096 first chunk (no prior tokens).
 
 Timing: CUDA events on the launching stream around each step; between steps a 512 MiB
 buffer is read to flush L2 (outside the events).  W warm-up steps first.
@@ -53,7 +55,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="all", help="comma list: sweep,bs784,batched,prefill or all/none")
+    ap.add_argument("--legs", default="all",
+                    help="comma list: sweep,bs784,batched,prefill,prefill_tail,prefill_first "
+                         "or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--contexts", default="4096,8192,16384,32768",
@@ -268,11 +272,18 @@ def decode_leg(pa, case, steps, warmup, flush, peaks, fused):
     return r, ms, kms
 
 
-PREFILL_FLOPS = 4.0 * workloads.HEAD_DIM * workloads.HQ * sum(4096 + i + 1 for i in range(4096))
+def causal_flops(q_len, q_start):
+    """Algorithmic FLOPs of a causal chunk: QK^T and PV, 2*D each per (row, visible key)."""
+    return 4.0 * workloads.HEAD_DIM * workloads.HQ * sum(q_start + i + 1 for i in range(q_len))
 
 
-def prefill_leg(pa, steps, warmup, flush, peaks):
-    case = workloads.prefill_chunk("cuda")
+PREFILL_FLOPS = causal_flops(4096, 4096)
+
+
+def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
+    case = getattr(workloads, make)("cuda")
+    q_len, q_start = case.q.shape[0], case.q_start
+    flops = causal_flops(q_len, q_start)
     out = torch.empty_like(case.q)
     slots = torch.empty(case.positions.numel(), dtype=torch.int64, device="cuda")
     bt0 = case.block_table[0].contiguous()
@@ -289,10 +300,10 @@ def prefill_leg(pa, steps, warmup, flush, peaks):
     ms = time_steps(g.replay, steps, warmup, flush)
     kms = time_main_kernel(pa, attn, steps, warmup, flush)
     step_ms, k_ms = statistics.mean(ms), statistics.mean(kms)
-    r = {"q_len": 4096, "q_start": 4096, "causal_flops": PREFILL_FLOPS,
-         "ms_per_step": step_ms, "step_tflops": PREFILL_FLOPS / (step_ms * 1e-3) / 1e12,
+    r = {"q_len": q_len, "q_start": q_start, "causal_flops": flops,
+         "ms_per_step": step_ms, "step_tflops": flops / (step_ms * 1e-3) / 1e12,
          "kernel_ms": k_ms, "kernel_ms_min": min(kms),
-         "kernel_tflops": PREFILL_FLOPS / (k_ms * 1e-3) / 1e12}
+         "kernel_tflops": flops / (k_ms * 1e-3) / 1e12}
     peak = peaks["bf16_tflops"]
     r["roofline"] = {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
                      "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak, "traffic": None,
@@ -444,7 +455,8 @@ def main():
 
     legs = {}
     want = set() if args.legs == "none" else (
-        {"sweep", "bs784", "batched", "prefill"} if args.legs == "all" else set(args.legs.split(",")))
+        {"sweep", "bs784", "batched", "prefill", "prefill_tail", "prefill_first"}
+        if args.legs == "all" else set(args.legs.split(",")))
     if rank == 0 and "sweep" in want:
         sweep = {}
         for ctx in [int(x) for x in args.contexts.split(",") if x]:
@@ -465,6 +477,12 @@ def main():
             pa, c, max(5, args.steps // 2), args.warmup, flush, peaks, fused=True)
         del c
         torch.cuda.empty_cache()
+    if rank == 0 and "prefill_tail" in want:
+        legs["prefill_tail_q1685_over_12288"] = prefill_leg(
+            pa, max(5, args.steps // 4), args.warmup, flush, peaks, "prefill_tail")
+    if rank == 0 and "prefill_first" in want:
+        legs["prefill_first_q4096_at_0"] = prefill_leg(
+            pa, max(5, args.steps // 4), args.warmup, flush, peaks, "prefill_first")
     if rank == 0 and "prefill" in want:
         legs["prefill_q4096_over_4096"] = prefill_leg(pa, max(5, args.steps // 4), args.warmup,
                                                       flush, peaks)

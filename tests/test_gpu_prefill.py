@@ -63,9 +63,14 @@ def test_prefill_non_causal(cuda_lib, bs, q_len, q_start):
     assert_attention_close(out, ref, "non-causal")
 
 
-def test_prefill_chunk_4096_over_4096_sampled(cuda_lib):
+@pytest.mark.parametrize("make", ["prefill_chunk", "prefill_tail", "prefill_first"])
+def test_prefill_full_chunk_sampled(cuda_lib, make):
+    # The q=4096 chunk over 4096 prior tokens, the q=1685 tail chunk over 12288 and the
+    # q=4096 first chunk, at full size: sampled rows (the first and last of several
+    # 64- and 128-row tiles, and random ones) against the oracle, one by one.
     pa = cuda_lib
-    case = workloads.prefill_chunk("cuda")
+    case = getattr(workloads, make)("cuda")
+    q_len = case.q.shape[0]
     k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
     _write_chunk(pa, case)
     out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
@@ -75,15 +80,16 @@ def test_prefill_chunk_4096_over_4096_sampled(cuda_lib):
     # The GPU's copy of the cache after its own write is the oracle's copy, bit for bit.
     assert np.array_equal(bits(case.k_cache), k_host)
     assert np.array_equal(bits(case.v_cache), v_host)
-    rng = np.random.default_rng(4096)
-    rows = np.concatenate([[0, 1, 63, 64, 65, 127, 128, 2047, 2048, 4032, 4094, 4095],
-                           rng.integers(0, 4096, 180)]).astype(np.int32)
+    rng = np.random.default_rng(q_len + case.q_start)
+    fixed = [r for r in (0, 1, 63, 64, 65, 127, 128, 1536, 1663, 1664, 1684, 2047, 2048,
+                         4032, 4094, 4095) if r < q_len]
+    rows = np.concatenate([fixed, rng.integers(0, q_len, 180)]).astype(np.int32)
     heads = rng.integers(0, 24, rows.size).astype(np.int32)
-    heads[:12] = np.arange(12) * 2 + 1
+    heads[:len(fixed)] = (np.arange(len(fixed)) * 5 + 1) % 24
     ref = oracle.prefill_rows(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
                               case.q_start, True, case.scale, rows, heads)
     got = out[torch.from_numpy(rows).long().cuda(), torch.from_numpy(heads).long().cuda()]
-    assert_attention_close(got, ref, "q=4096 chunk (sampled)")
+    assert_attention_close(got, ref, f"{make} (sampled)")
     assert pa.device_errors() == 0
     again = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
                              case.q_start, True, case.scale)

@@ -207,6 +207,19 @@ def prefill_chunk(device="cpu", q_len=4096, q_start=4096, block_size=832, num_pa
                       q_start=q_start, device=device)
 
 
+def prefill_tail(device="cpu", block_size=832, num_pages=24):
+    """The prompt's last, shorter chunk: q=1685 causal rows at positions 12288..13972 over
+    12288 prior paged tokens (three q=4096 chunks before it)."""
+    return paged_case(1006, [12288 + 1685], block_size, num_pages, q_rows=1685,
+                      q_start=12288, device=device)
+
+
+def prefill_first(device="cpu", block_size=832, num_pages=16):
+    """The prompt's first chunk: q=4096 causal rows at positions 0..4095, no prior tokens."""
+    return paged_case(1007, [4096], block_size, num_pages, q_rows=4096, q_start=0,
+                      device=device)
+
+
 def batched_decode(device="cpu", num_seqs=16, lo=4096, hi=32768, block_size=832,
                    num_pages=640):
     """16 sequences with lengths uniform in [4096, 32768], one new token each, block
