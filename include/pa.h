@@ -80,6 +80,37 @@ int pa_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
                     void *stream);
 
 /*
+ * pa_decode_input_prep -- the inputs of one decode step, computed on the device in one
+ * launch for every KV-cache group [input-prep §4, §5]: num_seqs sequences decode one new
+ * token each, at positions[s] (the number of tokens already in its cache).  Writes
+ *   seq_lens[s]          = positions[s] + 1    (0 for a padding entry, positions[s] < 0)
+ *   input_ids[s]         = sampled_ids[s]      (the token sampled by the previous step)
+ *   query_start_loc[s]   = s, query_start_loc[num_seqs] = num_seqs
+ *   slot_mappings[g][s]  = block_tables[g][s * bt_strides[g] + p / block_sizes[g]]
+ *                          * block_sizes[g] + p % block_sizes[g],   p = positions[s]
+ * for each group g, with the checks of pa_slot_mapping (slot -1 for padding; -1 and
+ * PA_DEVERR_POSITION for a logical page >= max_blocks[g] or a negative table entry).
+ *   positions        int32 [num_seqs], device
+ *   sampled_ids, input_ids   int32 [num_seqs], device; both NULL to skip the copy
+ *   seq_lens         int32 [num_seqs], device, or NULL (not written)
+ *   query_start_loc  int32 [num_seqs + 1], device, or NULL (not written)
+ *   block_tables, bt_strides, max_blocks, block_sizes, slot_mappings: HOST arrays of
+ *                    num_groups entries (1 <= num_groups <= 8); block_tables[g] points to
+ *                    the group's int32 [num_seqs, bt_strides[g]] table on the device,
+ *                    slot_mappings[g] to its int64 [num_seqs] output on the device.  The
+ *                    pointers are read during the call only (under stream capture they
+ *                    are baked into the captured launch).
+ * The groups may differ in block size (a model whose layers keep separate caches).
+ * Returns PA_ERR_INVALID_ARG for a bad count, a NULL pointer, or bt_strides[g] <
+ * max_blocks[g]; num_seqs == 0 is a no-op.
+ */
+int pa_decode_input_prep(const int32_t *positions, const int32_t *sampled_ids,
+                         int32_t *input_ids, int32_t *seq_lens, int32_t *query_start_loc,
+                         int num_seqs, int num_groups, const int32_t *const *block_tables,
+                         const int64_t *bt_strides, const int *max_blocks,
+                         const int *block_sizes, int64_t *const *slot_mappings, void *stream);
+
+/*
  * pa_reshape_and_cache -- KV write of new tokens.  key and value are BF16
  * [num_tokens, num_kv_heads, head_dim], contiguous; token i's rows are copied bit for
  * bit to page slot_mapping[i] / block_size, offset slot_mapping[i] % block_size of

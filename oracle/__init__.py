@@ -10,6 +10,8 @@ C code decodes them to their exact values itself.
 
 Function -> passage it follows (pages cited by post and section):
   slot_mapping       -- input-prep post §3.2 (slot = block_table[pos // bs] * bs + pos % bs)
+  decode_input_prep  -- input-prep post §4, §5: seq_lens = position + 1, query_start_loc,
+                        input_ids from the sampled tokens, one slot mapping per KV group
   reshape_and_cache  -- page832 post §4 (cache layout [pages, BS, Hkv, D]) and the slot above
   attend_row         -- page832 post §1 (address translation) and §5 (score = q.k * scale,
                         softmax, weighted V), written as the exact, non-online definition
@@ -61,6 +63,8 @@ def _load():
             lib.pa_oracle_threads.restype = i32
             lib.pa_oracle_slot_mapping.argtypes = [P, P, P, i64, i32, i32, P]
             lib.pa_oracle_slot_mapping.restype = i32
+            lib.pa_oracle_decode_input_prep.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P]
+            lib.pa_oracle_decode_input_prep.restype = i32
             lib.pa_oracle_reshape_and_cache.argtypes = [P, P, P, P, i64, P, i32, i32, i32, i32]
             lib.pa_oracle_reshape_and_cache.restype = None
             lib.pa_oracle_attend_row.argtypes = [P, P, P, i64, i64, P, i32, i32, i32, i32, i64,
@@ -104,6 +108,29 @@ def slot_mapping(positions, block_table, block_size, seq_idx=None) -> np.ndarray
     if rc != 0:
         raise ValueError("oracle slot_mapping failed")
     return out
+
+
+def decode_input_prep(positions, block_tables, block_sizes, sampled_ids=None):
+    """One decode step's inputs: dict of seq_lens, query_start_loc, input_ids (or None)
+    and slot_mappings (one int64 array per KV-cache group)."""
+    lib = _load()
+    pos = _c(positions, np.int32)
+    S, G = pos.shape[0], len(block_tables)
+    tables = [_c(t, np.int32) for t in block_tables]
+    sid = None if sampled_ids is None else _c(sampled_ids, np.int32)
+    seq_lens = np.empty(S, np.int32)
+    qsl = np.empty(S + 1, np.int32)
+    ids = None if sid is None else np.empty(S, np.int32)
+    slots = [np.empty(S, np.int64) for _ in range(G)]
+    tp = (ctypes.c_void_p * G)(*[t.ctypes.data for t in tables])
+    sp = (ctypes.c_void_p * G)(*[x.ctypes.data for x in slots])
+    strides = (ctypes.c_int64 * G)(*[t.shape[1] for t in tables])
+    bss = (ctypes.c_int * G)(*[int(b) for b in block_sizes])
+    rc = lib.pa_oracle_decode_input_prep(_ptr(pos), _ptr(sid), _ptr(ids), _ptr(seq_lens),
+                                         _ptr(qsl), S, G, tp, strides, bss, sp)
+    if rc != 0:
+        raise ValueError("oracle decode_input_prep failed")
+    return {"seq_lens": seq_lens, "query_start_loc": qsl, "input_ids": ids, "slot_mappings": slots}
 
 
 def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping_, block_size,

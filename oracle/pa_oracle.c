@@ -88,6 +88,34 @@ int pa_oracle_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
     return 0;
 }
 
+/* Decode-step inputs [input-prep §4, §5]: num_seqs sequences decode one token each, at
+ * positions[s] (tokens already cached).  The step's metadata is written once:
+ * seq_lens[s] = position + 1 (0 for a padding entry), input_ids[s] = the token sampled by
+ * the previous step, query_start_loc = 0, 1, ..., num_seqs (one query row per sequence).
+ * Then every KV-cache group g, with its own block table and block size, gets its slot
+ * mapping by the slot formula above (row s of the group's table for sequence s). */
+int pa_oracle_decode_input_prep(const int32_t *positions, const int32_t *sampled_ids,
+                                int32_t *input_ids, int32_t *seq_lens,
+                                int32_t *query_start_loc, int num_seqs, int num_groups,
+                                const int32_t *const *block_tables, const int64_t *bt_strides,
+                                const int *block_sizes, int64_t *const *slot_mappings) {
+    for (int s = 0; s < num_seqs; ++s) {
+        int32_t pos = positions[s];
+        seq_lens[s] = pos >= 0 ? pos + 1 : 0;
+        if (sampled_ids) input_ids[s] = sampled_ids[s];
+        query_start_loc[s] = s;
+    }
+    query_start_loc[num_seqs] = num_seqs;
+    for (int g = 0; g < num_groups; ++g) {
+        for (int s = 0; s < num_seqs; ++s) {
+            int32_t seq = s;
+            pa_oracle_slot_mapping(&positions[s], &seq, block_tables[g], bt_strides[g], 1,
+                                   block_sizes[g], &slot_mappings[g][s]);
+        }
+    }
+    return 0;
+}
+
 /* KV write: token i's rows (all KV heads, [Hkv, D] contiguous) go to page slot/BS,
  * offset slot%BS of each cache [page832 §4 layout].  Negative slots are skipped. */
 void pa_oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,

@@ -8,6 +8,8 @@ loaded, every call raises.
 
 Functions (names follow the C ABI):
     slot_mapping(positions, block_table, block_size, seq_idx=None)    -> int64 slots
+    decode_input_prep(positions, block_tables, block_sizes, sampled_ids=None)
+                                                                      -> step inputs
     reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)     (in place)
     decode_workspace_size(...), decode(q, k_cache, v_cache, block_table, seq_lens, ...)
     prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale)
@@ -24,7 +26,8 @@ import torch
 
 from . import _build
 
-__all__ = ["load", "build", "slot_mapping", "reshape_and_cache", "decode_workspace_size",
+__all__ = ["load", "build", "slot_mapping", "decode_input_prep", "reshape_and_cache",
+           "decode_workspace_size",
            "decode", "prefill_chunk", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
            "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION", "DEVERR_LAYOUT",
            "LIB_PATH"]
@@ -63,6 +66,7 @@ def load():
         sig = {
             "pa_slot_mapping": ([P, P, P, i32, i64, i32, i32, i32, P, P], i32),
             "pa_reshape_and_cache": ([P, P, P, P, i64, i64, P, i32, i32, i32, i32, P], i32),
+            "pa_decode_input_prep": ([P, P, P, P, P, i32, i32, P, P, P, P, P, P], i32),
             "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
             "pa_decode": ([P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32, P, P,
                            sz, P, P, P, P], i32),
@@ -135,6 +139,49 @@ def slot_mapping(positions, block_table, block_size, seq_idx=None, max_blocks=No
     _raise(lib.pa_slot_mapping(_ptr(positions.contiguous()), _ptr(seq_idx), _ptr(bt),
                                bt.shape[0], bt.stride(0), mb, n, int(block_size), _ptr(out),
                                _stream()), "pa_slot_mapping")
+    return out
+
+
+def decode_input_prep(positions, block_tables, block_sizes, sampled_ids=None, max_blocks=None,
+                      out=None):
+    """One decode step's inputs for several KV-cache groups in one launch (see
+    pa_decode_input_prep).  block_tables / block_sizes: one int32 [S, n] table and one
+    block size per group.  Returns a dict with seq_lens, query_start_loc, input_ids (when
+    sampled_ids is given) and slot_mappings (a list, one int64 [S] tensor per group);
+    `out` may pass that dict back in to reuse its tensors."""
+    lib = load()
+    _check(positions, "positions", torch.int32, 1)
+    S, G = positions.shape[0], len(block_tables)
+    if len(block_sizes) != G or not 1 <= G <= 8:
+        raise ValueError("one block size per group, 1..8 groups")
+    dev = positions.device
+    if out is None:
+        out = {"seq_lens": torch.empty(S, dtype=torch.int32, device=dev),
+               "query_start_loc": torch.empty(S + 1, dtype=torch.int32, device=dev),
+               "slot_mappings": [torch.empty(S, dtype=torch.int64, device=dev) for _ in range(G)]}
+        if sampled_ids is not None:
+            out["input_ids"] = torch.empty(S, dtype=torch.int32, device=dev)
+    tables = []
+    for t in block_tables:
+        _check(t, "block_table", torch.int32, 2)
+        if t.shape[0] < S or t.stride(1) != 1:
+            raise ValueError("block tables: one row per sequence, contiguous rows")
+        tables.append(t)
+    mb = max_blocks if max_blocks is not None else [t.shape[1] for t in tables]
+    arr = lambda ctype, vals: (ctype * G)(*vals)
+    bt_ptrs = arr(ctypes.c_void_p, [t.data_ptr() for t in tables])
+    sm_ptrs = arr(ctypes.c_void_p, [m.data_ptr() for m in out["slot_mappings"]])
+    strides = arr(ctypes.c_int64, [t.stride(0) for t in tables])
+    mbs = arr(ctypes.c_int, [int(x) for x in mb])
+    bss = arr(ctypes.c_int, [int(x) for x in block_sizes])
+    sid = None
+    if sampled_ids is not None:
+        _check(sampled_ids, "sampled_ids", torch.int32, 1)
+        sid = sampled_ids.contiguous()
+    _raise(lib.pa_decode_input_prep(_ptr(positions.contiguous()), _ptr(sid),
+                                    _ptr(out.get("input_ids")), _ptr(out["seq_lens"]),
+                                    _ptr(out["query_start_loc"]), S, G, bt_ptrs, strides, mbs,
+                                    bss, sm_ptrs, _stream()), "pa_decode_input_prep")
     return out
 
 

@@ -222,6 +222,41 @@ int pa_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_decode_input_prep(const int32_t *positions, const int32_t *sampled_ids,
+                         int32_t *input_ids, int32_t *seq_lens, int32_t *query_start_loc,
+                         int num_seqs, int num_groups, const int32_t *const *block_tables,
+                         const int64_t *bt_strides, const int *max_blocks,
+                         const int *block_sizes, int64_t *const *slot_mappings, void *stream) {
+    if (num_seqs < 0 || num_groups < 1 || num_groups > pa::kPrepMaxGroups)
+        return PA_ERR_INVALID_ARG;
+    if (!block_tables || !bt_strides || !max_blocks || !block_sizes || !slot_mappings)
+        return PA_ERR_INVALID_ARG;
+    if ((sampled_ids == nullptr) != (input_ids == nullptr)) return PA_ERR_INVALID_ARG;
+    pa::PrepArgs a = {};
+    for (int g = 0; g < num_groups; ++g) {
+        if (!block_tables[g] || !slot_mappings[g] || block_sizes[g] < 1 || max_blocks[g] < 1 ||
+            bt_strides[g] < max_blocks[g])
+            return PA_ERR_INVALID_ARG;
+        a.g[g] = pa::PrepGroup{block_tables[g], bt_strides[g], max_blocks[g], block_sizes[g],
+                               slot_mappings[g]};
+    }
+    if (num_seqs == 0) return PA_OK;
+    if (!positions) return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    a.positions = positions;
+    a.sampled_ids = sampled_ids;
+    a.input_ids = input_ids;
+    a.seq_lens = seq_lens;
+    a.query_start_loc = query_start_loc;
+    a.num_seqs = num_seqs;
+    a.num_groups = num_groups;
+    a.err = dev.err;
+    return pa::launch_decode_input_prep(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 int pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *k_cache,
                          pa_bf16 *v_cache, int64_t page_stride, int64_t num_pages,
                          const int64_t *slot_mapping, int num_tokens, int num_kv_heads,

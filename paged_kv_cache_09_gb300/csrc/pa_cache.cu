@@ -24,6 +24,22 @@ cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
     return e;
 }
 
+// Slot of position pos of sequence s (row s of the block table), or -1: a negative
+// position is padding; a logical page past max_blocks, a sequence outside the table or a
+// negative table entry gives -1 and sets kErrPosition.
+__device__ __forceinline__ int64_t slot_of(int32_t pos, int64_t s, const int32_t *block_table,
+                                           int num_seqs, int64_t bt_stride, int max_blocks,
+                                           int block_size, unsigned *err) {
+    if (pos < 0) return -1;
+    const int logical_block = pos / block_size;
+    if (logical_block < max_blocks && s >= 0 && s < num_seqs) {
+        const int32_t block_number = block_table[s * bt_stride + logical_block];
+        if (block_number >= 0) return (int64_t)block_number * block_size + pos % block_size;
+    }
+    atomicOr(err, kErrPosition);
+    return -1;
+}
+
 __global__ void slot_mapping_kernel(const int32_t *__restrict__ positions,
                                     const int32_t *__restrict__ seq_idx,
                                     const int32_t *__restrict__ block_table, int num_seqs,
@@ -34,22 +50,37 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ positions,
     pdl_wait();
     pdl_trigger();
     if (i >= num_tokens) return;
-    const int32_t pos = positions[i];
-    int64_t slot = -1;
-    if (pos >= 0) {
-        const int64_t s = seq_idx ? seq_idx[i] : 0;
-        const int logical_block = pos / block_size;
-        if (logical_block < max_blocks && s >= 0 && s < num_seqs) {
-            const int32_t block_number = block_table[s * bt_stride + logical_block];
-            if (block_number >= 0)
-                slot = (int64_t)block_number * block_size + pos % block_size;
-            else
-                atomicOr(err, kErrPosition);
-        } else {
-            atomicOr(err, kErrPosition);
+    slot_mapping[i] = slot_of(positions[i], seq_idx ? seq_idx[i] : 0, block_table, num_seqs,
+                              bt_stride, max_blocks, block_size, err);
+}
+
+// Decode input preparation (input-prep post §4, §5): grid (sequence blocks, groups).  The
+// blocks of group 0 also write the step's shared metadata; every group writes its own
+// slots from its own block table and block size.
+__global__ void decode_input_prep_kernel(const __grid_constant__ PrepArgs a) {
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    const int grp = blockIdx.y;
+    pdl_wait();
+    pdl_trigger();
+    if (s >= a.num_seqs) return;
+    const int32_t pos = a.positions[s];
+    if (grp == 0) {
+        if (a.input_ids) a.input_ids[s] = a.sampled_ids[s];
+        if (a.seq_lens) a.seq_lens[s] = pos >= 0 ? pos + 1 : 0;
+        if (a.query_start_loc) {
+            a.query_start_loc[s] = s;
+            if (s == a.num_seqs - 1) a.query_start_loc[s + 1] = s + 1;
         }
     }
-    slot_mapping[i] = slot;
+    const PrepGroup &g = a.g[grp];
+    g.slot_mapping[s] = slot_of(pos, s, g.block_table, a.num_seqs, g.bt_stride, g.max_blocks,
+                                g.block_size, a.err);
+}
+
+cudaError_t launch_decode_input_prep(const PrepArgs &a, cudaStream_t stream) {
+    const int threads = 128;
+    const dim3 grid((a.num_seqs + threads - 1) / threads, a.num_groups);
+    return launch_pdl(decode_input_prep_kernel, grid, dim3(threads), 0, stream, a);
 }
 
 cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx,

@@ -40,6 +40,23 @@ cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx
                                 int num_tokens, int block_size, int64_t *slot_mapping,
                                 unsigned *err, cudaStream_t stream);
 
+// Decode input preparation for several KV-cache groups in one launch.
+constexpr int kPrepMaxGroups = 8;
+struct PrepGroup {
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int max_blocks, block_size;
+    int64_t *slot_mapping;
+};
+struct PrepArgs {
+    const int32_t *positions, *sampled_ids;
+    int32_t *input_ids, *seq_lens, *query_start_loc;
+    int num_seqs, num_groups;
+    PrepGroup g[kPrepMaxGroups];
+    unsigned *err;
+};
+cudaError_t launch_decode_input_prep(const PrepArgs &a, cudaStream_t stream);
+
 cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
                                      uint16_t *k_cache, uint16_t *v_cache, int64_t page_stride,
                                      int64_t num_pages, const int64_t *slot_mapping,

@@ -137,3 +137,35 @@ def test_workspace_size_is_zero_for_invalid_sizes(lib):
     assert lib.pa_decode_workspace_size(0, 24, 4, 256, 832, 8192) == 0
     assert lib.pa_decode_workspace_size(1, 24, 5, 256, 832, 8192) == 0
     assert lib.pa_decode_workspace_size(1, 24, 4, 128, 832, 8192) == 0
+
+
+def _prep(lib, num_seqs=4, num_groups=2, tables=(FAKE, FAKE), strides=(16, 16), mbs=(10, 10),
+          bss=(832, 16), slots=(FAKE, FAKE), positions=FAKE, sampled=None, ids=None):
+    import ctypes
+    G = len(tables)
+    arr = lambda t, v: (t * G)(*v)
+    return lib.pa_decode_input_prep(positions, sampled, ids, FAKE, FAKE, num_seqs, num_groups,
+                                    arr(ctypes.c_void_p, tables), arr(ctypes.c_int64, strides),
+                                    arr(ctypes.c_int, mbs), arr(ctypes.c_int, bss),
+                                    arr(ctypes.c_void_p, slots), None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_groups=0), PA_ERR_INVALID_ARG),
+    (dict(num_groups=9, tables=(FAKE,) * 9, strides=(16,) * 9, mbs=(10,) * 9, bss=(16,) * 9,
+          slots=(FAKE,) * 9), PA_ERR_INVALID_ARG),
+    (dict(tables=(FAKE, None)), PA_ERR_INVALID_ARG),
+    (dict(slots=(None, FAKE)), PA_ERR_INVALID_ARG),
+    (dict(strides=(16, 9)), PA_ERR_INVALID_ARG),     # stride below max_blocks
+    (dict(bss=(832, 0)), PA_ERR_INVALID_ARG),
+    (dict(mbs=(0, 10)), PA_ERR_INVALID_ARG),
+    (dict(sampled=FAKE), PA_ERR_INVALID_ARG),        # sampled ids without input_ids
+    (dict(positions=None), PA_ERR_INVALID_ARG),
+    (dict(num_seqs=-1), PA_ERR_INVALID_ARG),
+])
+def test_decode_input_prep_rejects_bad_arguments(lib, kw, want):
+    assert _prep(lib, **kw) == want
+
+
+def test_decode_input_prep_with_no_sequences_is_a_no_op(lib):
+    assert _prep(lib, num_seqs=0, positions=None) == 0

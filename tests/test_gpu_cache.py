@@ -116,3 +116,78 @@ def test_reshape_and_cache_unbind_views_and_padding(cuda_lib):
     pa.reshape_and_cache(key[:1], val[:1], k_cache, v_cache, bad)
     assert pa.device_errors() == pa.DEVERR_SLOT
     assert np.array_equal(bits(kv), want)
+
+
+def _prep_case(S, block_sizes, seed, pad_every=0):
+    """Positions and one random block table per KV-cache group (row s = sequence s)."""
+    rng = np.random.default_rng(seed)
+    pos = rng.integers(0, 20000, S).astype(np.int32)
+    if pad_every:
+        pos[::pad_every] = -1
+    tables = []
+    for bs in block_sizes:
+        mb = 20000 // bs + 1
+        tables.append(rng.permutation(S * mb + 7)[:S * mb].astype(np.int32).reshape(S, mb))
+    sampled = rng.integers(0, 150000, S).astype(np.int32)
+    return pos, tables, sampled
+
+
+@pytest.mark.parametrize("S,block_sizes", [(1, [832]), (1, [832, 16]), (16, [832, 784, 16]),
+                                           (300, [64, 832]), (5, [1, 7, 832, 784, 64, 16, 2, 3])])
+def test_decode_input_prep_matches_oracle(cuda_lib, S, block_sizes):
+    pa = cuda_lib
+    pos, tables, sampled = _prep_case(S, block_sizes, 50 + S + len(block_sizes), pad_every=4)
+    got = pa.decode_input_prep(torch.from_numpy(pos).cuda(),
+                               [torch.from_numpy(t).cuda() for t in tables], block_sizes,
+                               sampled_ids=torch.from_numpy(sampled).cuda())
+    want = oracle.decode_input_prep(pos, tables, block_sizes, sampled_ids=sampled)
+    for k in ("seq_lens", "query_start_loc", "input_ids"):
+        assert np.array_equal(got[k].cpu().numpy(), want[k]), k
+    for g in range(len(block_sizes)):
+        assert np.array_equal(got["slot_mappings"][g].cpu().numpy(), want["slot_mappings"][g])
+    assert pa.device_errors() == 0
+
+
+def test_decode_input_prep_reports_positions_past_the_table(cuda_lib):
+    pa = cuda_lib
+    pos = torch.tensor([100, 5000, 70], dtype=torch.int32, device="cuda")
+    t0 = torch.tensor([[3, 4], [5, 6], [-2, 7]], dtype=torch.int32, device="cuda")  # BS 832
+    t1 = torch.arange(3 * 400, dtype=torch.int32, device="cuda").reshape(3, 400)    # BS 16
+    got = pa.decode_input_prep(pos, [t0, t1], [832, 16])
+    # seq 1: 5000 // 832 = 6 >= 2 entries in group 0 -> -1; group 1 entry 312 is fine.
+    # seq 2: group 0 entry is negative -> -1.
+    assert got["slot_mappings"][0].tolist() == [3 * 832 + 100, -1, -1]
+    assert got["slot_mappings"][1].tolist() == [6 * 16 + 4, (400 + 312) * 16 + 8,
+                                                (800 + 4) * 16 + 6]
+    assert got["seq_lens"].tolist() == [101, 5001, 71]
+    assert pa.device_errors() == pa.DEVERR_POSITION
+
+
+def test_decode_input_prep_feeds_the_fused_decode(cuda_lib):
+    # The step of a two-group model: input prep writes seq_lens and both groups' slots in
+    # one launch; the attention layer of group 0 then decodes with the fused write.
+    pa = cuda_lib
+    from _util import assert_attention_close
+    case = workloads.batched_decode("cuda")
+    k_before, v_before = bits(case.k_cache), bits(case.v_cache)
+    positions = (case.seq_lens - 1).to(torch.int32)
+    S = positions.shape[0]
+    other = torch.arange(S * 2100, dtype=torch.int32, device="cuda").reshape(S, 2100)  # BS 16
+    prep = pa.decode_input_prep(positions, [case.block_table, other], [case.block_size, 16])
+    assert torch.equal(prep["seq_lens"], case.seq_lens)
+    msl = int(case.seq_lens.max())
+    out = pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, prep["seq_lens"],
+                    case.scale, msl, new_k=case.new_k, new_v=case.new_v,
+                    new_slots=prep["slot_mappings"][0])
+    torch.cuda.synchronize()
+    slots = oracle.slot_mapping(positions.cpu().numpy(), case.block_table.cpu().numpy(),
+                                case.block_size, np.arange(S, dtype=np.int32))
+    assert np.array_equal(prep["slot_mappings"][0].cpu().numpy(), slots)
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_before, v_before, slots,
+                             case.block_size)
+    assert np.array_equal(bits(case.k_cache), k_before)
+    assert np.array_equal(bits(case.v_cache), v_before)
+    ref = oracle.decode(bits(case.q), k_before, v_before, case.block_table.cpu().numpy(),
+                        case.seq_lens.cpu().numpy(), case.scale)
+    assert_attention_close(out, ref, "decode after input prep")
+    assert pa.device_errors() == 0

@@ -60,6 +60,22 @@ def test_slot_mapping_hand_worked_table():
         assert int(got[0]) == int(want), (bs, pos)
 
 
+def test_decode_input_prep_hand_worked_step():
+    rows = [ln.split("#")[0].split() for ln in
+            open(os.path.join(GOLDEN, "decode_input_prep_hand.txt"))]
+    rows = [list(map(int, r)) for r in rows if r]
+    g0 = np.array([[5, 2, 7, 0], [3, 1, 6, 4], [9, 8, 11, 10]], dtype=np.int32)
+    g1 = np.array([[1000 * (s + 1) + j for j in range(256)] for s in range(3)], dtype=np.int32)
+    pos = np.array([r[1] for r in rows], np.int32)
+    sampled = np.array([r[2] for r in rows], np.int32)
+    got = oracle.decode_input_prep(pos, [g0, g1], [832, 16], sampled_ids=sampled)
+    assert got["seq_lens"].tolist() == [r[3] for r in rows]
+    assert got["input_ids"].tolist() == [r[2] for r in rows]
+    assert got["slot_mappings"][0].tolist() == [r[4] for r in rows]
+    assert got["slot_mappings"][1].tolist() == [r[5] for r in rows]
+    assert got["query_start_loc"].tolist() == [0, 1, 2, 3]
+
+
 def test_page_geometry_from_pages():
     rows = [ln.split("#")[0].split() for ln in open(os.path.join(GOLDEN, "page_geometry.txt"))]
     for bs, groups, tail, nbytes in [r for r in rows if r]:
