@@ -56,8 +56,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all",
-                    help="comma list: sweep,bs784,batched,prefill,prefill_tail,prefill_first "
-                         "or all/none")
+                    help="comma list: sweep,bs784,batched,prefill,prefill_tail,prefill_first,"
+                         "prep or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--contexts", default="4096,8192,16384,32768",
@@ -311,6 +311,37 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     return r
 
 
+def input_prep_leg(pa, steps, warmup, flush):
+    """Decode input preparation of one sequence for a two-group model (block sizes 832 and
+    16): one pa_decode_input_prep launch against one pa_slot_mapping launch per group plus
+    the metadata written by torch ops (the unfused path), each replayed from a graph."""
+    dev = "cuda"
+    pos = torch.tensor([8191], dtype=torch.int32, device=dev)
+    sampled = torch.tensor([42], dtype=torch.int32, device=dev)
+    t0 = torch.arange(16, dtype=torch.int32, device=dev).reshape(1, 16)
+    t1 = torch.arange(600, dtype=torch.int32, device=dev).reshape(1, 600)
+    out = pa.decode_input_prep(pos, [t0, t1], [832, 16], sampled_ids=sampled)
+    s0 = torch.empty(1, dtype=torch.int64, device=dev)
+    s1 = torch.empty(1, dtype=torch.int64, device=dev)
+    ids = torch.empty(1, dtype=torch.int32, device=dev)
+    seq_lens = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def fused():
+        pa.decode_input_prep(pos, [t0, t1], [832, 16], sampled_ids=sampled, out=out)
+
+    def unfused():
+        ids.copy_(sampled)
+        torch.add(pos, 1, out=seq_lens)
+        pa.slot_mapping(pos, t0, 832, out=s0)
+        pa.slot_mapping(pos, t1, 16, out=s1)
+    r = {}
+    for name, fn in (("one_launch", fused), ("per_group", unfused)):
+        g = graph_of(fn)
+        ms = time_steps(g.replay, steps, warmup, flush)
+        r[name + "_us"] = statistics.median(ms) * 1e3
+    return r
+
+
 def e2e_leg(pa, case, steps, warmup, flush):
     """The headline step through the public API with pinned host buffers: H2D of the
     step's inputs (q, the new token's K/V, its position, the block table and seq_lens),
@@ -455,7 +486,7 @@ def main():
 
     legs = {}
     want = set() if args.legs == "none" else (
-        {"sweep", "bs784", "batched", "prefill", "prefill_tail", "prefill_first"}
+        {"sweep", "bs784", "batched", "prefill", "prefill_tail", "prefill_first", "prep"}
         if args.legs == "all" else set(args.legs.split(",")))
     if rank == 0 and "sweep" in want:
         sweep = {}
@@ -477,6 +508,8 @@ def main():
             pa, c, max(5, args.steps // 2), args.warmup, flush, peaks, fused=True)
         del c
         torch.cuda.empty_cache()
+    if rank == 0 and "prep" in want:
+        legs["decode_input_prep_2_groups"] = input_prep_leg(pa, args.steps, args.warmup, flush)
     if rank == 0 and "prefill_tail" in want:
         legs["prefill_tail_q1685_over_12288"] = prefill_leg(
             pa, max(5, args.steps // 4), args.warmup, flush, peaks, "prefill_tail")
