@@ -16,7 +16,8 @@ Other legs, each timed the same way and reported under "legs": the 4K/8K/16K/32K
 4K-32K, fused write), the q=4096 prefill chunk over 4096 prior tokens (chunk KV write +
 prefill; TFLOP/s counts the causal work 4*D*Hq*sum_i(4096+i+1) = 6.185e11), and two more
 chunk shapes of the same prompt: the q=1685 tail chunk over 12288 prior tokens and the
-q=4096 first chunk (no prior tokens).
+q=4096 first chunk (no prior tokens); a mixed batch of four sequences' chunks in one
+varlen call; and the decode input preparation of a two-group model.
 
 Timing: CUDA events on the launching stream around each step; between steps a 512 MiB
 buffer is read to flush L2 (outside the events).  W warm-up steps first.
@@ -57,7 +58,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all",
                     help="comma list: sweep,bs784,batched,prefill,prefill_tail,prefill_first,"
-                         "prep or all/none")
+                         "prefill_mixed,prep or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--contexts", default="4096,8192,16384,32768",
@@ -282,18 +283,30 @@ PREFILL_FLOPS = causal_flops(4096, 4096)
 
 def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     case = getattr(workloads, make)("cuda")
-    q_len, q_start = case.q.shape[0], case.q_start
-    flops = causal_flops(q_len, q_start)
     out = torch.empty_like(case.q)
     slots = torch.empty(case.positions.numel(), dtype=torch.int64, device="cuda")
-    bt0 = case.block_table[0].contiguous()
+    cu = case.meta.get("cu_seqlens_q")
+    if cu is None:  # one sequence's chunk
+        q_len, q_start = case.q.shape[0], case.q_start
+        flops = causal_flops(q_len, q_start)
+        bt0 = case.block_table[0].contiguous()
 
-    def attn():
-        pa.prefill_chunk(case.q, case.k_cache, case.v_cache, bt0, case.q_start, True,
-                         case.scale, out=out)
+        def attn():
+            pa.prefill_chunk(case.q, case.k_cache, case.v_cache, bt0, case.q_start, True,
+                             case.scale, out=out)
+    else:  # a mixed batch of chunks
+        k_lens = case.meta["seq_lens"]
+        q_len = int(cu[-1])
+        q_start = [L - (cu[b + 1] - cu[b]) for b, L in enumerate(k_lens)]
+        flops = sum(causal_flops(cu[b + 1] - cu[b], q_start[b]) for b in range(len(k_lens)))
+
+        def attn():
+            pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                              True, case.scale, out=out)
 
     def step():
-        pa.slot_mapping(case.positions, case.block_table, case.block_size, out=slots)
+        pa.slot_mapping(case.positions, case.block_table, case.block_size,
+                        seq_idx=case.seq_idx, out=slots)
         pa.reshape_and_cache(case.new_k, case.new_v, case.k_cache, case.v_cache, slots)
         attn()
     g = graph_of(step)
@@ -486,7 +499,8 @@ def main():
 
     legs = {}
     want = set() if args.legs == "none" else (
-        {"sweep", "bs784", "batched", "prefill", "prefill_tail", "prefill_first", "prep"}
+        {"sweep", "bs784", "batched", "prefill", "prefill_tail", "prefill_first",
+         "prefill_mixed", "prep"}
         if args.legs == "all" else set(args.legs.split(",")))
     if rank == 0 and "sweep" in want:
         sweep = {}
@@ -510,6 +524,9 @@ def main():
         torch.cuda.empty_cache()
     if rank == 0 and "prep" in want:
         legs["decode_input_prep_2_groups"] = input_prep_leg(pa, args.steps, args.warmup, flush)
+    if rank == 0 and "prefill_mixed" in want:
+        legs["prefill_mixed_4_chunks"] = prefill_leg(
+            pa, max(5, args.steps // 4), args.warmup, flush, peaks, "prefill_mixed")
     if rank == 0 and "prefill_tail" in want:
         legs["prefill_tail_q1685_over_12288"] = prefill_leg(
             pa, max(5, args.steps // 4), args.warmup, flush, peaks, "prefill_tail")

@@ -208,6 +208,31 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
                      int head_dim, int block_size, float scale, pa_bf16 *out, void *stream);
 
 /*
+ * pa_prefill_varlen -- pa_prefill_chunk for a mixed batch: the chunks of num_seqs
+ * sequences, stacked row-wise, in one call [page832 §6: the vendor kernel's
+ * cu_seqlens_q / seqused_k / block_table interface].  Sequence b's chunk is rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q and out; they are the LAST
+ * q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] tokens of the sequence's seq_lens_k[b]
+ * keys, i.e. row i of the chunk sits at absolute position seq_lens_k[b] - q_len_b + i and,
+ * with causal != 0, sees keys 0 .. that position; otherwise all seq_lens_k[b] keys.  The
+ * chunk's own K/V must already be in the cache.
+ *   q, out         BF16 [cu_seqlens_q[num_seqs], num_q_heads, head_dim], contiguous
+ *   block_table    int32 [num_seqs, bt_stride], device; row b for sequence b; bt_stride
+ *                  >= ceil(seq_lens_k[b] / block_size) for every b
+ *   cu_seqlens_q   int32 [num_seqs + 1], HOST, cu_seqlens_q[0] = 0, non-decreasing
+ *   seq_lens_k     int32 [num_seqs], HOST, each >= its chunk's rows
+ * The lengths are host arrays because the library plans the work on the host (which
+ * CTA runs which 128-row tile of which sequence and head).  Sequences with an empty chunk
+ * are skipped; more than 32 non-empty chunks run as several launches, 32 chunks each,
+ * one after another on the stream.  num_seqs == 0 or no rows at all is a no-op.
+ */
+int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                      int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                      int64_t bt_stride, const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                      int num_seqs, int causal, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, float scale, pa_bf16 *out, void *stream);
+
+/*
  * pa_prefill_plan -- the static work assignment pa_prefill_chunk uses, for inspection.
  * The pages have no counterpart: it describes how this library spreads one chunk over
  * the GPU, not what the attention computes.  Host only; touches no device.

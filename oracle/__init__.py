@@ -18,6 +18,7 @@ Function -> passage it follows (pages cited by post and section):
   decode             -- attend_row over seq_lens[i] keys per sequence, head h -> kv head h // G
   prefill_rows       -- page832 post §6: causal chunk, row i at position q_start + i sees
                         keys 0..q_start+i
+  prefill_varlen     -- page832 post §6 (cu_seqlens_q interface): `prefill` per sequence
 """
 from __future__ import annotations
 
@@ -225,3 +226,18 @@ def prefill(q, k_cache, v_cache, block_table_row, q_start, causal, scale, num_th
     out = prefill_rows(q, k_cache, v_cache, block_table_row, q_start, causal, scale, rows, heads,
                        num_threads)
     return out.reshape(q_len, hq, d)
+
+
+def prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, causal, scale,
+                   num_threads=None):
+    """Chunks of several sequences stacked row-wise (page832 post §6's varlen interface):
+    chunk b = rows cu[b]..cu[b+1]-1, the last rows of sequence b's seq_lens_k[b] keys, each
+    computed by `prefill` over row b of the block table."""
+    q = np.ascontiguousarray(q)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in range(len(seq_lens_k)):
+        r0, r1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        if r1 > r0:
+            out[r0:r1] = prefill(q[r0:r1], k_cache, v_cache, block_table[b],
+                                 int(seq_lens_k[b]) - (r1 - r0), causal, scale, num_threads)
+    return out

@@ -13,6 +13,7 @@ Functions (names follow the C ABI):
     reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)     (in place)
     decode_workspace_size(...), decode(q, k_cache, v_cache, block_table, seq_lens, ...)
     prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale)
+    prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, causal, scale)
     prefill_plan(q_len, q_start, causal, num_q_heads, block_size, num_ctas)  (host only)
     device_errors(clear=True)
 """
@@ -28,7 +29,7 @@ from . import _build
 
 __all__ = ["load", "build", "slot_mapping", "decode_input_prep", "reshape_and_cache",
            "decode_workspace_size",
-           "decode", "prefill_chunk", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
+           "decode", "prefill_chunk", "prefill_varlen", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
            "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION", "DEVERR_LAYOUT",
            "LIB_PATH"]
 
@@ -73,6 +74,8 @@ def load():
             "pa_prefill_chunk": ([P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                   P, P], i32),
             "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, P, P, P], i32),
+            "pa_prefill_varlen": ([P, P, P, i64, i64, P, i64, P, P, i32, i32, i32, i32, i32,
+                                   i32, f32, P, P], i32),
             "pa_get_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32, P], i32),
             "pa_set_kernel_events": ([P, P], i32),
             "pa_status_string": ([i32], ctypes.c_char_p),
@@ -246,6 +249,33 @@ def prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale, out=
     _raise(lib.pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
                                 _ptr(bt), q_len, int(q_start), int(bool(causal)), hq, hkv, d,
                                 bs, float(scale), _ptr(out), _stream()), "pa_prefill_chunk")
+    return out
+
+
+def prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, causal, scale,
+                   out=None):
+    """Chunks of several sequences stacked row-wise in q (see pa_prefill_varlen).
+    cu_seqlens_q and seq_lens_k are host sequences of ints (lists or arrays)."""
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(block_table, "block_table", torch.int32, 2)
+    ps = _check_cache(k_cache, v_cache)
+    q = q.contiguous()
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    B = len(seq_lens_k)
+    if len(cu_seqlens_q) != B + 1 or int(cu_seqlens_q[-1]) != q.shape[0]:
+        raise ValueError("cu_seqlens_q: num_seqs + 1 offsets ending at q's row count")
+    cu = (ctypes.c_int32 * (B + 1))(*[int(x) for x in cu_seqlens_q])
+    sk = (ctypes.c_int32 * max(B, 1))(*[int(x) for x in seq_lens_k])
+    _, hq, d = q.shape
+    _, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _raise(lib.pa_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
+                                 _ptr(block_table), block_table.stride(0), cu, sk, B,
+                                 int(bool(causal)), hq, hkv, d, bs, float(scale), _ptr(out),
+                                 _stream()), "pa_prefill_varlen")
     return out
 
 

@@ -8,7 +8,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "pa.h"
 #include "pa_device.cuh"
@@ -357,6 +359,64 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
     return pa::launch_decode(tk, tv, a, plan, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// One prefill launch over 1 .. kPfMaxSeqs chunks whose rows lie in q / out of total_q rows.
+static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
+                          const pa_bf16 *v_cache, int64_t page_stride, int64_t num_pages,
+                          const int32_t *block_table, int64_t bt_stride,
+                          const pa::PrefillSeq *seqs, int nseq, int causal, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, float scale,
+                          pa_bf16 *out, const DeviceInfo &dev, cudaEvent_t ev_start,
+                          cudaEvent_t ev_stop, cudaStream_t stream) {
+    CUtensorMap maps[3 + 2 * pa::kPfMaxSeqs];
+    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, total_q, pa::kPfQRows) ||
+        !make_cache_map(&maps[1], k_cache, head_dim, num_kv_heads, block_size, num_pages,
+                        page_stride, pa::kPfBlock) ||
+        !make_cache_map(&maps[2], v_cache, head_dim, num_kv_heads, block_size, num_pages,
+                        page_stride, pa::kPfBlock))
+        return PA_ERR_CUDA;
+    int q_lens[pa::kPfMaxSeqs], q_starts[pa::kPfMaxSeqs];
+    for (int b = 0; b < nseq; ++b) {
+        // The sequence's last page is read through maps whose rows end at its last token,
+        // so rows past it come back as zeros.
+        const int seq_len_k = seqs[b].q_start + seqs[b].q_len;
+        const int last_rows = seq_len_k - ((seq_len_k - 1) / block_size) * block_size;
+        if (!make_cache_map(&maps[3 + 2 * b], k_cache, head_dim, num_kv_heads, last_rows,
+                            num_pages, page_stride, pa::kPfBlock) ||
+            !make_cache_map(&maps[4 + 2 * b], v_cache, head_dim, num_kv_heads, last_rows,
+                            num_pages, page_stride, pa::kPfBlock))
+            return PA_ERR_CUDA;
+        q_lens[b] = seqs[b].q_len;
+        q_starts[b] = seqs[b].q_start;
+    }
+    // The static work assignment (cached per shape); problems too large for its arrays
+    // run without one.
+    static thread_local pa::PrefillSchedule sched;
+    const bool planned = pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads,
+                                          block_size, dev.num_sms, &sched, nullptr);
+    pa::PrefillArgs a;
+    a.sched = planned ? &sched : nullptr;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.num_seqs = nseq;
+    a.seqs = seqs;
+    a.causal = causal;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_q_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.out = out;
+    a.err = dev.err;
+    a.num_sms = dev.num_sms;
+    a.ev_start = ev_start;
+    a.ev_stop = ev_stop;
+    if (diag_enabled())
+        fprintf(stderr, "[pa] prefill: %d chunk(s), first q_len=%d q_start=%d causal=%d bs=%d\n",
+                nseq, seqs[0].q_len, seqs[0].q_start, causal, block_size);
+    return pa::launch_prefill(maps, a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
                      int64_t page_stride, int64_t num_pages, const int32_t *block_table,
                      int q_len, int q_start, int causal, int num_q_heads, int num_kv_heads,
@@ -370,54 +430,63 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
     if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return PA_ERR_INVALID_ARG;
-    const int num_q_tiles = (q_len + pa::kPfQRows - 1) / pa::kPfQRows;
-    if (num_q_tiles > 0x7fffffff) return PA_ERR_INVALID_ARG;
-
     DeviceInfo dev;
     if (int rc = device_info(&dev)) return rc;
-    const int seq_len_k = q_start + q_len;
-    const int last_page = (seq_len_k - 1) / block_size;
-    const int last_rows = seq_len_k - last_page * block_size;
-    CUtensorMap maps[5];
-    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, q_len, pa::kPfQRows) ||
-        !make_cache_map(&maps[1], k_cache, head_dim, num_kv_heads, block_size, num_pages,
-                        page_stride, pa::kPfBlock) ||
-        !make_cache_map(&maps[2], v_cache, head_dim, num_kv_heads, block_size, num_pages,
-                        page_stride, pa::kPfBlock) ||
-        !make_cache_map(&maps[3], k_cache, head_dim, num_kv_heads, last_rows, num_pages,
-                        page_stride, pa::kPfBlock) ||
-        !make_cache_map(&maps[4], v_cache, head_dim, num_kv_heads, last_rows, num_pages,
-                        page_stride, pa::kPfBlock))
-        return PA_ERR_CUDA;
-    // The static work assignment (cached per shape); problems too large for its arrays
-    // run without one.
-    static thread_local pa::PrefillSchedule sched;
-    const bool planned = pa::plan_prefill(q_len, q_start, causal ? 1 : 0, num_q_heads,
-                                          block_size, dev.num_sms, &sched, nullptr);
-    pa::PrefillArgs a;
-    a.sched = planned ? &sched : nullptr;
-    a.q = q;
-    a.block_table = block_table;
-    a.q_len = q_len;
-    a.q_start = q_start;
-    a.causal = causal ? 1 : 0;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.group = num_q_heads / num_kv_heads;
-    a.block_size = block_size;
-    a.last_page = last_page;
-    a.num_pages = num_pages;
-    a.scale = scale;
-    a.out = out;
-    a.err = dev.err;
-    a.num_sms = dev.num_sms;
-    take_kernel_events(&a.ev_start, &a.ev_stop);
-    if (diag_enabled())
-        fprintf(stderr, "[pa] prefill: q_len=%d q_start=%d causal=%d bs=%d q_tiles=%d\n", q_len,
-                q_start, a.causal, block_size, num_q_tiles);
-    return pa::launch_prefill(maps, a, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PA_OK
-               : PA_ERR_CUDA;
+    cudaEvent_t e0, e1;
+    take_kernel_events(&e0, &e1);
+    const pa::PrefillSeq seq{0, q_len, q_start, 0};
+    return prefill_launch(q, q_len, k_cache, v_cache, page_stride, num_pages, block_table, 0,
+                          &seq, 1, causal ? 1 : 0, num_q_heads, num_kv_heads, head_dim,
+                          block_size, scale, out, dev, e0, e1, static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                      int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                      int64_t bt_stride, const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                      int num_seqs, int causal, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, float scale, pa_bf16 *out, void *stream) {
+    if (num_seqs < 0 || !cu_seqlens_q || (num_seqs > 0 && !seq_lens_k)) return PA_ERR_INVALID_ARG;
+    if (cu_seqlens_q[0] != 0) return PA_ERR_INVALID_ARG;
+    int64_t max_pages = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int64_t ql = (int64_t)cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        if (ql < 0 || seq_lens_k[b] < 0 || ql > seq_lens_k[b]) return PA_ERR_INVALID_ARG;
+        if (block_size >= 1)
+            max_pages = std::max<int64_t>(max_pages, (seq_lens_k[b] + block_size - 1) / block_size);
+    }
+    const int total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
+    if (int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
+                                       num_pages, page_stride))
+        return rc;
+    if (total_q == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !out || bt_stride < max_pages)
+        return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (int rc = device_info(&dev)) return rc;
+    cudaEvent_t e0, e1;
+    take_kernel_events(&e0, &e1);
+    // The non-empty chunks, kPfMaxSeqs per launch (each launch spreads its chunks over all
+    // SMs; the launches run back to back on the stream).
+    std::vector<pa::PrefillSeq> seqs;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int ql = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        if (ql > 0) seqs.push_back(pa::PrefillSeq{cu_seqlens_q[b], ql, seq_lens_k[b] - ql, b});
+    }
+    const int n = (int)seqs.size();
+    for (int s0 = 0; s0 < n; s0 += pa::kPfMaxSeqs) {
+        const int cnt = std::min(pa::kPfMaxSeqs, n - s0);
+        if (int rc = prefill_launch(q, total_q, k_cache, v_cache, page_stride, num_pages,
+                                    block_table, bt_stride, &seqs[s0], cnt, causal ? 1 : 0,
+                                    num_q_heads, num_kv_heads, head_dim, block_size, scale, out,
+                                    dev, s0 == 0 ? e0 : nullptr,
+                                    s0 + cnt == n ? e1 : nullptr,
+                                    static_cast<cudaStream_t>(stream)))
+            return rc;
+    }
+    return PA_OK;
 }
 
 int pa_set_kernel_events(void *start, void *stop) {

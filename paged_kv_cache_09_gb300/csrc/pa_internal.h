@@ -139,19 +139,34 @@ struct PrefillSchedule {
     uint16_t items[kPfSchedMaxItems];
 };
 
-// Plans the schedule (cached per shape); false when the problem exceeds the arrays.
+// Plans the schedule (cached per shape) for one launch over num_seqs chunks (chunk b:
+// q_lens[b] rows at positions q_starts[b]..; work items numbered sequence by sequence,
+// each sequence's longest query tile first); false when the problem exceeds the arrays.
 // max_cost (optional): the largest per-CTA cost, in tiles plus one per item.
-bool plan_prefill(int q_len, int q_start, int causal, int num_q_heads, int block_size,
-                  int num_ctas, PrefillSchedule *s, int *max_cost);
+bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int causal,
+                  int num_q_heads, int block_size, int num_ctas, PrefillSchedule *s,
+                  int *max_cost);
+
+// Sequences one prefill launch takes (their chunks' tensor maps travel in the launch's
+// parameters); a larger batch is split into several launches.
+constexpr int kPfMaxSeqs = 32;
+
+struct PrefillSeq {
+    int q_off;    // first row of the chunk in q / out
+    int q_len;    // rows of the chunk (>= 1)
+    int q_start;  // absolute position of the chunk's first row
+    int bt_row;   // its row of the block table
+};
 
 struct PrefillArgs {
     const PrefillSchedule *sched;  // host copy, passed to the kernel by value (or NULL)
-    const uint16_t *q;    // [q_len, Hq, D]
-    const int32_t *block_table;
-    int q_len, q_start, causal;
+    const int32_t *block_table;    // [num_seqs, bt_stride]: row b for sequence b
+    int64_t bt_stride;
+    int num_seqs;                  // 1 .. kPfMaxSeqs
+    const PrefillSeq *seqs;        // host array of num_seqs entries
+    int causal;
     int num_q_heads, num_kv_heads, group;
     int block_size;
-    int last_page;        // logical index of the sequence's last page
     int64_t num_pages;
     float scale;
     uint16_t *out;
@@ -160,7 +175,7 @@ struct PrefillArgs {
     int num_sms;                    // persistent grid size bound
 };
 
-// tmaps: Q, K, V, K of the last page, V of the last page.
+// tmaps: Q, K, V, then the K and V maps cut at each sequence's last token (2 per sequence).
 cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream);
 
 }  // namespace pa

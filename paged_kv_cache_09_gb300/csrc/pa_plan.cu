@@ -27,10 +27,11 @@ namespace pa {
 namespace {
 
 struct PlanKey {
-    int q_len, q_start, causal, hq, bs, ctas;
+    std::vector<std::pair<int, int>> chunks;  // (q_len, q_start) of each sequence
+    int causal, hq, bs, ctas;
     bool operator==(const PlanKey &o) const {
-        return q_len == o.q_len && q_start == o.q_start && causal == o.causal && hq == o.hq &&
-               bs == o.bs && ctas == o.ctas;
+        return chunks == o.chunks && causal == o.causal && hq == o.hq && bs == o.bs &&
+               ctas == o.ctas;
     }
 };
 
@@ -45,14 +46,19 @@ std::mutex g_plan_mu;
 std::vector<CachedPlan> g_plan_cache;  // most recently used last
 
 void compute_plan(const PlanKey &k, CachedPlan &out) {
-    const int nqt = (k.q_len + kPfQRows - 1) / kPfQRows;
-    const int n = nqt * k.hq;
-    const int G = std::min(k.ctas, n);
-    std::vector<int> cost(n);
-    for (int i = 0; i < n; ++i) {
-        const int qt = nqt - 1 - i / k.hq;
-        cost[i] = prefill_item_tiles(k.q_len, k.q_start, k.causal, qt * kPfQRows, k.bs) + 1;
+    // Items sequence by sequence; within a sequence item i is query tile nqt - 1 - i / hq
+    // of head i % hq.
+    std::vector<int> cost;
+    for (const auto &c : k.chunks) {
+        const int nqt = (c.first + kPfQRows - 1) / kPfQRows;
+        for (int i = 0; i < nqt * k.hq; ++i) {
+            const int qt = nqt - 1 - i / k.hq;
+            cost.push_back(prefill_item_tiles(c.first, c.second, k.causal, qt * kPfQRows, k.bs) +
+                           1);
+        }
     }
+    const int n = (int)cost.size();
+    const int G = std::min(k.ctas, n);
     // 2. LPT.
     std::vector<int> order(n);
     for (int i = 0; i < n; ++i) order[i] = i;
@@ -126,14 +132,19 @@ void compute_plan(const PlanKey &k, CachedPlan &out) {
 
 }  // namespace
 
-bool plan_prefill(int q_len, int q_start, int causal, int num_q_heads, int block_size,
-                  int num_ctas, PrefillSchedule *s, int *max_cost) {
-    const long long nqt = (q_len + kPfQRows - 1) / kPfQRows;
-    const long long n = nqt * num_q_heads;
-    if (q_len < 1 || q_start < 0 || num_q_heads < 1 || block_size < 1 || num_ctas < 1 ||
-        n > kPfSchedMaxItems || std::min<long long>(num_ctas, n) > kPfSchedMaxCtas)
+bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int causal,
+                  int num_q_heads, int block_size, int num_ctas, PrefillSchedule *s,
+                  int *max_cost) {
+    if (num_seqs < 1 || num_q_heads < 1 || block_size < 1 || num_ctas < 1) return false;
+    long long n = 0;
+    PlanKey key{{}, causal ? 1 : 0, num_q_heads, block_size, num_ctas};
+    for (int b = 0; b < num_seqs; ++b) {
+        if (q_lens[b] < 1 || q_starts[b] < 0) return false;
+        n += (long long)((q_lens[b] + kPfQRows - 1) / kPfQRows) * num_q_heads;
+        key.chunks.emplace_back(q_lens[b], q_starts[b]);
+    }
+    if (n > kPfSchedMaxItems || std::min<long long>(num_ctas, n) > kPfSchedMaxCtas)
         return false;
-    const PlanKey key{q_len, q_start, causal ? 1 : 0, num_q_heads, block_size, num_ctas};
     std::lock_guard<std::mutex> lock(g_plan_mu);
     auto it = std::find_if(g_plan_cache.begin(), g_plan_cache.end(),
                            [&](const CachedPlan &c) { return c.key == key; });
@@ -167,7 +178,8 @@ extern "C" int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_hea
         return PA_ERR_INVALID_ARG;
     static thread_local pa::PrefillSchedule s;
     int mc = 0;
-    if (!pa::plan_prefill(q_len, q_start, causal, num_q_heads, block_size, num_ctas, &s, &mc))
+    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, block_size, num_ctas, &s,
+                          &mc))
         return PA_ERR_UNSUPPORTED;
     const int n = s.off[s.num_ctas];
     if (num_items) *num_items = n;

@@ -93,28 +93,45 @@ enum Bar {
 constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
+// One sequence of the launch: its chunk is rows q_off .. q_off + q_len - 1 of q / out, at
+// absolute positions q_start .. q_start + q_len - 1 of a sequence of seq_len_k keys.
+struct SeqInfo {
+    int q_off, q_len, q_start, seq_len_k;
+    int last_page;    // logical index of the sequence's last page
+    int num_q_tiles;  // ceil(q_len / 128)
+    int item_off;     // its first work item: items item_off .. item_off + tiles * Hq - 1
+    int bt_row;       // its row of the block table
+};
+
+template <int kSeqs>
 struct TcParams {
-    const int32_t *block_table;
-    int q_len, q_start, causal, seq_len_k;
+    const int32_t *block_table;  // row b of sequence b, bt_stride entries apart
+    int64_t bt_stride;
+    int causal, num_seqs, num_items;
     int num_q_heads, group;
-    int block_size, blocks_per_page, last_page, num_q_tiles, num_items;
+    int block_size, blocks_per_page;
     int64_t num_pages;
     float sc;             // |scale| * log2(e), at least FLT_MIN
     int neg;              // scale < 0
     uint16_t *out;
     unsigned *err;
+    SeqInfo seq[kSeqs];
     PrefillSchedule sched;  // static item -> CTA assignment (num_ctas 0: snake order)
 };
 
+template <int kSeqs>
 struct TcMaps {
-    CUtensorMap q, k, v, k_last, v_last;
+    CUtensorMap q, k, v;
+    CUtensorMap k_last[kSeqs], v_last[kSeqs];  // cut at each sequence's last token
 };
 
 struct Item {
     int h, g, r0, rows, nblocks, n;  // head, KV head, first row, rows present, blocks, tiles
+    int b, q_off, q_start, seq_len_k, last_page, bt_row;  // its sequence
 };
 
-__device__ __forceinline__ bool item_of(const TcParams &p, int k, Item &it) {
+template <int kSeqs>
+__device__ __forceinline__ bool item_of(const TcParams<kSeqs> &p, int k, Item &it) {
     const int G = gridDim.x, b = blockIdx.x;
     int idx;
     if (p.sched.num_ctas) {
@@ -125,12 +142,22 @@ __device__ __forceinline__ bool item_of(const TcParams &p, int k, Item &it) {
         idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
         if (idx >= p.num_items) return false;
     }
-    const int qt = p.num_q_tiles - 1 - idx / p.num_q_heads;
-    it.h = idx % p.num_q_heads;
+    int sb = 0;
+    while (sb + 1 < p.num_seqs && idx >= p.seq[sb + 1].item_off) ++sb;
+    const SeqInfo &sq = p.seq[sb];
+    const int local = idx - sq.item_off;
+    const int qt = sq.num_q_tiles - 1 - local / p.num_q_heads;
+    it.h = local % p.num_q_heads;
     it.g = it.h / p.group;
     it.r0 = qt * kBM;
-    it.rows = min(kBM, p.q_len - it.r0);
-    const int nkeys = p.causal ? p.q_start + it.r0 + it.rows : p.seq_len_k;
+    it.rows = min(kBM, sq.q_len - it.r0);
+    it.b = sb;
+    it.q_off = sq.q_off;
+    it.q_start = sq.q_start;
+    it.seq_len_k = sq.seq_len_k;
+    it.last_page = sq.last_page;
+    it.bt_row = sq.bt_row;
+    const int nkeys = p.causal ? sq.q_start + it.r0 + it.rows : sq.seq_len_k;
     const int full = nkeys / p.block_size;
     const int rem = nkeys - full * p.block_size;
     it.nblocks = full * p.blocks_per_page + (rem + kBlk - 1) / kBlk;
@@ -155,8 +182,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, un
     }
 }
 
+template <int kSeqs>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+    prefill_tc_kernel(const __grid_constant__ TcMaps<kSeqs> maps,
+                      const __grid_constant__ TcParams<kSeqs> p) {
     extern __shared__ __align__(16) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // CTA-uniform; nothing has been set up yet
         if (threadIdx.x == 0) atomicOr(p.err, kErrLayout);
@@ -221,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
                     tma_load_3d(qs + c * kQChunk, &maps.q, &bars[kQFull], c * kChunkElems, it.h,
-                                it.r0);
+                                it.q_off + it.r0);
+                const int32_t *bt = p.block_table + (int64_t)it.bt_row * p.bt_stride;
                 for (int j = 0; j < it.n && !stop; ++j) {
                     // Page, offset and map of each of the tile's four blocks; blocks past the
                     // item's last are read from outside the pool (zeros) and masked.
@@ -233,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int lp = kb / p.blocks_per_page;
                         of[bb] = (kb - lp * p.blocks_per_page) * kBlk;
                         if (kb < it.nblocks) {
-                            pg[bb] = p.block_table[lp];
+                            pg[bb] = bt[lp];
                             if (pg[bb] < 0 || pg[bb] >= p.num_pages) atomicOr(p.err, kErrPage);
-                            mk[bb] = lp == p.last_page ? &maps.k_last : &maps.k;
-                            mv[bb] = lp == p.last_page ? &maps.v_last : &maps.v;
+                            mk[bb] = lp == it.last_page ? &maps.k_last[it.b] : &maps.k;
+                            mv[bb] = lp == it.last_page ? &maps.v_last[it.b] : &maps.v;
                         } else {
                             pg[bb] = (int)p.num_pages;
                             of[bb] = 0;
@@ -372,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
         bool stop = false;
         for (int k = 0; !stop && item_of(p, k, it); ++k) {
-            const int qpos = p.q_start + it.r0 + row;
+            const int qpos = it.q_start + it.r0 + row;
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int j = 0; j < it.n && !stop; ++j) {
                 if (!__all_sync(0xffffffffu,
@@ -403,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int lp = kb / p.blocks_per_page;
                         const int off = (kb - lp * p.blocks_per_page) * kBlk;
                         const int tok0 = lp * p.block_size + off;
-                        lim = min(kBlk, min(p.block_size - off, p.seq_len_k - tok0));
+                        lim = min(kBlk, min(p.block_size - off, it.seq_len_k - tok0));
                         if (p.causal) lim = min(lim, qpos - tok0 + 1);
                     }
                     lim -= 32 * hf;  // valid keys of this warp's half
@@ -492,8 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            uint16_t *dst = p.out + ((int64_t)(it.r0 + row) * p.num_q_heads + it.h) * kHeadDim +
-                            128 * hf;
+            uint16_t *dst =
+                p.out + ((int64_t)(it.q_off + it.r0 + row) * p.num_q_heads + it.h) * kHeadDim +
+                128 * hf;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
@@ -530,28 +561,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream) {
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(prefill_tc_kernel), kSmemBytes, 1);
+namespace {
+
+template <int kSeqs>
+cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int slot,
+                             cudaStream_t stream) {
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(prefill_tc_kernel<kSeqs>),
+                                  kSmemBytes, slot);
     if (e != cudaSuccess) return e;
-    TcMaps maps;
+    TcMaps<kSeqs> maps;
     maps.q = tmaps[0];
     maps.k = tmaps[1];
     maps.v = tmaps[2];
-    maps.k_last = tmaps[3];
-    maps.v_last = tmaps[4];
-    TcParams p;
+    TcParams<kSeqs> p;
     p.block_table = a.block_table;
-    p.q_len = a.q_len;
-    p.q_start = a.q_start;
+    p.bt_stride = a.bt_stride;
     p.causal = a.causal;
-    p.seq_len_k = a.q_start + a.q_len;
+    p.num_seqs = a.num_seqs;
+    int items = 0;
+    for (int b = 0; b < a.num_seqs; ++b) {
+        const PrefillSeq &sq = a.seqs[b];
+        maps.k_last[b] = tmaps[3 + 2 * b];
+        maps.v_last[b] = tmaps[4 + 2 * b];
+        SeqInfo &si = p.seq[b];
+        si.q_off = sq.q_off;
+        si.q_len = sq.q_len;
+        si.q_start = sq.q_start;
+        si.seq_len_k = sq.q_start + sq.q_len;
+        si.last_page = (si.seq_len_k - 1) / a.block_size;
+        si.num_q_tiles = (sq.q_len + kBM - 1) / kBM;
+        si.item_off = items;
+        si.bt_row = sq.bt_row;
+        items += si.num_q_tiles * a.num_q_heads;
+    }
+    p.num_items = items;
     p.num_q_heads = a.num_q_heads;
     p.group = a.group;
     p.block_size = a.block_size;
     p.blocks_per_page = (a.block_size + kBlk - 1) / kBlk;
-    p.last_page = a.last_page;
-    p.num_q_tiles = (a.q_len + kBM - 1) / kBM;
-    p.num_items = p.num_q_tiles * a.num_q_heads;
     p.num_pages = a.num_pages;
     p.sc = fmaxf(fabsf(a.scale) * 1.4426950408889634f, FLT_MIN);
     p.neg = a.scale < 0.f;
@@ -568,10 +615,19 @@ cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaS
         p.sched.num_ctas = 0;
     }
     if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
-    e = launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, maps, p);
+    e = launch_pdl(prefill_tc_kernel<kSeqs>, dim3(grid), dim3(kThreads), kSmemBytes, stream,
+                   maps, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
     return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream) {
+    if (a.num_seqs < 1 || a.num_seqs > kPfMaxSeqs) return cudaErrorInvalidValue;
+    if (a.num_seqs == 1) return launch_prefill_n<1>(tmaps, a, 1, stream);
+    return launch_prefill_n<kPfMaxSeqs>(tmaps, a, 2, stream);
 }
 
 }  // namespace pa

@@ -169,3 +169,34 @@ def test_decode_input_prep_rejects_bad_arguments(lib, kw, want):
 
 def test_decode_input_prep_with_no_sequences_is_a_no_op(lib):
     assert _prep(lib, num_seqs=0, positions=None) == 0
+
+
+def _varlen(lib, cu=(0, 10, 30), k_lens=(10, 40), bt_stride=1, num_seqs=None, **kw):
+    import ctypes
+    B = len(k_lens) if num_seqs is None else num_seqs
+    cua = (ctypes.c_int32 * len(cu))(*cu)
+    ska = (ctypes.c_int32 * max(1, len(k_lens)))(*k_lens)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, page_stride=832 * 4 * 256, num_pages=64, bt=FAKE,
+             hq=24, hkv=4, d=256, bs=832, scale=0.0625, out=FAKE)
+    a.update(kw)
+    return lib.pa_prefill_varlen(a["q"], a["k"], a["v"], a["page_stride"], a["num_pages"],
+                                 a["bt"], bt_stride, cua, ska, B, 1, a["hq"], a["hkv"], a["d"],
+                                 a["bs"], a["scale"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(cu=(1, 10, 30)), PA_ERR_INVALID_ARG),          # must start at 0
+    (dict(cu=(0, 10, 5)), PA_ERR_INVALID_ARG),           # decreasing
+    (dict(k_lens=(5, 40)), PA_ERR_INVALID_ARG),          # 10 rows over 5 keys
+    (dict(k_lens=(10, 900)), PA_ERR_INVALID_ARG),        # 900 keys need 2 table entries
+    (dict(q=None), PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), PA_ERR_INVALID_ARG),
+    (dict(d=128, page_stride=832 * 4 * 128), PA_ERR_UNSUPPORTED),
+])
+def test_prefill_varlen_rejects_bad_arguments(lib, kw, want):
+    assert _varlen(lib, **kw) == want
+
+
+def test_prefill_varlen_without_rows_is_a_no_op(lib):
+    assert _varlen(lib, cu=(0, 0, 0), k_lens=(5, 7)) == 0
+    assert _varlen(lib, cu=(0,), k_lens=(), num_seqs=0) == 0

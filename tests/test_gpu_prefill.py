@@ -23,7 +23,7 @@ def _write_chunk(pa, case):
 
 def _oracle_caches_after_write(case, k_host, v_host):
     sl = oracle.slot_mapping(case.positions.cpu().numpy(), case.block_table.cpu().numpy(),
-                             case.block_size)
+                             case.block_size, seq_idx=case.seq_idx.cpu().numpy())
     oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_host, v_host, sl,
                              case.block_size)
     return k_host, v_host
@@ -124,3 +124,86 @@ def test_prefill_row_equals_decode_of_its_prefix(cuda_lib):
                     case.scale, q_start + q_len)
     d = (out[-1].float() - dec[0].float()).abs().max().item()
     assert d <= 1e-2
+
+
+# ------------------------------------------------------------------ mixed batches (varlen)
+VARLEN = [
+    # block size, chunk rows per sequence, keys per sequence, causal
+    (832, [130, 1, 257], [900, 1, 257], True),
+    (784, [64, 0, 300, 5], [784, 100, 1000, 5], True),
+    (16, [33, 70], [40, 200], False),
+    (64, [1, 2, 3, 200, 129, 128, 127], [1, 70, 64, 200, 500, 128, 1000], True),
+]
+
+
+@pytest.mark.parametrize("bs,q_rows,k_lens,causal", VARLEN)
+def test_prefill_varlen_every_element(cuda_lib, bs, q_rows, k_lens, causal):
+    pa = cuda_lib
+    npg = sum(-(-L // bs) for L in k_lens) + 3
+    case = workloads.paged_case(500 + sum(q_rows), k_lens, bs, npg, q_rows=q_rows, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    cu = case.meta["cu_seqlens_q"]
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            causal, case.scale)
+    ref = oracle.prefill_varlen(bits(case.q), k_host, v_host, case.block_table.cpu().numpy(),
+                                cu, k_lens, causal, case.scale)
+    assert_attention_close(out, ref, f"varlen bs={bs} {q_rows}")
+    assert pa.device_errors() == 0
+
+
+def test_prefill_varlen_more_chunks_than_one_launch_takes(cuda_lib):
+    # 45 non-empty chunks (and 2 empty ones) run as two launches of at most 32 chunks.
+    pa = cuda_lib
+    rng = np.random.default_rng(45)
+    k_lens = rng.integers(1, 300, 47).tolist()
+    q_rows = [int(rng.integers(1, L + 1)) for L in k_lens]
+    q_rows[5] = q_rows[30] = 0
+    bs = 64
+    npg = sum(-(-L // bs) for L in k_lens) + 2
+    case = workloads.paged_case(4545, k_lens, bs, npg, q_rows=q_rows, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    cu = case.meta["cu_seqlens_q"]
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            True, case.scale)
+    ref = oracle.prefill_varlen(bits(case.q), k_host, v_host, case.block_table.cpu().numpy(),
+                                cu, k_lens, True, case.scale)
+    assert_attention_close(out, ref, "varlen, 45 chunks")
+    assert pa.device_errors() == 0
+
+
+def test_prefill_varlen_of_one_sequence_is_prefill_chunk(cuda_lib):
+    pa = cuda_lib
+    case = workloads.paged_case(77, [1000], 832, 5, q_rows=700, q_start=300, device="cuda")
+    _write_chunk(pa, case)
+    a = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], 300, True,
+                         case.scale)
+    b = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, [0, 700],
+                          [1000], True, case.scale)
+    assert torch.equal(a, b)
+
+
+def test_prefill_mixed_batch_full_size_sampled(cuda_lib):
+    # Four chunks of a serving step (1024 rows over 3072 keys, 4096 over 8192, the 1685-row
+    # tail over 13973, a whole 512-token prompt): sampled rows of every chunk.
+    pa = cuda_lib
+    case = workloads.prefill_mixed("cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    cu, k_lens = case.meta["cu_seqlens_q"], case.meta["seq_lens"]
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            True, case.scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7317)
+    bt = case.block_table.cpu().numpy()
+    for b in range(len(k_lens)):
+        q_len = cu[b + 1] - cu[b]
+        rows = np.concatenate([[0, q_len - 1, min(127, q_len - 1), min(128, q_len - 1)],
+                               rng.integers(0, q_len, 40)]).astype(np.int32)
+        heads = rng.integers(0, 24, rows.size).astype(np.int32)
+        ref = oracle.prefill_rows(bits(case.q[cu[b]:cu[b + 1]]), k_host, v_host, bt[b],
+                                  k_lens[b] - q_len, True, case.scale, rows, heads)
+        got = out[torch.from_numpy(rows + cu[b]).long().cuda(), torch.from_numpy(heads).long().cuda()]
+        assert_attention_close(got, ref, f"mixed batch, chunk {b} (sampled)")
+    assert pa.device_errors() == 0

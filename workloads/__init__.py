@@ -100,7 +100,9 @@ def paged_case(seed, seq_lens, block_size, num_pages, *, q_rows=None, q_start=0,
 
     seq_lens   -- keys per sequence (each count includes that sequence's new tokens).
     q_rows     -- None for decode (one query row per sequence); an int for a prefill
-                  chunk of that many rows of sequence 0 at positions q_start.. .
+                  chunk of that many rows of sequence 0 at positions q_start.. ; a list
+                  (one count per sequence) for a mixed batch of chunks, each the last
+                  q_rows[s] keys of sequence s, stacked row-wise in q (meta["cu_seqlens_q"]).
     new_tokens -- decode: 1 means each sequence's last token (position seq_len-1) is
                   supplied as new_k/new_v and its slot starts out as NaN.  For a prefill
                   chunk the q_rows chunk tokens are always supplied this way.
@@ -134,6 +136,15 @@ def paged_case(seed, seq_lens, block_size, num_pages, *, q_rows=None, q_start=0,
         if new_tokens:
             case.positions = (sl - 1).to(torch.int32).to(device)
             case.seq_idx = torch.arange(S, dtype=torch.int32, device=device)
+    elif isinstance(q_rows, (list, tuple)):
+        if len(q_rows) != S or any(not 0 <= r <= L for r, L in zip(q_rows, seq_lens)):
+            raise ValueError("one chunk length per sequence, at most its key count")
+        cu = np.concatenate([[0], np.cumsum(q_rows)]).astype(np.int32)
+        case.q = _randn_bf16((int(cu[-1]), hq, head_dim), gen, device)
+        case.positions = torch.cat([torch.arange(L - r, L, dtype=torch.int32)
+                                    for r, L in zip(q_rows, seq_lens)]).to(device)
+        case.seq_idx = torch.cat([torch.full((r,), s, dtype=torch.int32)
+                                  for s, r in enumerate(q_rows)]).to(device)
     else:
         if S != 1 or q_start + q_rows != seq_lens[0]:
             raise ValueError("a prefill chunk is one sequence with q_start + q_rows keys")
@@ -154,6 +165,8 @@ def paged_case(seed, seq_lens, block_size, num_pages, *, q_rows=None, q_start=0,
         if case.positions is not None:
             if q_rows is None:
                 lens_before = sl - 1
+            elif isinstance(q_rows, (list, tuple)):
+                lens_before = sl - torch.tensor(q_rows, dtype=torch.int32)
             else:
                 lens_before = torch.tensor([q_start], dtype=torch.int32)
         _poison(k_cache, bt, lens_before.clamp(min=0), block_size, num_pages)
@@ -161,6 +174,8 @@ def paged_case(seed, seq_lens, block_size, num_pages, *, q_rows=None, q_start=0,
     case.meta = dict(seed=int(seed), seq_lens=seq_lens, block_size=block_size,
                      num_pages=num_pages, peaked_frac=peaked_frac, hq=hq, hkv=hkv,
                      head_dim=head_dim)
+    if isinstance(q_rows, (list, tuple)):
+        case.meta["cu_seqlens_q"] = [int(x) for x in np.concatenate([[0], np.cumsum(q_rows)])]
     return case
 
 
@@ -218,6 +233,14 @@ def prefill_first(device="cpu", block_size=832, num_pages=16):
     """The prompt's first chunk: q=4096 causal rows at positions 0..4095, no prior tokens."""
     return paged_case(1007, [4096], block_size, num_pages, q_rows=4096, q_start=0,
                       device=device)
+
+
+def prefill_mixed(device="cpu", block_size=832, num_pages=96):
+    """A mixed batch of chunked prefills, as a serving step schedules them: four
+    sequences whose chunks (1024, 4096, 1685 and 512 rows) sit at the end of 3072, 8192,
+    13973 and 512 keys."""
+    return paged_case(1008, [3072, 8192, 13973, 512], block_size, num_pages,
+                      q_rows=[1024, 4096, 1685, 512], device=device)
 
 
 def batched_decode(device="cpu", num_seqs=16, lo=4096, hi=32768, block_size=832,
