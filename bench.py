@@ -356,32 +356,53 @@ def input_prep_leg(pa, steps, warmup, flush):
 
 
 def e2e_leg(pa, case, steps, warmup, flush):
-    """The headline step through the public API with pinned host buffers: H2D of the
-    step's inputs (q, the new token's K/V, its position, the block table and seq_lens),
-    slot mapping + fused write + decode, D2H of the output."""
+    """The headline step through the public API with pinned host buffers: one H2D copy of
+    the step's inputs (q, the new token's K/V, its position, sequence index, block table
+    and seq_lens, packed in one pinned staging buffer), slot mapping + fused write +
+    decode, and the D2H copy of the output -- the whole step replayed from a CUDA graph,
+    as a serving loop would capture its decode step."""
     S, hq, d = case.q.shape
     msl = int(case.seq_lens.max())
-    host = {k: getattr(case, k).cpu().pin_memory()
-            for k in ("q", "new_k", "new_v", "positions", "seq_idx", "block_table", "seq_lens")}
-    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    names = ("q", "new_k", "new_v", "positions", "seq_idx", "block_table", "seq_lens")
+    srcs = {k: getattr(case, k).contiguous() for k in names}
+    offs, total = {}, 0
+    for k in names:  # 256-byte aligned slices of one staging buffer
+        offs[k] = total
+        total += (srcs[k].numel() * srcs[k].element_size() + 255) // 256 * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total, dtype=torch.uint8, device="cuda")
+
+    def view(buf, k):
+        t = srcs[k]
+        nb = t.numel() * t.element_size()
+        return buf[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
+    for k in names:  # the host fills the step's inputs into the staging buffer
+        view(stage_h, k).copy_(srcs[k].cpu())
+    dev = {k: view(stage_d, k) for k in names}
     out_h = torch.empty((S, hq, d), dtype=torch.bfloat16).pin_memory()
     out_d = torch.empty((S, hq, d), dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(max(256, pa.decode_workspace_size(S, hq, case.k_cache.shape[2], d,
                                                         case.block_size, msl)),
                      dtype=torch.uint8, device="cuda")
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    slots = torch.empty(S, dtype=torch.int64, device="cuda")
+    h2d = total
     d2h = out_h.numel() * out_h.element_size()
 
     def step():
-        for k, v in host.items():
-            dev[k].copy_(v, non_blocking=True)
-        slots = pa.slot_mapping(dev["positions"], dev["block_table"], case.block_size,
-                                seq_idx=dev["seq_idx"])
+        stage_d.copy_(stage_h, non_blocking=True)
+        pa.slot_mapping(dev["positions"], dev["block_table"], case.block_size,
+                        seq_idx=dev["seq_idx"], out=slots)
         pa.decode(dev["q"], case.k_cache, case.v_cache, dev["block_table"], dev["seq_lens"],
                   case.scale, msl, out=out_d, workspace=ws, new_k=dev["new_k"],
                   new_v=dev["new_v"], new_slots=slots)
         out_h.copy_(out_d, non_blocking=True)
-    ms = time_steps(step, steps, warmup, flush)
+    g = graph_of(step)
+    ms = time_steps(g.replay, steps, warmup, flush)
+    torch.cuda.synchronize()
+    ref = out_d.clone()
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref.cpu()), "the graph's D2H copy does not hold the step's output"
     return statistics.mean(ms), h2d, d2h
 
 

@@ -210,11 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[kQEmpty], 1);
         mbar_init(&bars[kSFull], 1);
         for (int i = 0; i < 4; ++i) {
-            mbar_init(&bars[kPFull + i], kSoftmaxWarps * 32);
+            mbar_init(&bars[kPFull + i], kSoftmaxWarps);  // one elected lane per warp
             mbar_init(&bars[kPvDone + i], 1);
-            mbar_init(&bars[kPair + i], 64);
+            mbar_init(&bars[kPair + i], 2);
         }
-        mbar_init(&bars[kOEmpty], kSoftmaxWarps * 32);
+        mbar_init(&bars[kOEmpty], kSoftmaxWarps);
         mbar_init(&bars[kDrain], 1);
         *abort = 0;
         fence_mbar_init();
@@ -392,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph = pc & 1;
             xq[ph * 64 + hf * 32 + lane] = v;
             tc_fence_before();
-            mbar_arrive(pair);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair);
             ok = wait_or_abort(pair, ph, p.err, abort);
             tc_fence_after();
             ++pc;
@@ -508,7 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_wait_st();
                     tc_fence_before();
-                    mbar_arrive(&bars[kPFull + qq]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kPFull + qq]);
                 }
             }
             if (stop) break;
@@ -544,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars[kOEmpty]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kOEmpty]);
             jt += it.n;
         }
     }
