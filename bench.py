@@ -448,24 +448,44 @@ def headline_case(device):
     return workloads.paged_case(1002, [8192], 832, 64, new_tokens=1, device=device)
 
 
+METRIC = "paged decode KV GB/s (% of HBM peak) at 4K-32K ctx; q=4096 prefill TFLOP/s"
+
+
+def headline_config(step_desc, ws):
+    return {"workload": HEADLINE, "block_size": 832, "context": 8192, "step": step_desc,
+            "parallelism": f"replica per GPU x{ws}"}
+
+
 def run_reference(args, rank, ws):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores, over the
+    headline workload: W untimed steps, then exactly K timed steps (each a full decode
+    step: slot mapping, KV write of the new token, exact attention of 24 heads over 8192
+    keys).  Under torchrun only rank 0 runs it."""
     if rank != 0:
         return
-    torch.manual_seed(0)
+    import oracle
     case = headline_case("cpu")
-    ch = host_case(case)
-    per_step, n, threads = cpu_oracle_timing(ch, seconds=max(1.0, args.cpu_seconds),
-                                             max_steps=args.steps + args.warmup)
-    nbytes = 8192 * KV_BYTES_PER_TOKEN
-    v = nbytes / per_step / 1e9
-    line = {"impl": "reference", "metric": "paged decode KV GB/s (batch 1, ctx 8192, bs 832)",
-            "value": v, "unit": "GB/s", "n_gpus": args.gpus, "steps": n, "warmup": 1,
+    step = oracle_step_fn(host_case(case))
+    for _ in range(max(1, args.warmup)):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    v = 8192 * KV_BYTES_PER_TOKEN / per_step / 1e9
+    threads = oracle.max_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": HEADLINE, "block_size": 832, "context": 8192},
+            "config": headline_config("fp64 CPU oracle: slot mapping + KV write of the new "
+                                      "token + exact attention", 1),
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n} full decode steps (slot mapping + KV write + "
-                                       f"fp64 attention of 24 heads over 8192 keys)"},
+                             "sample": f"{args.steps} full decode steps of the headline "
+                                       f"workload (slot mapping + KV write + fp64 attention "
+                                       f"of 24 heads over 8192 keys)"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -573,7 +593,7 @@ def main():
         return
     step_ms = statistics.mean(ms)
     line = {
-        "metric": "paged decode KV GB/s (% of HBM peak) at 4K-32K ctx; q=4096 prefill TFLOP/s",
+        "metric": METRIC,
         "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
