@@ -127,7 +127,7 @@ bool cached_cache_map(CUtensorMap *m, const MapKey &k) {
         CUtensorMap map;
         bool used;
     };
-    thread_local Entry entries[8] = {};
+    thread_local Entry entries[16] = {};
     thread_local int next = 0;
     for (auto &e : entries)
         if (e.used && e.key == k) {
@@ -138,7 +138,7 @@ bool cached_cache_map(CUtensorMap *m, const MapKey &k) {
                         k.page_stride, k.box_rows))
         return false;
     entries[next] = Entry{k, *m, true};
-    next = (next + 1) % 8;
+    next = (next + 1) % 16;
     return true;
 }
 
@@ -322,12 +322,25 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
     if (workspace_bytes < pa::decode_workspace_bytes(num_seqs, num_q_heads, plan))
         return PA_ERR_INVALID_ARG;
 
-    CUtensorMap tk, tv;
-    if (!cached_cache_map(&tk, MapKey{k_cache, head_dim, num_kv_heads, block_size, pa::kDecTile,
-                                      num_pages, page_stride}) ||
-        !cached_cache_map(&tv, MapKey{v_cache, head_dim, num_kv_heads, block_size, pa::kDecTile,
-                                      num_pages, page_stride}))
+    // Stage-wide boxes, plus tile-high boxes when a page holds an odd number of tiles (a
+    // stage may then straddle two pages).  With one tile per page the stage-wide maps are
+    // never used and take tile-high boxes too.
+    CUtensorMap maps[4];
+    const int box_rows = plan.tiles_per_page > 1 ? pa::kDecBoxRows : pa::kDecTile;
+    if (!cached_cache_map(&maps[0], MapKey{k_cache, head_dim, num_kv_heads, block_size,
+                                           box_rows, num_pages, page_stride}) ||
+        !cached_cache_map(&maps[1], MapKey{v_cache, head_dim, num_kv_heads, block_size,
+                                           box_rows, num_pages, page_stride}))
         return PA_ERR_CUDA;
+    if (plan.tiles_per_page % pa::kDecPair == 0) {
+        maps[2] = maps[0];
+        maps[3] = maps[1];
+    } else if (!cached_cache_map(&maps[2], MapKey{k_cache, head_dim, num_kv_heads, block_size,
+                                                  pa::kDecTile, num_pages, page_stride}) ||
+               !cached_cache_map(&maps[3], MapKey{v_cache, head_dim, num_kv_heads, block_size,
+                                                  pa::kDecTile, num_pages, page_stride})) {
+        return PA_ERR_CUDA;
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     pa::DecodeArgs a;
@@ -356,7 +369,7 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
     if (diag_enabled())
         fprintf(stderr, "[pa] decode: seqs=%d max_seq_len=%d bs=%d splits=%d tiles/split=%d\n",
                 num_seqs, max_seq_len, block_size, plan.num_splits, plan.tiles_per_split);
-    return pa::launch_decode(tk, tv, a, plan, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return pa::launch_decode(maps, a, plan, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 // One prefill launch over 1 .. kPfMaxSeqs chunks whose rows lie in q / out of total_q rows.

@@ -8,15 +8,20 @@
 //   * grid = (splits, KV heads, sequences).  A CTA owns a contiguous run of page-local
 //     16-token tiles of one (sequence, KV head) and all G <= 8 query heads of that KV
 //     head, so each K/V byte is read from HBM once for the whole group.
-//   * One producer warp walks the block table once per tile and issues TMA box loads
-//     (4 x 128-byte-swizzled boxes of 16 rows for K, 4 for V) into a 14-stage ring;
-//     tiles never straddle a page, and rows past the page end (block_size 784 leaves a
-//     16-token tail tile) come back as zeros and are masked.
-//   * Seven consumer warps take tiles round-robin (tile i -> warp i % 7, stage i % 14).
-//     Per tile: S^T = K Q^T on the tensor cores (mma.m16n8k16, tokens as M, the group's
-//     heads as N, two accumulator chains), online softmax over tokens with warp
-//     shuffles, then O^T += V^T P^T with P split into a BF16 high part and a BF16 low
-//     part (two MMAs), which keeps P to ~16 significant bits.
+//   * Tiles are 16 page-local tokens; a ring stage holds two consecutive tiles (32 KB).
+//     One producer thread reads each block-table entry once and issues the stage's TMA
+//     loads: 4 x 128-byte-swizzled boxes of 32 rows for K and 4 for V.  A TMA box costs
+//     the SM about the same issue time whatever its height up to 64 rows, and 16-row
+//     boxes capped an SM below its share of HBM bandwidth; 32-row boxes do not.  When
+//     a page holds an odd number of tiles, a stage whose two tiles lie in different
+//     pages is loaded with 16-row boxes.  Rows past a page end come back as zeros and
+//     are masked.
+//   * Seven consumer warps take stages round-robin (stage m -> warp m % 7, ring slot
+//     m % 7), each processing its stage's two tiles in order.  Per tile: S^T = K Q^T
+//     on the tensor cores (mma.m16n8k16, tokens as M, the group's heads as N, two
+//     accumulator chains), online softmax over tokens with warp shuffles, then
+//     O^T += V^T P^T with P split into a BF16 high part and a BF16 low part (two MMAs),
+//     which keeps P to ~16 significant bits.
 //   * At the end the warps merge their (max, sum, acc) through shared memory and the
 //     CTA writes one fp32 partial per query head; the combine kernel merges the splits
 //     with a log-sum-exp and writes BF16.  Both kernels use programmatic dependent
@@ -31,16 +36,15 @@ namespace pa {
 namespace {
 
 constexpr int kDecThreads = (kDecConsumers + 1) * 32;
-constexpr int kDecChunkBytes = kDecTile * 128;             // one 64-dim box: 16 rows x 128 B
-constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one tile: 8 KB
-constexpr int kDecStageBytes = 2 * kDecHalf;                // 16 KB
+constexpr int kDecTileBytes = kDecTile * 128;               // one tile's rows of a 64-dim chunk
+constexpr int kDecChunkBytes = kDecBoxRows * 128;           // one 64-dim chunk of a stage: 4 KB
+constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one stage: 16 KB
+constexpr int kDecStageBytes = 2 * kDecHalf;                // 32 KB
 constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 224 KB
 // Merge buffers, per warp and head: O row (padded by 4 floats, so that the 4 head
-// columns a warp stores at once fall in different banks), max, sum, weight; per head:
-// CTA max and sum.
+// columns a warp stores at once fall in different banks), max and sum.
 constexpr int kDecMergeRow = kHeadDim + 4;
-constexpr int kDecMergeBytes =
-    (kDecConsumers * kDecMaxGroup * (kDecMergeRow + 3) + 2 * kDecMaxGroup) * 4;
+constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kDecMergeRow + 2) * 4;
 static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
 constexpr int kDecSmemBytes = 1024 + kDecRingBytes + (2 * kDecStages + 1) * 8;
 constexpr int kCombineThreads = kHeadDim;
@@ -103,6 +107,45 @@ __device__ __forceinline__ void write_newest_token(const DecodeKParams &p, const
     if (lane == 0) mbar_arrive(written);
 }
 
+// The decode's four tensor maps: K and V with 32-row boxes, and with 16-row boxes.
+struct DecMaps {
+    CUtensorMap k, v, k16, v16;
+};
+
+// Loads rows [off, off + 32) of page `page` (K and V of KV head g: both tiles of a
+// stage that lies in one page) into ring stage `st`, completing on `bar`.  Rows past the
+// page end, and a page outside the pool, read as zeros.
+__device__ __forceinline__ void load_stage(const DecMaps &mp, uint8_t *st, uint64_t *bar, int g,
+                                           int off, int page) {
+    mbar_arrive_expect_tx(bar, kDecStageBytes);
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(st + c * kDecChunkBytes, &mp.k, bar, c * kChunkElems, g, off, page);
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(st + kDecHalf + c * kDecChunkBytes, &mp.v, bar, c * kChunkElems, g, off,
+                    page);
+}
+
+// Loads a stage whose first tile is rows [off, off + 16) of `page` (that page's last
+// tile) and whose second tile is rows [0, 16) of `page2`, with 16-row boxes.
+__device__ __forceinline__ void load_stage_split(const DecMaps &mp, uint8_t *st, uint64_t *bar,
+                                                 int g, int off, int page, int page2) {
+    mbar_arrive_expect_tx(bar, kDecStageBytes);
+#pragma unroll
+    for (int h = 0; h < kDecPair; ++h) {
+        const int o = h == 0 ? off : 0, pg = h == 0 ? page : page2;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(st + c * kDecChunkBytes + h * kDecTileBytes, &mp.k16, bar,
+                        c * kChunkElems, g, o, pg);
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(st + kDecHalf + c * kDecChunkBytes + h * kDecTileBytes, &mp.v16, bar,
+                        c * kChunkElems, g, o, pg);
+    }
+}
+
 __device__ __forceinline__ int seq_tiles(int seq_len, int block_size, int tiles_per_page) {
     const int full = seq_len / block_size;
     const int rem = seq_len - full * block_size;
@@ -123,8 +166,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1)
-    decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const DecodeKParams p) {
+    decode_split_kernel(const __grid_constant__ DecMaps maps, const DecodeKParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,48 +187,87 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         fence_mbar_init();
     }
     if (warp == kDecConsumers && lane == 0) {
-        tma_prefetch_desc(&tmk);
-        tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(&maps.v);
+        tma_prefetch_desc(&maps.k16);
+        tma_prefetch_desc(&maps.v16);
     }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
 
     const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
-    const int t0 = split * p.tiles_per_split;
+    const int tpp = p.tiles_per_page;
+    const int t0 = split * p.tiles_per_split;  // a multiple of kDecPair
+    const int lp0 = t0 / tpp;
+    const int tip0 = t0 - lp0 * tpp;
+    const int off0 = tip0 * kDecTile;
+    const bool producer = warp == kDecConsumers && lane == 0;
+    // The producer loads the split's first stage before the sequence length is known, so
+    // that the block-table read and the sequence-length read overlap instead of following
+    // one another.  t0 lies below the tile count of the longest allowed sequence and a
+    // block-table row holds that many pages, so the read stays inside the table.  Past the
+    // sequence's end the entry may hold anything; a page outside the pool only makes the
+    // boxes read as zeros, and such a tile is never consumed.  A first stage that would
+    // straddle two pages waits for the length instead.
+    const bool spec = tip0 + 1 < tpp;
+    int page0 = 0;
+    if (producer) page0 = bt[lp0];
     const int seq_len = checked_seq_len(p, seq, threadIdx.x == 0 && split == 0 && g == 0);
-    const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
+    if (producer && spec) load_stage(maps, smem, &full[0], g, off0, page0);
+    const int ntiles = seq_tiles(seq_len, p.block_size, tpp);
     const int t1 = min(ntiles, t0 + p.tiles_per_split);
-    if (t0 >= t1) return;  // this split has no tiles of this sequence (CTA-uniform)
-    const int n = t1 - t0;
+    if (t0 >= t1) {
+        // This split has no tiles of this sequence (CTA-uniform): the first stage's load
+        // lands before the CTA exits.
+        if (producer && spec) mbar_wait(&full[0], 0, p.err);
+        return;
+    }
+    const int n = t1 - t0;                            // tiles of this split
+    const int nst = (n + kDecPair - 1) / kDecPair;    // stages of this split
     // This CTA holds the tile of the token being decoded and has to write that token.
     const bool writes_newest = p.new_slots != nullptr && t1 == ntiles;
 
     if (warp == kDecConsumers) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            for (int i = 0; i < n; ++i) {
-                const int s = i % kDecStages;
-                if (i >= kDecStages &&
-                    !mbar_wait(&empty[s], ((i / kDecStages) - 1) & 1, p.err))
+            // A page outside the pool is reported; the TMA boxes then lie outside the
+            // tensor and read as zeros, so nothing faults.
+            if (page0 < 0 || page0 >= p.num_pages) atomicOr(p.err, kErrPage);
+            // Block-table entries are read once per page and one page ahead, never
+            // between two loads of the ring.
+            const int lp_last = (t1 - 1) / tpp;
+            int lp = lp0, page = page0;
+            int page_next = lp0 < lp_last ? bt[lp0 + 1] : 0;
+            for (int m = spec ? 1 : 0; m < nst; ++m) {
+                const int s = m % kDecStages;
+                if (m >= kDecStages &&
+                    !mbar_wait(&empty[s], ((m / kDecStages) - 1) & 1, p.err))
                     break;
-                const int j = t0 + i;
-                const int lp = j / p.tiles_per_page;
-                const int off = (j - lp * p.tiles_per_page) * kDecTile;
-                // The last tile holds the token being decoded: wait until it is written.
-                if (writes_newest && i == n - 1 && !mbar_wait(written, 0, p.err)) break;
-                const int page = bt[lp];
-                // A page outside the pool is reported; the TMA box then lies outside the
-                // tensor and reads as zeros, so nothing faults.
-                if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrPage);
+                const int j = t0 + m * kDecPair;
+                const int l = j / tpp;
+                const int tip = j - l * tpp;
+                if (l != lp) {
+                    // Usually the next page; with one tile per page a stage spans two
+                    // pages and the next stage starts two pages further on.
+                    page = l == lp + 1 ? page_next : bt[l];
+                    lp = l;
+                    if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrPage);
+                    if (lp < lp_last) page_next = bt[lp + 1];
+                }
+                // The last stage holds the token being decoded: wait until it is written.
+                if (writes_newest && m == nst - 1 && !mbar_wait(written, 0, p.err)) break;
                 uint8_t *st = smem + s * kDecStageBytes;
-                mbar_arrive_expect_tx(&full[s], kDecStageBytes);
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    tma_load_4d(st + c * kDecChunkBytes, &tmk, &full[s], c * kChunkElems, g,
-                                off, page);
-                    tma_load_4d(st + kDecHalf + c * kDecChunkBytes, &tmv, &full[s],
-                                c * kChunkElems, g, off, page);
+                if (tip + 1 < tpp) {
+                    load_stage(maps, st, &full[s], g, tip * kDecTile, page);
+                } else {
+                    // The first tile closes its page: the second opens the next page, or
+                    // lies past the split's end and reads as zeros from page -1.
+                    const bool second = j + 1 < t1;
+                    if (second && (page_next < 0 || page_next >= p.num_pages))
+                        atomicOr(p.err, kErrPage);
+                    load_stage_split(maps, st, &full[s], g, tip * kDecTile, page,
+                                     second ? page_next : -1);
                 }
             }
         }
@@ -221,21 +302,34 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int r_lo = lane >> 2;  // token rows r_lo and r_lo + 8 of the tile
 
-    for (int i = warp; i < n; i += kDecConsumers) {
-        const int s = i % kDecStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kDecStages) & 1, p.err))) break;
-        const int j = t0 + i;
-        const int lp = j / p.tiles_per_page;
-        const int off = (j - lp * p.tiles_per_page) * kDecTile;
+    for (int m = warp; m < nst; m += kDecConsumers) {
+        const int s = m % kDecStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (m / kDecStages) & 1, p.err))) break;
+        if (writes_newest && nst == 1 && spec) {
+            // The only stage (m = 0, warp 0) holds the token being decoded and was loaded
+            // before that token was written: load it again once the write is done.
+            bool issued = false;
+            if (lane == 0 && mbar_wait(written, 0, p.err)) {
+                load_stage(maps, smem, &full[0], g, off0, bt[lp0]);
+                issued = true;
+            }
+            if (!__shfl_sync(0xffffffffu, issued, 0) ||
+                !__all_sync(0xffffffffu, mbar_wait(&full[0], 1, p.err)))
+                break;
+        }
+        for (int h = 0; h < kDecPair && m * kDecPair + h < n; ++h) {
+        const int j = t0 + m * kDecPair + h;
+        const int lp = j / tpp;
+        const int off = (j - lp * tpp) * kDecTile;
         const int tok0 = lp * p.block_size + off;
         const int nvalid = min(kDecTile, min(p.block_size - off, seq_len - tok0));
-        const uint32_t kb = sbase + s * kDecStageBytes;
+        const uint32_t kb = sbase + s * kDecStageBytes + h * kDecTileBytes;
         const uint32_t vb = kb + kDecHalf;
 
         if (nvalid < kDecTile) {
             // Rows past the sequence end may hold anything (even NaN): zero them in V
             // so that a zero weight cannot meet a NaN inside the MMA.
-            uint8_t *vp = smem + s * kDecStageBytes + kDecHalf;
+            uint8_t *vp = smem + s * kDecStageBytes + kDecHalf + h * kDecTileBytes;
             const int per_chunk = (kDecTile - nvalid) * 8;
             for (int u = lane; u < per_chunk * kChunks; u += 32) {
                 const int c = u / per_chunk;
@@ -321,6 +415,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
         }
+        }  // tiles of the stage
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -355,36 +450,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
     }
     named_bar_sync(1, kDecConsumers * 32);
-    // The CTA's running max per head and each warp's weight exp2(m_w - M), once per head.
-    float *red_e = red_l + kDecConsumers * kDecMaxGroup;  // [warp][head]
-    float *cta_m = red_e + kDecConsumers * kDecMaxGroup;  // [head]
-    float *cta_l = cta_m + kDecMaxGroup;                  // [head]
-    if (threadIdx.x < p.group) {
-        const int c = threadIdx.x;
-        float M = -CUDART_INF_F;
+    // Thread t merges the quads (4 consecutive dims of one head) t, t + 224, ...  Every
+    // thread derives its head's CTA max and the warps' weights exp2(m_w - M) itself, so
+    // no further barrier is needed and all loads of a quad are independent.
+    constexpr int kQuadsPerHead = kHeadDim / 4;
+    constexpr int kMergeThreads = kDecConsumers * 32;
+    const int nquads = p.group * kQuadsPerHead;
 #pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, red_m[w * kDecMaxGroup + c]);
-        float L = 0.f;
+    for (int k = 0; k < (kDecMaxGroup * kQuadsPerHead + kMergeThreads - 1) / kMergeThreads;
+         ++k) {
+        const int q = threadIdx.x + k * kMergeThreads;
+        if (q < nquads) {
+            const int c = q / kQuadsPerHead, d = (q - c * kQuadsPerHead) * 4;
+            float mw[kDecConsumers];
+            float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w) {
-            const float e = M == -CUDART_INF_F ? 0.f : exp2f(red_m[w * kDecMaxGroup + c] - M);
-            red_e[w * kDecMaxGroup + c] = e;
-            L += e * red_l[w * kDecMaxGroup + c];
+            for (int w = 0; w < kDecConsumers; ++w) {
+                mw[w] = red_m[w * kDecMaxGroup + c];
+                M = fmaxf(M, mw[w]);
+            }
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kDecConsumers; ++w) {
+                const float e = M == -CUDART_INF_F ? 0.f : exp2f(mw[w] - M);
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    red_o + (w * kDecMaxGroup + c) * kDecMergeRow + d);
+                L += e * red_l[w * kDecMaxGroup + c];
+                O.x += e * v.x;
+                O.y += e * v.y;
+                O.z += e * v.z;
+                O.w += e * v.w;
+            }
+            const int64_t pi =
+                ((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split;
+            *reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim + d) = O;
+            if (d == 0) p.part_ml[pi] = make_float2(M, L);
         }
-        cta_m[c] = M;
-        cta_l[c] = L;
-    }
-    named_bar_sync(1, kDecConsumers * 32);
-    for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += kDecConsumers * 32) {
-        const int c = idx / kHeadDim, d = idx - c * kHeadDim;
-        float O = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w)
-            O += red_e[w * kDecMaxGroup + c] * red_o[(w * kDecMaxGroup + c) * kDecMergeRow + d];
-        const int64_t pi =
-            ((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split;
-        p.part_o[pi * kHeadDim + d] = O;
-        if (d == 0) p.part_ml[pi] = make_float2(cta_m[c], cta_l[c]);
     }
 }
 
@@ -481,13 +583,15 @@ DecodePlan plan_decode(int num_seqs, int num_kv_heads, int block_size, int max_s
     const int rem = max_seq_len - full * block_size;
     pl.max_tiles = full * pl.tiles_per_page + (rem + kDecTile - 1) / kDecTile;
     const long long pairs = (long long)num_seqs * num_kv_heads;
-    // One CTA per SM across all (sequence, KV head) pairs, at least one tile per warp.
+    // One CTA per SM across all (sequence, KV head) pairs, whole stages per CTA and at
+    // least 8 tiles (4 stages) each.
     long long want = (num_sms + pairs - 1) / pairs;
     if (want < 1) want = 1;
     int tps = (int)((pl.max_tiles + want - 1) / want);
-    if (tps < kDecConsumers) tps = kDecConsumers;
+    if (tps < 8) tps = 8;
     if ((pl.max_tiles + tps - 1) / tps > kDecMaxSplits)
         tps = (pl.max_tiles + kDecMaxSplits - 1) / kDecMaxSplits;
+    tps = (tps + kDecPair - 1) / kDecPair * kDecPair;
     pl.tiles_per_split = tps;
     pl.num_splits = (pl.max_tiles + tps - 1) / tps;
     return pl;
@@ -500,8 +604,8 @@ size_t decode_workspace_bytes(int num_seqs, int num_q_heads, const DecodePlan &p
     return o_bytes + ml_bytes;
 }
 
-cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                          const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const DecodePlan &plan,
+                          cudaStream_t stream) {
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_split_kernel),
                                   kDecSmemBytes, 0);
     if (e != cudaSuccess) return e;
@@ -534,8 +638,12 @@ cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
     p.num_kv_heads = a.num_kv_heads;
     const dim3 grid(plan.num_splits, a.num_kv_heads, a.num_seqs);
     if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
-    e = launch_pdl(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream, tmap_k,
-                   tmap_v, p);
+    DecMaps maps;
+    maps.k = tmaps[0];
+    maps.v = tmaps[1];
+    maps.k16 = tmaps[2];
+    maps.v16 = tmaps[3];
+    e = launch_pdl(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream, maps, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, stream)) != cudaSuccess) return e;
     return launch_pdl(decode_combine_kernel, dim3(a.num_q_heads, a.num_seqs),

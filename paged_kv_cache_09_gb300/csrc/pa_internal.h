@@ -64,13 +64,15 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
                                      unsigned *err, cudaStream_t stream);
 
 // ----------------------------------------------------------------- decode
-constexpr int kDecTile = 16;       // tokens per pipeline stage (page-local)
-constexpr int kDecStages = 14;     // shared-memory ring depth
+constexpr int kDecTile = 16;       // tokens per MMA tile (page-local)
+constexpr int kDecPair = 2;        // tiles per ring stage
+constexpr int kDecBoxRows = kDecTile * kDecPair;  // rows of the stage-wide TMA boxes
+constexpr int kDecStages = 7;      // shared-memory ring depth (32 KB stages)
 constexpr int kDecConsumers = 7;   // consumer warps per CTA (plus one producer warp)
-// Tile i uses stage i % kDecStages and is consumed by warp i % kDecConsumers.  An
-// mbarrier wait only tells the last two phases apart, so every stage must always be
-// consumed by the same warp (which then waits on it in order): the ring depth is a
-// multiple of the consumer count.
+// Stage m holds tiles 2m and 2m + 1 of the split, uses ring slot m % kDecStages and is
+// consumed by warp m % kDecConsumers.  An mbarrier wait only tells the last two phases
+// apart, so every slot must always be consumed by the same warp (which then waits on it
+// in order): the ring depth is a multiple of the consumer count.
 static_assert(kDecStages % kDecConsumers == 0, "stage -> warp mapping must be fixed");
 constexpr int kDecMaxSplits = 1024;  // upper bound on CTAs per (sequence, KV head)
 constexpr int kDecMaxGroup = 8;    // query heads per KV head handled by one MMA column tile
@@ -78,7 +80,7 @@ constexpr int kDecMaxGroup = 8;    // query heads per KV head handled by one MMA
 struct DecodePlan {
     int tiles_per_page;   // ceil(block_size / kDecTile)
     int max_tiles;        // tiles of the longest allowed sequence
-    int tiles_per_split;  // tiles one CTA processes
+    int tiles_per_split;  // tiles one CTA processes (a multiple of kDecPair)
     int num_splits;       // CTAs per (sequence, KV head)
 };
 
@@ -107,8 +109,11 @@ struct DecodeArgs {
     int64_t page_stride;            // elements between consecutive pages
 };
 
-cudaError_t launch_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                          const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+// tmaps: K and V with kDecBoxRows-row boxes, then K and V with kDecTile-row boxes (used
+// for a stage whose two tiles lie in different pages; the first two again when a page
+// holds an even number of tiles, since then no stage straddles a page).
+cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const DecodePlan &plan,
+                          cudaStream_t stream);
 
 // ----------------------------------------------------------------- prefill
 constexpr int kPfQRows = 128;      // query rows per work item (one TMEM lane each)

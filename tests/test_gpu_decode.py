@@ -48,6 +48,29 @@ def test_tiny_decode_with_fused_new_token_write(cuda_lib):
     assert pa.device_errors() == 0
 
 
+@pytest.mark.parametrize("seq_len", [1665 + 16 * k for k in range(-7, 7)] + [1696])
+def test_fused_write_when_the_newest_tile_starts_a_split(cuda_lib, seq_len):
+    # The kernel loads each split's first tile before it knows the sequence length.  When
+    # that tile is also the one holding the token being decoded (the split's only tile),
+    # it has to be loaded again after the fused write; the slot starts as NaN, so a stale
+    # copy shows in the output.  These lengths put the last split at every tile count
+    # modulo 7 (the smallest split length), with the token on the first row of its tile
+    # (and, for 1696, on the last row).
+    pa = cuda_lib
+    case = workloads.paged_case(73, [seq_len], 832, 8, new_tokens=1, device="cuda")
+    k_ref, v_ref = bits(case.k_cache).copy(), bits(case.v_cache).copy()
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_ref, v_ref,
+                             oracle.slot_mapping(case.positions.cpu().numpy(),
+                                                 case.block_table.cpu().numpy(), 832,
+                                                 case.seq_idx.cpu().numpy()), 832)
+    slots = pa.slot_mapping(case.positions, case.block_table, 832, seq_idx=case.seq_idx)
+    out = _gpu_decode(pa, case, new_k=case.new_k, new_v=case.new_v, new_slots=slots)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(case.k_cache), k_ref) and np.array_equal(bits(case.v_cache), v_ref)
+    assert_attention_close(out, _oracle_decode(case, k_ref, v_ref), f"fused write, L={seq_len}")
+    assert pa.device_errors() == 0
+
+
 @pytest.mark.parametrize("bs", [832, 784])
 def test_decode_8k(cuda_lib, bs):
     pa = cuda_lib
