@@ -50,12 +50,12 @@ def test_tiny_decode_with_fused_new_token_write(cuda_lib):
 
 @pytest.mark.parametrize("seq_len", [1665 + 16 * k for k in range(-7, 7)] + [1696])
 def test_fused_write_when_the_newest_tile_starts_a_split(cuda_lib, seq_len):
-    # The kernel loads each split's first tile before it knows the sequence length.  When
-    # that tile is also the one holding the token being decoded (the split's only tile),
-    # it has to be loaded again after the fused write; the slot starts as NaN, so a stale
-    # copy shows in the output.  These lengths put the last split at every tile count
-    # modulo 7 (the smallest split length), with the token on the first row of its tile
-    # (and, for 1696, on the last row).
+    # The kernel loads each split's first stage (two 16-token tiles) before it knows the
+    # sequence length.  When that stage also holds the token being decoded (the split's
+    # only stage), it has to be loaded again after the fused write; the slot starts as
+    # NaN, so a stale copy shows in the output.  These 14 consecutive tile counts put the
+    # last split at every length modulo 8 (the smallest split length), with the token on
+    # the first row of its tile (and, for 1696, on the last row).
     pa = cuda_lib
     case = workloads.paged_case(73, [seq_len], 832, 8, new_tokens=1, device="cuda")
     k_ref, v_ref = bits(case.k_cache).copy(), bits(case.v_cache).copy()
