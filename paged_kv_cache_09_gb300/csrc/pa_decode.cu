@@ -16,8 +16,9 @@
 //     a page holds an odd number of tiles, a stage whose two tiles lie in different
 //     pages is loaded with 16-row boxes.  Rows past a page end come back as zeros and
 //     are masked.
-//   * Seven consumer warps take stages round-robin (stage m -> warp m % 7, ring slot
-//     m % 7), each processing its stage's two tiles in order.  Per tile: S^T = K Q^T
+//   * Seven consumer warps take tiles round-robin (tile i -> warp i % 7, half i % 2 of
+//     ring slot (i / 2) % 7; a slot is released by the warps of both its tiles).  Per
+//     tile: S^T = K Q^T
 //     on the tensor cores (mma.m16n8k16, tokens as M, the group's heads as N, two
 //     accumulator chains), online softmax over tokens with warp shuffles, then
 //     O^T += V^T P^T with P split into a BF16 high part and a BF16 low part (two MMAs),
@@ -47,6 +48,8 @@ constexpr int kDecMergeRow = kHeadDim + 4;
 constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kDecMergeRow + 2) * 4;
 static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
 constexpr int kDecSmemBytes = 1024 + kDecRingBytes + (2 * kDecStages + 1) * 8;
+// Splits of at most this many tiles hand out single tiles to the consumer warps.
+constexpr int kDecPerTileMaxTiles = 64;
 constexpr int kCombineThreads = kHeadDim;
 
 struct DecodeKParams {
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kDecPair);  // released by the warps of both tiles
         }
         mbar_init(written, 1);
         fence_mbar_init();
@@ -227,6 +230,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int nst = (n + kDecPair - 1) / kDecPair;    // stages of this split
     // This CTA holds the tile of the token being decoded and has to write that token.
     const bool writes_newest = p.new_slots != nullptr && t1 == ntiles;
+    // ... and if that tile is in the stage loaded ahead, the stage is loaded twice.
+    const bool refetch = writes_newest && spec && nst == 1;
 
     if (warp == kDecConsumers) {
         // ------------------------------------------------------------ producer
@@ -239,6 +244,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const int lp_last = (t1 - 1) / tpp;
             int lp = lp0, page = page0;
             int page_next = lp0 < lp_last ? bt[lp0 + 1] : 0;
+            if (refetch) {
+                // The split's only stage holds the token being decoded and was loaded
+                // before that token was written: load it again once the first load has
+                // landed and the write is done.  Its consumers wait for both loads.
+                if (mbar_wait(&full[0], 0, p.err) && mbar_wait(written, 0, p.err))
+                    load_stage(maps, smem, &full[0], g, off0, page0);
+            }
             for (int m = spec ? 1 : 0; m < nst; ++m) {
                 const int s = m % kDecStages;
                 if (m >= kDecStages &&
@@ -302,23 +314,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int r_lo = lane >> 2;  // token rows r_lo and r_lo + 8 of the tile
 
-    for (int m = warp; m < nst; m += kDecConsumers) {
-        const int s = m % kDecStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (m / kDecStages) & 1, p.err))) break;
-        if (writes_newest && nst == 1 && spec) {
-            // The only stage (m = 0, warp 0) holds the token being decoded and was loaded
-            // before that token was written: load it again once the write is done.
-            bool issued = false;
-            if (lane == 0 && mbar_wait(written, 0, p.err)) {
-                load_stage(maps, smem, &full[0], g, off0, bt[lp0]);
-                issued = true;
-            }
-            if (!__shfl_sync(0xffffffffu, issued, 0) ||
-                !__all_sync(0xffffffffu, mbar_wait(&full[0], 1, p.err)))
-                break;
-        }
-        for (int h = 0; h < kDecPair && m * kDecPair + h < n; ++h) {
-        const int j = t0 + m * kDecPair + h;
+    // Tile i of the split, held in half h of ring slot s.
+    auto tile = [&](int s, int h, int i) {
+        const int j = t0 + i;
         const int lp = j / tpp;
         const int off = (j - lp * tpp) * kDecTile;
         const int tok0 = lp * p.block_size + off;
@@ -415,9 +413,35 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
         }
-        }  // tiles of the stage
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+    };
+
+    // Short splits (the tail of the stream is a large share of their time): tile i is
+    // consumed by warp i % 7 from half i % 2 of stage i / 2 (ring slot (i / 2) % 7), so the
+    // two tiles of a stage are processed in parallel.  Within a ring round of 14 tiles
+    // every (warp, slot, half) is fixed, so each warp waits on its two slots alternately
+    // and in phase order.  Long splits: stage m is consumed whole by warp m % 7, which
+    // measured faster over long streams.  The choice is CTA-uniform; a slot is released
+    // by two arrivals either way.
+    if (n <= kDecPerTileMaxTiles) {
+        for (int i = warp; i < n; i += kDecConsumers) {
+            const int m = i / kDecPair, h = i - m * kDecPair;
+            const int s = m % kDecStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (m / kDecStages) & 1, p.err)))
+                break;
+            if (refetch && !__all_sync(0xffffffffu, mbar_wait(&full[0], 1, p.err))) break;
+            tile(s, h, i);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    } else {
+        for (int m = warp; m < nst; m += kDecConsumers) {
+            const int s = m % kDecStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (m / kDecStages) & 1, p.err)))
+                break;
+            for (int h = 0; h < kDecPair && m * kDecPair + h < n; ++h) tile(s, h, m * kDecPair + h);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s], kDecPair);
+        }
     }
 
 #pragma unroll

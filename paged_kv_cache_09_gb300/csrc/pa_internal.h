@@ -69,11 +69,12 @@ constexpr int kDecPair = 2;        // tiles per ring stage
 constexpr int kDecBoxRows = kDecTile * kDecPair;  // rows of the stage-wide TMA boxes
 constexpr int kDecStages = 7;      // shared-memory ring depth (32 KB stages)
 constexpr int kDecConsumers = 7;   // consumer warps per CTA (plus one producer warp)
-// Stage m holds tiles 2m and 2m + 1 of the split, uses ring slot m % kDecStages and is
-// consumed by warp m % kDecConsumers.  An mbarrier wait only tells the last two phases
-// apart, so every slot must always be consumed by the same warp (which then waits on it
-// in order): the ring depth is a multiple of the consumer count.
-static_assert(kDecStages % kDecConsumers == 0, "stage -> warp mapping must be fixed");
+// Stage m holds tiles 2m and 2m + 1 of the split and uses ring slot m % kDecStages; tile
+// i is consumed by warp i % kDecConsumers.  An mbarrier wait only tells the last two
+// phases apart, so a warp must visit each of its slots once per ring round, in phase
+// order: with a ring round of kDecStages * kDecPair tiles a multiple of the consumer
+// count, every (tile of the round) -> (warp, slot, half) assignment is fixed.
+static_assert((kDecStages * kDecPair) % kDecConsumers == 0, "tile -> warp mapping must be fixed");
 constexpr int kDecMaxSplits = 1024;  // upper bound on CTAs per (sequence, KV head)
 constexpr int kDecMaxGroup = 8;    // query heads per KV head handled by one MMA column tile
 
