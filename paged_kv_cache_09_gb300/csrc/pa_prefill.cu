@@ -252,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(qs + c * kQChunk, &maps.q, &bars[kQFull], c * kChunkElems, it.h,
                                 it.q_off + it.r0);
                 const int32_t *bt = p.block_table + (int64_t)it.bt_row * p.bt_stride;
+                // Page and in-page index of block kb, advanced block by block: a division
+                // here would take the MUFU, which the softmax warps keep busy.
+                int blk_lp = 0, blk_in = 0;
                 for (int j = 0; j < it.n && !stop; ++j) {
                     // Page, offset and map of each of the tile's four blocks; blocks past the
                     // item's last are read from outside the pool (zeros) and masked.
@@ -260,8 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int bb = 0; bb < 4; ++bb) {
                         const int kb = 4 * j + bb;
-                        const int lp = kb / p.blocks_per_page;
-                        of[bb] = (kb - lp * p.blocks_per_page) * kBlk;
+                        const int lp = blk_lp;
+                        of[bb] = blk_in * kBlk;
+                        if (++blk_in == p.blocks_per_page) {
+                            blk_in = 0;
+                            ++blk_lp;
+                        }
                         if (kb < it.nblocks) {
                             pg[bb] = bt[lp];
                             if (pg[bb] < 0 || pg[bb] >= p.num_pages) atomicOr(p.err, kErrPage);
@@ -405,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; !stop && item_of(p, k, it); ++k) {
             const int qpos = it.q_start + it.r0 + row;
             float m_used = -CUDART_INF_F, l = 0.f;
+            // First token of block kb = 4j + qq and its in-page index, advanced quarter by
+            // quarter (no division: it would wait behind the partner warp's exps on the MUFU).
+            int blk_tok0 = 0, blk_in = 0;
             for (int j = 0; j < it.n && !stop; ++j) {
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(&bars[kSFull], (jt + j) & 1, p.err, abort))) {
@@ -431,11 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kb = 4 * j + qq;
                     int lim = 0;
                     if (kb < it.nblocks) {
-                        const int lp = kb / p.blocks_per_page;
-                        const int off = (kb - lp * p.blocks_per_page) * kBlk;
-                        const int tok0 = lp * p.block_size + off;
+                        const int off = blk_in * kBlk, tok0 = blk_tok0;
                         lim = min(kBlk, min(p.block_size - off, it.seq_len_k - tok0));
                         if (p.causal) lim = min(lim, qpos - tok0 + 1);
+                    }
+                    if (++blk_in == p.blocks_per_page) {  // the next block opens a page
+                        blk_tok0 += p.block_size - (p.blocks_per_page - 1) * kBlk;
+                        blk_in = 0;
+                    } else {
+                        blk_tok0 += kBlk;
                     }
                     lim -= 32 * hf;  // valid keys of this warp's half
                     if (!__all_sync(0xffffffffu, lim >= 32)) {
