@@ -390,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t obase = tmem + lane_off + kColO + 128 * hf;
         const uint32_t sbase = tmem + lane_off + kColS;
         float *xq = xchg + lq * 128;  // [phase][half][lane]
+        // Loop-invariant parameters, read once into registers.
+        const int block_size = p.block_size, blocks_per_page = p.blocks_per_page;
+        const bool causal = p.causal != 0, neg = p.neg != 0;
+        const float sc = p.sc;
         uint64_t *pair = &bars[kPair + lq];
         uint32_t pc = 0;  // exchanges done by this pair (both warps count alike)
         // Publishes v, meets the partner warp, returns the partner's value.  The meeting
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
                     }
-                    if (p.neg) {  // a negative scale reverses the order of the raw scores
+                    if (neg) {  // a negative scale reverses the order of the raw scores
 #pragma unroll
                         for (int i = 0; i < 32; ++i) x[i] = -x[i];
                     }
@@ -442,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int lim = 0;
                     if (kb < it.nblocks) {
                         const int off = blk_in * kBlk, tok0 = blk_tok0;
-                        lim = min(kBlk, min(p.block_size - off, it.seq_len_k - tok0));
-                        if (p.causal) lim = min(lim, qpos - tok0 + 1);
+                        lim = min(kBlk, min(block_size - off, it.seq_len_k - tok0));
+                        if (causal) lim = min(lim, qpos - tok0 + 1);
                     }
-                    if (++blk_in == p.blocks_per_page) {  // the next block opens a page
-                        blk_tok0 += p.block_size - (p.blocks_per_page - 1) * kBlk;
+                    if (++blk_in == blocks_per_page) {  // the next block opens a page
+                        blk_tok0 += block_size - (blocks_per_page - 1) * kBlk;
                         blk_in = 0;
                     } else {
                         blk_tok0 += kBlk;
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stop = true;
                         break;
                     }
-                    const float mx = mh * p.sc;
+                    const float mx = mh * sc;
                     const float m_new = fmaxf(m_used, mx);
                     const bool need = m_new > m_used + 8.f;  // also true for the first finite max
                     const float alpha =
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float e0, e1;
-                        fma2_bc(e0, e1, x[2 * i], x[2 * i + 1], p.sc, nmu);
+                        fma2_bc(e0, e1, x[2 * i], x[2 * i + 1], sc, nmu);
                         const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
                         add2(sa[i & 3], sb[i & 3], sa[i & 3], sb[i & 3], p0, p1);
                         hi[i] = pack_bf16x2(p0, p1);
