@@ -48,22 +48,24 @@ def test_tiny_decode_with_fused_new_token_write(cuda_lib):
     assert pa.device_errors() == 0
 
 
+@pytest.mark.parametrize("bs", [832, 784])
 @pytest.mark.parametrize("seq_len", [1665 + 16 * k for k in range(-7, 7)] + [1696])
-def test_fused_write_when_the_newest_tile_starts_a_split(cuda_lib, seq_len):
+def test_fused_write_when_the_newest_tile_starts_a_split(cuda_lib, seq_len, bs):
     # The kernel loads each split's first stage (two 16-token tiles) before it knows the
     # sequence length.  When that stage also holds the token being decoded (the split's
     # only stage), it has to be loaded again after the fused write; the slot starts as
     # NaN, so a stale copy shows in the output.  These 14 consecutive tile counts put the
     # last split at every length modulo 8 (the smallest split length), with the token on
-    # the first row of its tile (and, for 1696, on the last row).
+    # the first row of its tile (and, for 1696, on the last row).  At block size 784 a page
+    # holds 49 tiles, so some of these first stages straddle two pages instead.
     pa = cuda_lib
-    case = workloads.paged_case(73, [seq_len], 832, 8, new_tokens=1, device="cuda")
+    case = workloads.paged_case(73, [seq_len], bs, 8, new_tokens=1, device="cuda")
     k_ref, v_ref = bits(case.k_cache).copy(), bits(case.v_cache).copy()
     oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_ref, v_ref,
                              oracle.slot_mapping(case.positions.cpu().numpy(),
-                                                 case.block_table.cpu().numpy(), 832,
-                                                 case.seq_idx.cpu().numpy()), 832)
-    slots = pa.slot_mapping(case.positions, case.block_table, 832, seq_idx=case.seq_idx)
+                                                 case.block_table.cpu().numpy(), bs,
+                                                 case.seq_idx.cpu().numpy()), bs)
+    slots = pa.slot_mapping(case.positions, case.block_table, bs, seq_idx=case.seq_idx)
     out = _gpu_decode(pa, case, new_k=case.new_k, new_v=case.new_v, new_slots=slots)
     torch.cuda.synchronize()
     assert np.array_equal(bits(case.k_cache), k_ref) and np.array_equal(bits(case.v_cache), v_ref)
@@ -110,8 +112,10 @@ def test_batched_decode_fused_write(cuda_lib):
 EDGE_LENS = [1, 15, 16, 17, 63, 64, 65, 783, 784, 785, 831, 832, 833, 1700]
 
 
-@pytest.mark.parametrize("bs", [784, 832, 64, 16])
+@pytest.mark.parametrize("bs", [784, 832, 64, 16, 48, 100])
 def test_decode_edge_lengths_in_one_batch(cuda_lib, bs):
+    # 784 and 48: odd tiles per page (two-tile stages straddle pages); 100: a page ends in
+    # a 4-row tile; 16: one tile per page (every stage spans two pages).
     pa = cuda_lib
     npg = sum(-(-L // bs) for L in EDGE_LENS) + 3
     case = workloads.paged_case(77 + bs, EDGE_LENS, bs, npg, device="cuda")
