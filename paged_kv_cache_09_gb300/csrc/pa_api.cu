@@ -198,9 +198,11 @@ const char *pa_build_info(void) {
     static std::once_flag once;
     std::call_once(once, [] {
         snprintf(buf, sizeof buf,
-                 "paged_kv_cache_09_gb300: sm_103a; decode tile %d x %d stages, %d consumer "
-                 "warps; prefill %dx%d tcgen05 tiles; nvcc %d.%d",
-                 pa::kDecTile, pa::kDecStages, pa::kDecConsumers, pa::kPfQRows, pa::kPfKvTile,
+                 "paged_kv_cache_09_gb300: sm_103a; decode tiles of %d tokens, two per stage, "
+                 "%d warps x %d stages (splits <= %d tiles) or %d x %d; prefill %dx%d tcgen05 "
+                 "tiles; nvcc %d.%d",
+                 pa::kDecTile, pa::kDecShortConsumers, pa::kDecShortStages, pa::kDecShortTiles,
+                 pa::kDecLongConsumers, pa::kDecLongStages, pa::kPfQRows, pa::kPfKvTile,
                  __CUDACC_VER_MAJOR__, __CUDACC_VER_MINOR__);
     });
     return buf;

@@ -16,9 +16,10 @@
 //     a page holds an odd number of tiles, a stage whose two tiles lie in different
 //     pages is loaded with 16-row boxes.  Rows past a page end come back as zeros and
 //     are masked.
-//   * Seven consumer warps take tiles round-robin (tile i -> warp i % 7, half i % 2 of
-//     ring slot (i / 2) % 7; a slot is released by the warps of both its tiles).  Per
-//     tile: S^T = K Q^T
+//   * The consumer warps (four with a 4-stage ring for short splits, three with a 6-stage
+//     ring for long ones) take tiles round-robin (short splits: tile i -> warp i % C,
+//     half i % 2 of ring slot (i / 2) % S, a slot released by the warps of both its tiles;
+//     long splits: stage m -> warp m % C).  Per tile: S^T = K Q^T
 //     on the tensor cores (mma.m16n8k16, tokens as M, the group's heads as N, two
 //     accumulator chains), online softmax over tokens with warp shuffles, then
 //     O^T += V^T P^T with P split into a BF16 high part and a BF16 low part (two MMAs),
@@ -36,20 +37,20 @@ namespace pa {
 
 namespace {
 
-constexpr int kDecThreads = (kDecConsumers + 1) * 32;
 constexpr int kDecTileBytes = kDecTile * 128;               // one tile's rows of a 64-dim chunk
 constexpr int kDecChunkBytes = kDecBoxRows * 128;           // one 64-dim chunk of a stage: 4 KB
 constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one stage: 16 KB
 constexpr int kDecStageBytes = 2 * kDecHalf;                // 32 KB
-constexpr int kDecRingBytes = kDecStages * kDecStageBytes;  // 224 KB
 // Merge buffers, per warp and head: O row (padded by 4 floats, so that the 4 head
 // columns a warp stores at once fall in different banks), max and sum.
 constexpr int kDecMergeRow = kHeadDim + 4;
-constexpr int kDecMergeBytes = kDecConsumers * kDecMaxGroup * (kDecMergeRow + 2) * 4;
-static_assert(kDecMergeBytes <= kDecRingBytes, "merge buffers reuse the ring");
-constexpr int kDecSmemBytes = 1024 + kDecRingBytes + (2 * kDecStages + 1) * 8;
-// Splits of at most this many tiles hand out single tiles to the consumer warps.
-constexpr int kDecPerTileMaxTiles = 64;
+template <int kC, int kS>
+constexpr int dec_smem_bytes() {
+    static_assert(kC * kDecMaxGroup * (kDecMergeRow + 2) * 4 <= kS * kDecStageBytes,
+                  "merge buffers reuse the ring");
+    return 1024 + kS * kDecStageBytes + (2 * kS + 1) * 8;
+}
+
 constexpr int kCombineThreads = kHeadDim;
 
 struct DecodeKParams {
@@ -168,8 +169,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1)
+template <int kDecConsumers, int kDecStages>
+__global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     decode_split_kernel(const __grid_constant__ DecMaps maps, const DecodeKParams p) {
+    (void)DecShape<kDecConsumers, kDecStages>::consumers;  // checks the warp mapping
+    constexpr int kDecRingBytes = kDecStages * kDecStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -422,7 +426,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // and in phase order.  Long splits: stage m is consumed whole by warp m % 7, which
     // measured faster over long streams.  The choice is CTA-uniform; a slot is released
     // by two arrivals either way.
-    if (n <= kDecPerTileMaxTiles) {
+    if (n <= kDecShortTiles) {
         for (int i = warp; i < n; i += kDecConsumers) {
             const int m = i / kDecPair, h = i - m * kDecPair;
             const int s = m % kDecStages;
@@ -630,8 +634,16 @@ size_t decode_workspace_bytes(int num_seqs, int num_q_heads, const DecodePlan &p
 
 cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const DecodePlan &plan,
                           cudaStream_t stream) {
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_split_kernel),
-                                  kDecSmemBytes, 0);
+    // The kernel shape for this plan's split length (see DecShape).
+    const bool short_splits = plan.tiles_per_split <= kDecShortTiles;
+    void (*split_kernel)(DecMaps, DecodeKParams) =
+        short_splits ? decode_split_kernel<kDecShortConsumers, kDecShortStages>
+                     : decode_split_kernel<kDecLongConsumers, kDecLongStages>;
+    const int smem = short_splits ? dec_smem_bytes<kDecShortConsumers, kDecShortStages>()
+                                  : dec_smem_bytes<kDecLongConsumers, kDecLongStages>();
+    const int threads = ((short_splits ? kDecShortConsumers : kDecLongConsumers) + 1) * 32;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(split_kernel), smem,
+                                  short_splits ? 0 : 3);
     if (e != cudaSuccess) return e;
     DecodeKParams p;
     p.q = a.q;
@@ -667,7 +679,7 @@ cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const D
     maps.v = tmaps[1];
     maps.k16 = tmaps[2];
     maps.v16 = tmaps[3];
-    e = launch_pdl(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream, maps, p);
+    e = launch_pdl(split_kernel, grid, dim3(threads), smem, stream, maps, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, stream)) != cudaSuccess) return e;
     return launch_pdl(decode_combine_kernel, dim3(a.num_q_heads, a.num_seqs),

@@ -67,14 +67,23 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
 constexpr int kDecTile = 16;       // tokens per MMA tile (page-local)
 constexpr int kDecPair = 2;        // tiles per ring stage
 constexpr int kDecBoxRows = kDecTile * kDecPair;  // rows of the stage-wide TMA boxes
-constexpr int kDecStages = 7;      // shared-memory ring depth (32 KB stages)
-constexpr int kDecConsumers = 7;   // consumer warps per CTA (plus one producer warp)
-// Stage m holds tiles 2m and 2m + 1 of the split and uses ring slot m % kDecStages; tile
-// i is consumed by warp i % kDecConsumers.  An mbarrier wait only tells the last two
-// phases apart, so a warp must visit each of its slots once per ring round, in phase
-// order: with a ring round of kDecStages * kDecPair tiles a multiple of the consumer
-// count, every (tile of the round) -> (warp, slot, half) assignment is fixed.
-static_assert((kDecStages * kDecPair) % kDecConsumers == 0, "tile -> warp mapping must be fixed");
+// Two shapes of the split kernel (consumer warps, 32 KB ring stages): splits of up to
+// kDecShortTiles tiles (the tail of the stream and the CTA merge are a large share of their
+// time) run with four consumer warps and a 4-stage ring; longer splits with three consumer
+// warps and a 6-stage ring (measured fastest for each; fewer warps means less to merge).
+constexpr int kDecShortConsumers = 4, kDecShortStages = 4;
+constexpr int kDecLongConsumers = 3, kDecLongStages = 6;
+constexpr int kDecShortTiles = 64;
+// Stage m holds tiles 2m and 2m + 1 of the split and uses ring slot m % stages.  In a short
+// split tile i is consumed by warp i % consumers; in a long one stage m by warp
+// m % consumers.  An mbarrier wait only tells the last two phases apart, so a warp must
+// visit each of its slots once per ring round, in phase order: the ring round (stages *
+// kDecPair tiles, or stages stages) is a multiple of the consumer count.
+template <int kC, int kS>
+struct DecShape {
+    static_assert((kS * kDecPair) % kC == 0 && kS % kC == 0, "tile -> warp mapping must be fixed");
+    static constexpr int consumers = kC, stages = kS;
+};
 constexpr int kDecMaxSplits = 1024;  // upper bound on CTAs per (sequence, KV head)
 constexpr int kDecMaxGroup = 8;    // query heads per KV head handled by one MMA column tile
 
