@@ -341,9 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (stop) break;
                     if (j == it.n - 1) umma_commit(&bars[kQEmpty]);
                     umma_commit(&bars[kSFull]);
-                    // O += P V, one 64-key quarter (one V unit) at a time.
+                    // O += P V, one 64-key quarter (one V unit) at a time.  The V unit and
+                    // the O buffer are usually ready long before P: their waits (each
+                    // costs this thread a few hundred cycles even when already complete)
+                    // and the descriptors come first, so that only the P hand-off sits
+                    // between one quarter's MMAs and the next.
                     for (int qq = 0; qq < 4; ++qq, ++u) {
-                        if (!wait_or_abort(&bars[kPFull + qq], (jt + j) & 1, p.err, abort)) {
+                        const int s = u % kRing;
+                        if (!wait_or_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
@@ -352,8 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             stop = true;
                             break;
                         }
-                        const int s = u % kRing;
-                        if (!wait_or_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
+                        uint64_t vd[kBlk / 16];
+#pragma unroll
+                        for (int ks = 0; ks < kBlk / 16; ++ks)
+                            vd[ks] = umma_sdesc_sw128(ring_addr + s * kUnit + ks * 2048, kBlkBytes);
+                        if (!wait_or_abort(&bars[kPFull + qq], (jt + j) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
@@ -361,10 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t phi = sbuf + 64 * qq;
 #pragma unroll
                         for (int ks = 0; ks < kBlk / 16; ++ks) {
-                            const uint64_t vd =
-                                umma_sdesc_sw128(ring_addr + s * kUnit + ks * 2048, kBlkBytes);
-                            umma_ts(obuf, phi + 8 * ks, vd, kIdPV, (j | qq | ks) != 0);
-                            umma_ts(obuf, phi + 32 + 8 * ks, vd, kIdPV, 1);
+                            umma_ts(obuf, phi + 8 * ks, vd[ks], kIdPV, (j | qq | ks) != 0);
+                            umma_ts(obuf, phi + 32 + 8 * ks, vd[ks], kIdPV, 1);
                         }
                         umma_commit(&bars[kRingEmpty + s]);
                         umma_commit(&bars[kPvDone + qq]);
