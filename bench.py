@@ -367,7 +367,8 @@ def e2e_leg(pa, case, steps, warmup, flush):
     the step's inputs (q, the new token's K/V, its position, sequence index, block table
     and seq_lens, packed in one pinned staging buffer), slot mapping + fused write +
     decode, and the D2H copy of the output -- the whole step replayed from a CUDA graph,
-    as a serving loop would capture its decode step."""
+    as a serving loop would capture its decode step.  Both copies are pa_copy kernels
+    (a copy-engine node costs several microseconds more per copy on this system)."""
     S, hq, d = case.q.shape
     msl = int(case.seq_lens.max())
     names = ("q", "new_k", "new_v", "positions", "seq_idx", "block_table", "seq_lens")
@@ -396,13 +397,13 @@ def e2e_leg(pa, case, steps, warmup, flush):
     d2h = out_h.numel() * out_h.element_size()
 
     def step():
-        stage_d.copy_(stage_h, non_blocking=True)
+        pa.copy(stage_d, stage_h)
         pa.slot_mapping(dev["positions"], dev["block_table"], case.block_size,
                         seq_idx=dev["seq_idx"], out=slots)
         pa.decode(dev["q"], case.k_cache, case.v_cache, dev["block_table"], dev["seq_lens"],
                   case.scale, msl, out=out_d, workspace=ws, new_k=dev["new_k"],
                   new_v=dev["new_v"], new_slots=slots)
-        out_h.copy_(out_d, non_blocking=True)
+        pa.copy(out_h, out_d)
     g = graph_of(step)
     ms = time_steps(g.replay, steps, warmup, flush)
     torch.cuda.synchronize()
@@ -614,7 +615,9 @@ def main():
                    "parallelism": f"replica per GPU x{ws}"},
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copies": "pa_copy kernels between pinned host buffers and the device, "
+                          "inside the step's CUDA graph"},
         # per step: slot mapping, split decode (with the fused KV write), LSE combine
         "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peaks["hbm_gbs"],

@@ -252,6 +252,19 @@ int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads, int blo
                     int num_ctas, int32_t *cta_of_item, int *num_items, int *max_cost);
 
 /*
+ * pa_copy -- copies `bytes` bytes from src to dst with a kernel on `stream` (ordered like
+ * the library's other launches, and capturable into a CUDA graph).  Each address may be
+ * device memory or page-locked host memory (cudaHostAlloc / cudaMallocHost / registered
+ * with cudaHostRegister), which the kernel reaches through its device mapping; for a
+ * step's few kilobytes of inputs and results this avoids a copy-engine node, whose fixed
+ * cost on this system is several microseconds.  Both addresses must be 16-byte aligned
+ * and bytes a multiple of 16; the ranges must not overlap.  Returns PA_ERR_INVALID_ARG
+ * for a NULL or misaligned pointer, a bad size, or an address the device cannot reach
+ * (pageable host memory); bytes == 0 is a no-op.
+ */
+int pa_copy(void *dst, const void *src, size_t bytes, void *stream);
+
+/*
  * pa_get_device_errors -- waits for `stream`, then returns in *bits the device error
  * word of the current device (PA_DEVERR_* bits set by any call since the last clear)
  * and, if clear != 0, resets it to zero.

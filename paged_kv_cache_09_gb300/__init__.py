@@ -76,6 +76,7 @@ def load():
             "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, P, P, P], i32),
             "pa_prefill_varlen": ([P, P, P, i64, i64, P, i64, P, P, i32, i32, i32, i32, i32,
                                    i32, f32, P, P], i32),
+            "pa_copy": ([P, P, sz, P], i32),
             "pa_get_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32, P], i32),
             "pa_set_kernel_events": ([P, P], i32),
             "pa_status_string": ([i32], ctypes.c_char_p),
@@ -200,6 +201,23 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping_):
     _raise(lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), ps,
                                     k_cache.shape[0], _ptr(slot_mapping_), T, hkv, d,
                                     k_cache.shape[1], _stream()), "pa_reshape_and_cache")
+
+
+def copy(dst, src):
+    """Copy src into dst (same byte size, both contiguous) with a kernel on the current
+    stream (see pa_copy).  Each tensor may live on the GPU or in pinned host memory."""
+    lib = load()
+    for t, nm in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{nm} must be a CUDA tensor or pinned host memory")
+    nb = dst.numel() * dst.element_size()
+    if nb != src.numel() * src.element_size():
+        raise ValueError("dst and src differ in size")
+    _raise(lib.pa_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nb,
+                       _stream()), "pa_copy")
+    return dst
 
 
 def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

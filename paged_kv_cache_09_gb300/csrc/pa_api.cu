@@ -193,6 +193,41 @@ const char *pa_status_string(int status) {
     }
 }
 
+// The address through which the device reaches p: p itself for device and managed
+// memory, the device mapping of page-locked host memory; false for memory the device
+// cannot reach (pageable host memory) or an unknown address.
+static bool device_address(const void *p, const void **dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of the query
+        return false;
+    }
+    switch (a.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged: *dev = p; return true;
+        case cudaMemoryTypeHost:
+            if (!a.devicePointer) return false;
+            *dev = a.devicePointer;
+            return true;
+        default: return false;
+    }
+}
+
+int pa_copy(void *dst, const void *src, size_t bytes, void *stream) {
+    if (bytes == 0) return PA_OK;
+    if (!dst || !src || (bytes & 15u) || (reinterpret_cast<uintptr_t>(dst) & 15u) ||
+        (reinterpret_cast<uintptr_t>(src) & 15u) || bytes > ((size_t)1 << 40))
+        return PA_ERR_INVALID_ARG;
+    const void *d = nullptr, *s = nullptr;
+    if (!device_address(dst, &d) || !device_address(src, &s)) return PA_ERR_INVALID_ARG;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d), s0 = reinterpret_cast<uintptr_t>(s);
+    if (d0 < s0 + bytes && s0 < d0 + bytes) return PA_ERR_INVALID_ARG;  // overlapping ranges
+    return pa::launch_copy(const_cast<void *>(d), s, bytes, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 const char *pa_build_info(void) {
     static char buf[256];
     static std::once_flag once;

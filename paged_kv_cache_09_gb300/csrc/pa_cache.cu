@@ -11,6 +11,25 @@
 
 namespace pa {
 
+// Byte copy between two device-accessible ranges (device memory or page-locked host
+// memory through its device mapping), 16 bytes per thread and step.
+__global__ void __launch_bounds__(256) copy_kernel(const uint4 *__restrict__ src,
+                                                   uint4 *__restrict__ dst, int64_t n16) {
+    pdl_wait();  // the source may be written by earlier work on the stream
+    pdl_trigger();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream) {
+    const int64_t n16 = (int64_t)(bytes / 16);
+    const int64_t blocks = (n16 + 255) / 256;
+    return launch_pdl(copy_kernel, dim3((unsigned)(blocks < 1024 ? blocks : 1024)), dim3(256),
+                      0, stream, static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                      n16);
+}
+
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
     static std::atomic<unsigned long long> done[4];  // bit d: device d already set
     int dev = 0;

@@ -33,6 +33,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Kernel copy of bytes (a multiple of 16) between 16-byte aligned device-accessible
+// addresses.
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+
 // ----------------------------------------------------------------- cache write
 cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
                                 const int32_t *block_table, int num_seqs, int64_t bt_stride,

@@ -200,3 +200,18 @@ def test_prefill_varlen_rejects_bad_arguments(lib, kw, want):
 def test_prefill_varlen_without_rows_is_a_no_op(lib):
     assert _varlen(lib, cu=(0, 0, 0), k_lens=(5, 7)) == 0
     assert _varlen(lib, cu=(0,), k_lens=(), num_seqs=0) == 0
+
+
+@pytest.mark.parametrize("dst,src,nbytes", [
+    (None, FAKE, 64),            # NULL destination
+    (FAKE, None, 64),            # NULL source
+    (FAKE + 8, FAKE + 4096, 64),  # misaligned destination
+    (FAKE, FAKE + 4096 + 4, 64),  # misaligned source
+    (FAKE, FAKE + 4096, 40),     # not a multiple of 16 bytes
+])
+def test_copy_rejects_bad_arguments(lib, dst, src, nbytes):
+    assert lib.pa_copy(dst, src, nbytes, None) == PA_ERR_INVALID_ARG
+
+
+def test_copy_of_nothing_is_a_no_op(lib):
+    assert lib.pa_copy(None, None, 0, None) == PA_OK
