@@ -420,12 +420,12 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     };
 
     // Short splits (the tail of the stream is a large share of their time): tile i is
-    // consumed by warp i % 7 from half i % 2 of stage i / 2 (ring slot (i / 2) % 7), so the
-    // two tiles of a stage are processed in parallel.  Within a ring round of 14 tiles
-    // every (warp, slot, half) is fixed, so each warp waits on its two slots alternately
-    // and in phase order.  Long splits: stage m is consumed whole by warp m % 7, which
-    // measured faster over long streams.  The choice is CTA-uniform; a slot is released
-    // by two arrivals either way.
+    // consumed by warp i % C from half i % 2 of stage i / 2 (ring slot (i / 2) % S), so the
+    // two tiles of a stage are processed in parallel.  Within a ring round of 2S tiles
+    // every (warp, slot, half) is fixed, so each warp waits on its slots in turn and in
+    // phase order.  Long splits: stage m is consumed whole by warp m % C, which measured
+    // faster over long streams.  The choice is CTA-uniform; a slot is released by two
+    // arrivals either way.
     if (n <= kDecShortTiles) {
         for (int i = warp; i < n; i += kDecConsumers) {
             const int m = i / kDecPair, h = i - m * kDecPair;
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
         }
     }
     named_bar_sync(1, kDecConsumers * 32);
-    // Thread t merges the quads (4 consecutive dims of one head) t, t + 224, ...  Every
+    // Thread t merges the quads (4 consecutive dims of one head) t, t + 32C, ...  Every
     // thread derives its head's CTA max and the warps' weights exp2(m_w - M) itself, so
     // no further barrier is needed and all loads of a quad are independent.
     constexpr int kQuadsPerHead = kHeadDim / 4;
