@@ -225,8 +225,12 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     const int ntiles = seq_tiles(seq_len, p.block_size, tpp);
     const int t1 = min(ntiles, t0 + p.tiles_per_split);
     if (t0 >= t1) {
-        // This split has no tiles of this sequence (CTA-uniform): the first stage's load
+        // This split has no tiles of this sequence (CTA-uniform).  It marks its partials
+        // empty (the combine then needs no sequence length), and the first stage's load
         // lands before the CTA exits.
+        if (threadIdx.x < p.group)
+            p.part_ml[((int64_t)seq * p.num_q_heads + g * p.group + threadIdx.x) * p.num_splits +
+                      split] = make_float2(-CUDART_INF_F, 0.f);
         if (producer && spec) mbar_wait(&full[0], 0, p.err);
         return;
     }
@@ -532,9 +536,9 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     const int warp = tid >> 5, lane = tid & 31;
     pdl_wait();
     pdl_trigger();
-    const int seq_len = checked_seq_len(p, seq, false);
-    const int ntiles = seq_tiles(seq_len, p.block_size, p.tiles_per_page);
-    const int nsplit = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    // Every split wrote its (max, sum); an empty one (max -inf) gets weight 0 and its
+    // partial sums, never written, are skipped.
+    const int nsplit = p.num_splits;
     const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.num_splits;
     const float4 *po = reinterpret_cast<const float4 *>(p.part_o + base * kHeadDim) + lane * 2;
     float M = -CUDART_INF_F, L = 0.f;
@@ -572,6 +576,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
             const float w = __shfl_sync(0xffffffffu, e, k);
+            if (w == 0.f) continue;  // warp-uniform: an empty split's sums are not read
             acc[0] += w * va[k].x; acc[1] += w * va[k].y; acc[2] += w * va[k].z; acc[3] += w * va[k].w;
             acc[4] += w * vb[k].x; acc[5] += w * vb[k].y; acc[6] += w * vb[k].z; acc[7] += w * vb[k].w;
         }
