@@ -162,6 +162,31 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
               void *stream);
 
 /*
+ * pa_decode_append -- one decode step in which each sequence's newest token is appended
+ * to the cache and attended to, with its slot derived on the device [input-prep §3.2,
+ * §5: the slot-mapping formula; page832 §5, §7].  For each sequence s, the token being
+ * decoded sits at position p = seq_lens[s] - 1 and its slot is
+ *     slot_mapping[s] = block_table[s][p / block_size] * block_size + p % block_size,
+ * the value pa_slot_mapping gives for (p, s).  The kernel writes new_k[s] / new_v[s]
+ * ([num_seqs, Hkv, D], contiguous) there, bit for bit as pa_reshape_and_cache would,
+ * then decodes as pa_decode does; no separate slot-mapping launch is needed.
+ *   slot_mapping  int64 [num_seqs], device, 8-byte aligned, OUTPUT, may be NULL: the
+ *                 slots written, for callers that reuse them (for example for the other
+ *                 layers' pa_reshape_and_cache of the same step).
+ * Every sequence has a newest token (no padding).  A block-table entry for that token
+ * outside [0, num_pages) writes nothing and sets PA_DEVERR_PAGE; slot_mapping[s] then
+ * holds -1 for a negative entry (as pa_slot_mapping gives) and the formula's value for
+ * one past the pool.  All other arguments, checks and errors are those of
+ * pa_decode; new_k and new_v must be non-NULL and 16-byte aligned.
+ */
+int pa_decode_append(const pa_bf16 *q, pa_bf16 *k_cache, pa_bf16 *v_cache, int64_t page_stride,
+                     int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
+                     const int32_t *seq_lens, int num_seqs, int max_seq_len, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, float scale, pa_bf16 *out,
+                     void *workspace, size_t workspace_bytes, const pa_bf16 *new_k,
+                     const pa_bf16 *new_v, int64_t *slot_mapping, void *stream);
+
+/*
  * pa_decode_noalloc -- the same decode as pa_decode (without the fused write), for
  * callers that cannot allocate device memory on the decode path: for example a serving
  * runtime that gives almost all device memory to its KV-cache pool at start-up and
@@ -272,10 +297,12 @@ int pa_copy(void *dst, const void *src, size_t bytes, void *stream);
 int pa_get_device_errors(unsigned int *bits, int clear, void *stream);
 
 /*
- * pa_set_kernel_events -- measurement hook.  The next pa_decode or pa_prefill_chunk
- * call made by this host thread records `start` on its stream immediately before it
- * launches its main kernel (the split-context decode kernel, or the prefill kernel)
- * and `stop` immediately after that launch, then forgets both.  The arguments are
+ * pa_set_kernel_events -- measurement hook.  The next pa_decode, pa_decode_append,
+ * pa_prefill_chunk or pa_prefill_varlen call made by this host thread records `start` on
+ * its stream immediately before it launches its main kernel (the split-context decode
+ * kernel, or the prefill kernel) and `stop` immediately after that launch, then forgets
+ * both.  Inside a stream capture the records carry cudaEventRecordExternal, so they
+ * become event record nodes that every replay of the graph records.  The arguments are
  * cudaEvent_t handles owned by the caller; passing NULL, NULL cancels a pending hook.
  * Both or neither must be NULL.
  */

@@ -29,7 +29,7 @@ from . import _build
 
 __all__ = ["load", "build", "slot_mapping", "decode_input_prep", "reshape_and_cache",
            "decode_workspace_size",
-           "decode", "prefill_chunk", "prefill_varlen", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
+           "decode", "decode_append", "prefill_chunk", "prefill_varlen", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
            "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION", "DEVERR_LAYOUT",
            "LIB_PATH"]
 
@@ -71,6 +71,8 @@ def load():
             "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
             "pa_decode": ([P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32, P, P,
                            sz, P, P, P, P], i32),
+            "pa_decode_append": ([P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32,
+                                  P, P, sz, P, P, P, P], i32),
             "pa_prefill_chunk": ([P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                   P, P], i32),
             "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, P, P, P], i32),
@@ -249,6 +251,43 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, scale, max_seq_len, out=N
                          int(max_seq_len), hq, hkv, d, bs, float(scale), _ptr(out),
                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                          _ptr(new_k), _ptr(new_v), _ptr(new_slots), _stream()), "pa_decode")
+    return out
+
+
+def decode_append(q, k_cache, v_cache, block_table, seq_lens, scale, max_seq_len, new_k, new_v,
+                  out=None, workspace=None, slot_mapping=None):
+    """Decode step that appends each sequence's newest token (position seq_lens[s] - 1)
+    from new_k / new_v at the slot the kernel derives from the block table, then attends
+    (see pa_decode_append).  slot_mapping, if given (int64 [S]), receives those slots.
+    Returns out [S, Hq, D] BF16."""
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(new_k, "new_k", torch.bfloat16, 3)
+    _check(new_v, "new_v", torch.bfloat16, 3)
+    if slot_mapping is not None:
+        _check(slot_mapping, "slot_mapping", torch.int64, 1)
+        if not slot_mapping.is_contiguous() or slot_mapping.numel() < q.shape[0]:
+            raise ValueError("slot_mapping must be a contiguous int64 tensor of num_seqs entries")
+    ps = _check_cache(k_cache, v_cache)
+    q = q.contiguous()
+    new_k, new_v = new_k.contiguous(), new_v.contiguous()
+    S, hq, d = q.shape
+    _, bs, hkv, _ = k_cache.shape
+    if new_k.shape != (S, hkv, d) or new_v.shape != (S, hkv, d):
+        raise ValueError("new_k / new_v must be [num_seqs, num_kv_heads, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_size(S, hq, hkv, d, bs, max_seq_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _raise(lib.pa_decode_append(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
+                                _ptr(block_table), block_table.stride(0), _ptr(seq_lens), S,
+                                int(max_seq_len), hq, hkv, d, bs, float(scale), _ptr(out),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _ptr(new_k), _ptr(new_v), _ptr(slot_mapping), _stream()),
+           "pa_decode_append")
     return out
 
 

@@ -330,12 +330,17 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     return pa::decode_workspace_bytes(num_seqs, num_q_heads, plan);
 }
 
-int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
-              int64_t page_stride, int64_t num_pages, const int32_t *block_table,
-              int64_t bt_stride, const int32_t *seq_lens, int num_seqs, int max_seq_len,
-              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
-              pa_bf16 *out, void *workspace, size_t workspace_bytes, const pa_bf16 *new_k,
-              const pa_bf16 *new_v, const int64_t *new_slots, void *stream) {
+// pa_decode and pa_decode_append.  fused: the newest tokens are written (new_k and new_v
+// set); their slots are new_slots when given, else derived in the kernel and stored to
+// slot_out (when set).
+static int decode_impl(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                       int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                       int64_t bt_stride, const int32_t *seq_lens, int num_seqs,
+                       int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, float scale, pa_bf16 *out, void *workspace,
+                       size_t workspace_bytes, bool fused, const pa_bf16 *new_k,
+                       const pa_bf16 *new_v, const int64_t *new_slots, int64_t *slot_out,
+                       void *stream) {
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
         return PA_ERR_INVALID_ARG;
     if (num_seqs < 1 || num_seqs > 65535 || max_seq_len < 1) return PA_ERR_INVALID_ARG;
@@ -348,9 +353,8 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PA_ERR_INVALID_ARG;
-    const int nfused = (new_k != nullptr) + (new_v != nullptr) + (new_slots != nullptr);
-    if (nfused != 0 && nfused != 3) return PA_ERR_INVALID_ARG;
-    if (nfused == 3 && (!aligned16(new_k) || !aligned16(new_v))) return PA_ERR_INVALID_ARG;
+    if (fused && (!new_k || !new_v || !aligned16(new_k) || !aligned16(new_v)))
+        return PA_ERR_INVALID_ARG;
 
     DeviceInfo dev;
     if (int rc = device_info(&dev)) return rc;
@@ -381,11 +385,12 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     pa::DecodeArgs a;
-    a.k_cache_w = nfused == 3 ? const_cast<pa_bf16 *>(k_cache) : nullptr;
-    a.v_cache_w = nfused == 3 ? const_cast<pa_bf16 *>(v_cache) : nullptr;
-    a.new_k = nfused == 3 ? new_k : nullptr;
-    a.new_v = nfused == 3 ? new_v : nullptr;
-    a.new_slots = nfused == 3 ? new_slots : nullptr;
+    a.k_cache_w = fused ? const_cast<pa_bf16 *>(k_cache) : nullptr;
+    a.v_cache_w = fused ? const_cast<pa_bf16 *>(v_cache) : nullptr;
+    a.new_k = fused ? new_k : nullptr;
+    a.new_v = fused ? new_v : nullptr;
+    a.new_slots = fused ? new_slots : nullptr;
+    a.slot_out = fused && !new_slots ? slot_out : nullptr;
     a.page_stride = page_stride;
     a.q = q;
     a.block_table = block_table;
@@ -407,6 +412,33 @@ int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
         fprintf(stderr, "[pa] decode: seqs=%d max_seq_len=%d bs=%d splits=%d tiles/split=%d\n",
                 num_seqs, max_seq_len, block_size, plan.num_splits, plan.tiles_per_split);
     return pa::launch_decode(maps, a, plan, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_decode(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+              int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+              int64_t bt_stride, const int32_t *seq_lens, int num_seqs, int max_seq_len,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+              pa_bf16 *out, void *workspace, size_t workspace_bytes, const pa_bf16 *new_k,
+              const pa_bf16 *new_v, const int64_t *new_slots, void *stream) {
+    const int nfused = (new_k != nullptr) + (new_v != nullptr) + (new_slots != nullptr);
+    if (nfused != 0 && nfused != 3) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, page_stride, num_pages, block_table, bt_stride,
+                       seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                       block_size, scale, out, workspace, workspace_bytes, nfused == 3, new_k,
+                       new_v, new_slots, nullptr, stream);
+}
+
+int pa_decode_append(const pa_bf16 *q, pa_bf16 *k_cache, pa_bf16 *v_cache, int64_t page_stride,
+                     int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
+                     const int32_t *seq_lens, int num_seqs, int max_seq_len, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, float scale, pa_bf16 *out,
+                     void *workspace, size_t workspace_bytes, const pa_bf16 *new_k,
+                     const pa_bf16 *new_v, int64_t *slot_mapping, void *stream) {
+    if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, page_stride, num_pages, block_table, bt_stride,
+                       seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                       block_size, scale, out, workspace, workspace_bytes, true, new_k, new_v,
+                       nullptr, slot_mapping, stream);
 }
 
 // One prefill launch over 1 .. kPfMaxSeqs chunks whose rows lie in q / out of total_q rows.

@@ -71,10 +71,13 @@ struct DecodeKParams {
     float2 *part_ml;    // [S, Hq, splits] (running max in base-2 units, sum of weights)
     uint16_t *out;
     unsigned *err;
-    // Fused write of the token being decoded (new_slots == nullptr: none).
+    // Fused write of the token being decoded (new_k == nullptr: none).  Its slot comes
+    // from new_slots, or, with new_slots == nullptr, from the block table (and is then
+    // stored to slot_out when that is set).
     uint16_t *k_cache_w, *v_cache_w;
     const uint16_t *new_k, *new_v;   // [S, Hkv, D]
     const int64_t *new_slots;        // [S]
+    int64_t *slot_out;               // [S]
     int64_t page_stride;
     int num_kv_heads;
 };
@@ -83,18 +86,23 @@ struct DecodeKParams {
 // sequence `seq`'s last tile as soon as the CTA starts: each lane copies 16 bytes of
 // the K row and 16 of the V row of KV head g, every lane fences its stores against the
 // async proxy, and after the warp has converged lane 0 arrives on `written`.  The
-// producer waits on `written` before it issues the TMA load of that last tile.  Only a
-// slot that matches the block table's slot for position seq_len - 1 is written.
+// producer waits on `written` before it issues the TMA load of that last tile.  A given
+// slot is written only if it matches the block table's slot for position seq_len - 1;
+// without given slots that slot is the one taken (the slot-mapping formula), and the
+// CTA of KV head 0 reports it.
 __device__ __forceinline__ void write_newest_token(const DecodeKParams &p, const int32_t *bt,
                                                    int seq, int g, int seq_len, int lane,
                                                    uint64_t *written) {
-    const int64_t slot = p.new_slots[seq];
     const int pos = seq_len - 1;
     const int lp = pos / p.block_size;
     const int off = pos - lp * p.block_size;
     const int page = bt[lp];
-    if (slot >= 0) {  // a negative slot is padding
-        if (page >= 0 && page < p.num_pages && slot == (int64_t)page * p.block_size + off) {
+    const int64_t mapped = page < 0 ? -1 : (int64_t)page * p.block_size + off;
+    const bool given = p.new_slots != nullptr;
+    const int64_t slot = given ? p.new_slots[seq] : mapped;
+    if (!given && g == 0 && lane == 0 && p.slot_out) p.slot_out[seq] = mapped;
+    if (slot >= 0 || !given) {  // a negative given slot is padding
+        if (page >= 0 && page < p.num_pages && slot == mapped) {
             const int64_t src = ((int64_t)seq * p.num_kv_heads + g) * kHeadDim;
             const int64_t dst =
                 page * p.page_stride + ((int64_t)off * p.num_kv_heads + g) * kHeadDim;
@@ -103,7 +111,7 @@ __device__ __forceinline__ void write_newest_token(const DecodeKParams &p, const
             reinterpret_cast<uint4 *>(p.k_cache_w + dst)[lane] = k;
             reinterpret_cast<uint4 *>(p.v_cache_w + dst)[lane] = v;
         } else if (lane == 0) {
-            atomicOr(p.err, kErrSlot);
+            atomicOr(p.err, given ? kErrSlot : kErrPage);
         }
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     const int n = t1 - t0;                            // tiles of this split
     const int nst = (n + kDecPair - 1) / kDecPair;    // stages of this split
     // This CTA holds the tile of the token being decoded and has to write that token.
-    const bool writes_newest = p.new_slots != nullptr && t1 == ntiles;
+    const bool writes_newest = p.new_k != nullptr && t1 == ntiles;
     // ... and if that tile is in the stage loaded ahead, the stage is loaded twice.
     const bool refetch = writes_newest && spec && nst == 1;
 
@@ -675,10 +683,11 @@ cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const D
     p.new_k = a.new_k;
     p.new_v = a.new_v;
     p.new_slots = a.new_slots;
+    p.slot_out = a.slot_out;
     p.page_stride = a.page_stride;
     p.num_kv_heads = a.num_kv_heads;
     const dim3 grid(plan.num_splits, a.num_kv_heads, a.num_seqs);
-    if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
+    if (a.ev_start && (e = record_event(a.ev_start, stream)) != cudaSuccess) return e;
     DecMaps maps;
     maps.k = tmaps[0];
     maps.v = tmaps[1];
@@ -686,7 +695,7 @@ cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const D
     maps.v16 = tmaps[3];
     e = launch_pdl(split_kernel, grid, dim3(threads), smem, stream, maps, p);
     if (e != cudaSuccess) return e;
-    if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, stream)) != cudaSuccess) return e;
+    if (a.ev_stop && (e = record_event(a.ev_stop, stream)) != cudaSuccess) return e;
     return launch_pdl(decode_combine_kernel, dim3(a.num_q_heads, a.num_seqs),
                       dim3(kCombineThreads), 0, stream, p);
 }

@@ -33,6 +33,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Records a measurement event on the stream.  Under stream capture it becomes an event
+// record node of the graph (cudaEventRecordExternal), so that each replay records it; a
+// plain record in a capturing stream would only order the capture.  Outside a capture it
+// is a plain record (the runtime refuses the external flag there).
+inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return e;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+               : cudaEventRecord(ev, stream);
+}
+
 // Kernel copy of bytes (a multiple of 16) between 16-byte aligned device-accessible
 // addresses.
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
@@ -116,10 +129,13 @@ struct DecodeArgs {
     void *workspace;
     unsigned *err;
     cudaEvent_t ev_start, ev_stop;  // optional: recorded around the split kernel
-    // Optional fused write of each sequence's newest token (all NULL when unused).
+    // Optional fused write of each sequence's newest token (all NULL when unused).  With
+    // new_k set and new_slots NULL the slots come from the block table, and are stored
+    // to slot_out when that is set.
     uint16_t *k_cache_w, *v_cache_w;
     const uint16_t *new_k, *new_v;
     const int64_t *new_slots;
+    int64_t *slot_out;
     int64_t page_stride;            // elements between consecutive pages
 };
 

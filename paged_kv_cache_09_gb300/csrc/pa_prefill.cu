@@ -641,11 +641,11 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     } else {
         p.sched.num_ctas = 0;
     }
-    if (a.ev_start && (e = cudaEventRecord(a.ev_start, stream)) != cudaSuccess) return e;
+    if (a.ev_start && (e = record_event(a.ev_start, stream)) != cudaSuccess) return e;
     e = launch_pdl(prefill_tc_kernel<kSeqs>, dim3(grid), dim3(kThreads), kSmemBytes, stream,
                    maps, p);
     if (e != cudaSuccess) return e;
-    if (a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
+    if (a.ev_stop) e = record_event(a.ev_stop, stream);
     return e;
 }
 

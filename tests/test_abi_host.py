@@ -32,7 +32,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for n in ("pa_slot_mapping", "pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk",
+    for n in ("pa_slot_mapping", "pa_reshape_and_cache", "pa_decode", "pa_decode_append",
+              "pa_prefill_chunk",
               "pa_decode_workspace_size", "pa_get_device_errors", "pa_status_string",
               "pa_build_info"):
         assert n in names
@@ -102,6 +103,32 @@ def _prefill(lib, **kw):
 ])
 def test_decode_rejects_bad_arguments(lib, kw, want):
     assert _decode(lib, **kw) == want
+
+
+def _append(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, page_stride=832 * 4 * 256, num_pages=64, bt=FAKE,
+             bt_stride=16, seq_lens=FAKE, num_seqs=1, max_seq_len=8192, hq=24, hkv=4, d=256,
+             bs=832, scale=0.0625, out=FAKE, ws=FAKE, ws_bytes=1 << 20, nk=FAKE, nv=FAKE,
+             slots=FAKE)
+    a.update(kw)
+    return lib.pa_decode_append(a["q"], a["k"], a["v"], a["page_stride"], a["num_pages"],
+                                a["bt"], a["bt_stride"], a["seq_lens"], a["num_seqs"],
+                                a["max_seq_len"], a["hq"], a["hkv"], a["d"], a["bs"], a["scale"],
+                                a["out"], a["ws"], a["ws_bytes"], a["nk"], a["nv"], a["slots"],
+                                None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(nk=None), PA_ERR_INVALID_ARG),              # the appended token is required
+    (dict(nv=None), PA_ERR_INVALID_ARG),
+    (dict(nk=FAKE + 8), PA_ERR_INVALID_ARG),          # misaligned new K
+    (dict(slots=FAKE + 4), PA_ERR_INVALID_ARG),       # int64 output must be 8-byte aligned
+    (dict(q=None), PA_ERR_INVALID_ARG),               # and every pa_decode check
+    (dict(bt_stride=9), PA_ERR_INVALID_ARG),
+    (dict(hq=40, hkv=4), PA_ERR_UNSUPPORTED),
+])
+def test_decode_append_rejects_bad_arguments(lib, kw, want):
+    assert _append(lib, **kw) == want
 
 
 @pytest.mark.parametrize("kw,want", [

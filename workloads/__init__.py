@@ -216,6 +216,15 @@ def decode_sweep(context, device="cpu", block_size=832):
     return paged_case(1003, [context], block_size, npg, peaked_frac=0.05, device=device)
 
 
+def decode_sweep_rotation(context, device="cpu", block_size=832, max_seqs=64):
+    """As decode_sweep, with as many sequences of `context` keys as the 1 GiB pool holds
+    on disjoint pages (at most max_seqs): a timing loop that decodes them one per step in
+    turn reads each sequence's K/V again only after the others', more than L2 holds."""
+    npg = pool_pages_for_bytes(GIB, block_size)
+    n = min(max_seqs, npg // -(-context // block_size))
+    return paged_case(1003, [context] * n, block_size, npg, peaked_frac=0.05, device=device)
+
+
 def prefill_chunk(device="cpu", q_len=4096, q_start=4096, block_size=832, num_pages=64):
     """q=4096 causal chunk at positions 4096..8191 over 4096 prior paged tokens."""
     return paged_case(1004, [q_start + q_len], block_size, num_pages, q_rows=q_len,
@@ -244,9 +253,10 @@ def prefill_mixed(device="cpu", block_size=832, num_pages=96):
 
 
 def batched_decode(device="cpu", num_seqs=16, lo=4096, hi=32768, block_size=832,
-                   num_pages=640):
+                   num_pages=640, seed=1005):
     """16 sequences with lengths uniform in [4096, 32768], one new token each, block
-    tables drawn without replacement from a shared shuffled pool of 640 pages."""
+    tables drawn without replacement from a shared shuffled pool of 640 pages.  The
+    lengths always come from seed 1005; `seed` draws the data and the pages."""
     rng = np.random.default_rng(1005)
     lens = rng.integers(lo, hi + 1, size=num_seqs).tolist()
-    return paged_case(1005, lens, block_size, num_pages, new_tokens=1, device=device)
+    return paged_case(seed, lens, block_size, num_pages, new_tokens=1, device=device)
