@@ -69,7 +69,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all",
                     help="comma list: sweep,bs784,batched,prefill,prefill_tail,prefill_first,"
-                         "prefill_mixed,prep or all/none")
+                         "prefill_mixed,prep or all/none; l2check (not in all) runs the "
+                         "stream of 8K steps that an ncu capture of DRAM bytes checks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--contexts", default="4096,8192,16384,32768",
@@ -381,6 +382,21 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     return r
 
 
+def l2check_leg(pa):
+    """For an ncu capture of dram__bytes_read.sum per split launch (--cache-control none):
+    32 consecutive 8K decode steps over 16 copies of the workload in turn (the headline
+    timing), then 16 steps of one copy (L2 warm, the control).  Small pools (11 pages per
+    copy) keep the device footprint under 1 GB."""
+    reps = [workloads.paged_case(1002 + 1000 * r, [8192], 832, 11, new_tokens=1,
+                                 device="cuda") for r in range(16)]
+    fns = [append_step_fn(pa, c, 8192)[0] for c in reps]
+    r = {"rotation_us_per_step": time_stream(fns, 32, 0) * 1e3,
+         "one_copy_us_per_step": time_stream(fns[:1], 16, 0) * 1e3}
+    del reps, fns
+    torch.cuda.empty_cache()
+    return r
+
+
 def input_prep_leg(pa, steps, warmup, flush):
     """Decode input preparation of one sequence for a two-group model (block sizes 832 and
     16): one pa_decode_input_prep launch against one pa_slot_mapping launch per group plus
@@ -635,6 +651,8 @@ def main():
             flush, peaks, "two copies of the workload (same lengths, 2.2 GB pools each), in turn")
         del reps, fns
         torch.cuda.empty_cache()
+    if rank == 0 and "l2check" in args.legs.split(","):
+        legs["l2check"] = l2check_leg(pa)
     if rank == 0 and "prep" in want:
         legs["decode_input_prep_2_groups"] = input_prep_leg(pa, args.steps, args.warmup, flush)
     if rank == 0 and "prefill_mixed" in want:
