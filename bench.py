@@ -591,7 +591,7 @@ def main():
 
     # ---- headline: timed K steps, barrier + synchronize on both sides
     value = kernel_gbs = k_ms = e2e_val = e2e_ms = alone_ms = None
-    step_ms = float("nan")
+    step_ms = None
     h2d = d2h = 0
     if not args.skip_headline:
         reps = headline_replicas("cuda")
@@ -706,7 +706,7 @@ def main():
                 "copies": "pa_copy kernels between pinned host buffers and the device, "
                           "inside the steps' CUDA graph"},
         # per step: the split decode (slot derivation + KV write fused) and the LSE combine
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 0 if args.skip_headline else 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": kernel_gbs / peaks["hbm_gbs"] if kernel_gbs else None,
                      "traffic": None,
