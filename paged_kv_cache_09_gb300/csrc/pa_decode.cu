@@ -15,7 +15,10 @@
 //     boxes capped an SM below its share of HBM bandwidth; 32-row boxes do not.  When
 //     a page holds an odd number of tiles, a stage whose two tiles lie in different
 //     pages is loaded with 16-row boxes.  Rows past a page end come back as zeros and
-//     are masked.
+//     are masked.  The loads mark their L2 lines evict-first: each is read once.
+//   * With a new token to append (a decode step), one consumer warp of the CTA holding
+//     that token's tile writes its K/V row at the slot the block table gives (or checks
+//     a given slot) before the producer loads that tile.
 //   * The consumer warps (four with a 4-stage ring for short splits, three with a 6-stage
 //     ring for long ones) take tiles round-robin (short splits: tile i -> warp i % C,
 //     half i % 2 of ring slot (i / 2) % S, a slot released by the warps of both its tiles;
@@ -25,9 +28,10 @@
 //     O^T += V^T P^T with P split into a BF16 high part and a BF16 low part (two MMAs),
 //     which keeps P to ~16 significant bits.
 //   * At the end the warps merge their (max, sum, acc) through shared memory and the
-//     CTA writes one fp32 partial per query head; the combine kernel merges the splits
-//     with a log-sum-exp and writes BF16.  Both kernels use programmatic dependent
-//     launch, so the combine's launch overlaps the split kernel's tail.
+//     CTA writes one fp32 partial per query head; the combine kernel (four CTAs per
+//     query head, 64 dims each) merges the splits with a log-sum-exp and writes BF16.
+//     Both kernels use programmatic dependent launch, so the combine's launch overlaps
+//     the split kernel's tail.
 #include <math_constants.h>
 
 #include "pa_device.cuh"

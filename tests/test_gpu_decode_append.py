@@ -199,3 +199,70 @@ def test_kernel_events_inside_a_graph(cuda_lib):
         ms = [a.elapsed_time(b) for a, b in evs]
         assert all(0.0 < t < 50.0 for t in ms), ms
     assert pa.device_errors() == 0
+
+
+def test_append_unbind_view_page_stride(cuda_lib):
+    # K and V as the two halves of one [pages, 2, BS, Hkv, D] tensor (page stride twice
+    # a page): the same writes and outputs as separate caches.
+    pa = cuda_lib
+    a = workloads.paged_case(61, [8192], 832, 12, new_tokens=1, device="cuda")
+    b = workloads.paged_case(61, [8192], 832, 12, new_tokens=1, device="cuda")
+    kv = torch.stack([b.k_cache, b.v_cache], dim=1)
+    b.k_cache, b.v_cache = kv.unbind(1)
+    out_b = pa.decode_append(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.scale,
+                             8192, b.new_k, b.new_v)
+    out_a, _ = _check_step(pa, a, "append, separate caches")
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert np.array_equal(bits(kv[:, 0]), bits(a.k_cache))
+    assert np.array_equal(bits(kv[:, 1]), bits(a.v_cache))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 2), (8, 1), (12, 4)])
+def test_append_other_group_sizes(cuda_lib, hq, hkv):
+    case = workloads.paged_case(930 + hq, [700, 2000, 1], 64, 48, hq=hq, hkv=hkv,
+                                new_tokens=1, device="cuda")
+    _check_step(cuda_lib, case, f"append group {hq}/{hkv}")
+
+
+def test_append_max_seq_len_above_actual_lengths(cuda_lib):
+    # The split plan is made for max_seq_len; shorter sequences leave splits empty, and
+    # the newest token's tile may sit in any split.
+    pa = cuda_lib
+    case = workloads.paged_case(62, [100, 5000, 1, 833], 832, 16, new_tokens=1,
+                                device="cuda", max_blocks=40)
+    k_host, v_host = bits(case.k_cache), bits(case.v_cache)
+    slots = torch.empty(4, dtype=torch.int64, device="cuda")
+    out = _append(pa, case, slot_mapping=slots, max_seq_len=40 * 832)
+    torch.cuda.synchronize()
+    want_slots, k_ref, v_ref, ref = _oracle_step(case, k_host, v_host)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
+    assert np.array_equal(bits(case.k_cache), k_ref)
+    assert_attention_close(out, ref, "append, max_seq_len slack")
+    assert pa.device_errors() == 0
+
+
+@pytest.mark.parametrize("T", [3001, 8192])
+def test_append_block_size_784_vs_832_bitwise(cuda_lib, T):
+    # The appended token's tile and every sum are the same at both page sizes (784 and
+    # 832 are multiples of the 16-token tile): identical output bits.
+    pa = cuda_lib
+    g = torch.Generator(device="cuda").manual_seed(4)
+    kc = torch.randn(T, 4, 256, generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(T, 4, 256, generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn(1, 24, 256, generator=g, device="cuda").to(torch.bfloat16)
+    outs = []
+    for bs in (784, 832):
+        npg = -(-T // bs)
+        k_cache = torch.zeros(npg + 2, bs, 4, 256, dtype=torch.bfloat16, device="cuda")
+        v_cache = torch.zeros_like(k_cache)
+        perm = torch.randperm(npg + 2, generator=torch.Generator().manual_seed(bs))[:npg]
+        bt = perm.to(torch.int32).view(1, -1).cuda()
+        slots = pa.slot_mapping(torch.arange(T - 1, dtype=torch.int32, device="cuda"), bt, bs)
+        pa.reshape_and_cache(kc[:T - 1], vc[:T - 1], k_cache, v_cache, slots)
+        sl = torch.tensor([T], dtype=torch.int32, device="cuda")
+        outs.append(pa.decode_append(q, k_cache, v_cache, bt, sl, 1 / 16, T,
+                                     kc[T - 1:].contiguous(), vc[T - 1:].contiguous()))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    assert pa.device_errors() == 0
