@@ -97,10 +97,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
 
 // Loads kept in program order (volatile asm): a batch of independent loads is issued
 // together before the first of them is used, even where the compiler would rather sink
-// some below code that waits for another.
+// some below code that waits for another.  They read L2 only (.cg): the data was
+// written by the previous grid and is read once, so an L1 copy could only be stale.
 __device__ __forceinline__ float2 ld_f2_ordered(const float2 *p) {
     float2 v;
-    asm volatile("ld.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
     return v;
 }
 
