@@ -59,6 +59,9 @@ HEADLINE = ("decode batch 1, context 8192 (new token at 8191 written by slot map
             "24 q / 4 kv heads, d=256, BF16 N(0,1), block_size 832, shuffled 64-page pool")
 KV_BYTES_PER_TOKEN = 2 * workloads.HKV * workloads.HEAD_DIM * 2   # K+V, all KV heads
 L2_FLUSH_BYTES = 512 << 20
+# DRAM bytes (read + write) of one 8K split launch in an ncu capture of the current split
+# kernel (summarised under profiles/); None whenever the kernel changes after a capture.
+SPLIT_8K_DRAM_BYTES = 33_629_952 + 0
 
 
 def parse():
@@ -709,7 +712,8 @@ def main():
         "gpu_launches": 0 if args.skip_headline else 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": kernel_gbs / peaks["hbm_gbs"] if kernel_gbs else None,
-                     "traffic": None,
+                     "traffic": SPLIT_8K_DRAM_BYTES,
+                     "traffic_unit": "bytes per launch",
                      "kernel": "decode_split_kernel",
                      "algorithmic_bytes_per_launch": 8192 * KV_BYTES_PER_TOKEN,
                      "kernel_ms": k_ms, "peak_source": f"{peaks['source']} hbm_gbs",
