@@ -62,6 +62,8 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one 8K split launch in an ncu capture of the current split
 # kernel (summarised under profiles/); None whenever the kernel changes after a capture.
 SPLIT_8K_DRAM_BYTES = 33_629_952 + 0
+# The same for one prefill launch of the q=4096 chunk over 4096 prior tokens.
+PREFILL_Q4096_DRAM_BYTES = 86_102_528 + 17_982_976
 
 
 def parse():
@@ -380,7 +382,8 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
          "kernel_tflops": flops / (k_ms * 1e-3) / 1e12}
     peak = peaks["bf16_tflops"]
     r["roofline"] = {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
-                     "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak,
+                     "traffic": PREFILL_Q4096_DRAM_BYTES if make == "prefill_chunk" else None,
                      "peak_source": f"{peaks['source']} bf16 dense burst"}
     return r
 
