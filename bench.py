@@ -438,10 +438,10 @@ def e2e_leg(pa, cases, steps, warmup):
     """The headline step through the public API with pinned host buffers, timed as a
     stream of steps like the headline: per step, one H2D copy of that step's inputs (q,
     the new token's K/V, block table and seq_lens of its replica, packed in one pinned
-    staging buffer), the append decode (slot, KV write, split decode, combine), and the
-    D2H copy of the output; the steps cycle the replicas inside one CUDA graph.  Both
-    copies are pa_copy kernels (a copy-engine node costs several microseconds more per
-    copy on this system)."""
+    staging buffer, by a pa_copy kernel: a copy-engine node costs several microseconds
+    more on this system), then the append decode (slot, KV write, split decode,
+    combine), whose combine writes the output straight into a pinned host buffer (the
+    step's D2H transfer); the steps cycle the replicas inside one CUDA graph."""
     names = ("q", "new_k", "new_v", "block_table", "seq_lens")
     fns, outs = [], []
     h2d = d2h = 0
@@ -464,26 +464,27 @@ def e2e_leg(pa, cases, steps, warmup):
             view(stage_h, k).copy_(srcs[k].cpu())
         dev = {k: view(stage_d, k) for k in names}
         out_h = torch.empty((S, hq, d), dtype=torch.bfloat16).pin_memory()
-        out_d = torch.empty((S, hq, d), dtype=torch.bfloat16, device="cuda")
         ws = torch.empty(max(256, pa.decode_workspace_size(S, hq, case.k_cache.shape[2], d,
                                                             case.block_size, msl)),
                          dtype=torch.uint8, device="cuda")
         slots = torch.empty(S, dtype=torch.int64, device="cuda")
         h2d, d2h = total, out_h.numel() * out_h.element_size()
 
-        def step(case=case, stage_h=stage_h, stage_d=stage_d, dev=dev, out_h=out_h,
-                 out_d=out_d, ws=ws, slots=slots, msl=msl):
+        def step(case=case, stage_h=stage_h, stage_d=stage_d, dev=dev, out_h=out_h, ws=ws,
+                 slots=slots, msl=msl):
             pa.copy(stage_d, stage_h)
             pa.decode_append(dev["q"], case.k_cache, case.v_cache, dev["block_table"],
                              dev["seq_lens"], case.scale, msl, dev["new_k"], dev["new_v"],
-                             out=out_d, workspace=ws, slot_mapping=slots)
-            pa.copy(out_h, out_d)
+                             out=out_h, workspace=ws, slot_mapping=slots)
         fns.append(step)
-        outs.append((out_h, out_d))
+        outs.append((out_h, case, msl))
     ms = time_stream(fns, steps, warmup)
     torch.cuda.synchronize()
-    for out_h, out_d in outs[:min(len(outs), steps)]:
-        assert torch.equal(out_h, out_d.cpu()), "a step's D2H copy does not hold its output"
+    # Each step's host output equals the same decode written to device memory.
+    for out_h, case, msl in outs[:min(len(outs), steps)]:
+        ref = pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                        case.scale, msl)
+        assert torch.equal(out_h, ref.cpu()), "a step's host output differs from the decode's"
     return ms, h2d, d2h
 
 
@@ -709,7 +710,8 @@ def main():
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "copies": "pa_copy kernels between pinned host buffers and the device, "
+                "copies": "H2D: one pa_copy kernel from a pinned staging buffer; D2H: the "
+                          "combine kernel writes the output into a pinned host buffer; all "
                           "inside the steps' CUDA graph"},
         # per step: the split decode (slot derivation + KV write fused) and the LSE combine
         "gpu_launches": 0 if args.skip_headline else 2 * args.steps,

@@ -135,7 +135,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * and query head h,
  *     out[s, h] = softmax_t( scale * q[s, h] . k_t ) . v_t,   t in [0, seq_lens[s])
  * with k_t, v_t of KV head h / (Hq / Hkv) fetched through row s of block_table.
- *   q, out       BF16 [num_seqs, num_q_heads, head_dim], contiguous
+ *   q, out       BF16 [num_seqs, num_q_heads, head_dim], contiguous.  out may also be
+ *                page-locked host memory (cudaHostAlloc or cudaHostRegister): the combine
+ *                kernel then writes the result straight to the host.  Other host memory
+ *                is refused (PA_ERR_INVALID_ARG).
  *   block_table  int32 [num_seqs, bt_stride]; entries past a sequence's last page unused
  *   seq_lens     int32 [num_seqs], device; each in [1, max_seq_len]
  *   workspace    device scratch of >= pa_decode_workspace_size(...) bytes, 256-byte

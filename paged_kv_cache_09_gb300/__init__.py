@@ -109,6 +109,15 @@ def _check(t, name, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
+def _check_out(out, like):
+    """A caller's decode output: BF16, contiguous, shaped like q, on the GPU or in
+    page-locked host memory (which the combine kernel writes directly)."""
+    if not isinstance(out, torch.Tensor) or not (out.is_cuda or out.is_pinned()):
+        raise TypeError("out must be a CUDA tensor or a pinned host tensor")
+    if out.dtype != torch.bfloat16 or out.shape != like.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous BF16 tensor shaped like q")
+
+
 def _check_cache(k_cache, v_cache):
     for n, c in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check(c, n, torch.bfloat16, 4)
@@ -241,6 +250,8 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, scale, max_seq_len, out=N
     _, bs, hkv, _ = k_cache.shape
     if out is None:
         out = torch.empty_like(q)
+    else:
+        _check_out(out, q)
     need = decode_workspace_size(S, hq, hkv, d, bs, max_seq_len)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -279,6 +290,8 @@ def decode_append(q, k_cache, v_cache, block_table, seq_lens, scale, max_seq_len
         raise ValueError("new_k / new_v must be [num_seqs, num_kv_heads, head_dim]")
     if out is None:
         out = torch.empty_like(q)
+    else:
+        _check_out(out, q)
     need = decode_workspace_size(S, hq, hkv, d, bs, max_seq_len)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

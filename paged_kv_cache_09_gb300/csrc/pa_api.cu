@@ -356,6 +356,11 @@ static int decode_impl(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *
     if (fused && (!new_k || !new_v || !aligned16(new_k) || !aligned16(new_v)))
         return PA_ERR_INVALID_ARG;
 
+    // The output may be page-locked host memory (the combine then writes the step's
+    // result straight to the host); pageable or unknown memory is refused.
+    const void *out_dev = nullptr;
+    if (!device_address(out, &out_dev)) return PA_ERR_INVALID_ARG;
+
     DeviceInfo dev;
     if (int rc = device_info(&dev)) return rc;
     const pa::DecodePlan plan =
@@ -404,7 +409,7 @@ static int decode_impl(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *
     a.block_size = block_size;
     a.num_pages = num_pages;
     a.scale = scale;
-    a.out = out;
+    a.out = static_cast<uint16_t *>(const_cast<void *>(out_dev));
     a.workspace = workspace;
     a.err = dev.err;
     take_kernel_events(&a.ev_start, &a.ev_stop);

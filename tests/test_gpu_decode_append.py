@@ -266,3 +266,34 @@ def test_append_block_size_784_vs_832_bitwise(cuda_lib, T):
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
     assert pa.device_errors() == 0
+
+
+def test_append_output_in_pinned_host_memory(cuda_lib):
+    # The combine writes the step's result straight into page-locked host memory: the
+    # same bits as a device output; pageable host memory is refused.
+    pa = cuda_lib
+    a = workloads.paged_case(63, [5000, 300], 832, 12, new_tokens=1, device="cuda")
+    b = workloads.paged_case(63, [5000, 300], 832, 12, new_tokens=1, device="cuda")
+    out_d = _append(pa, a)
+    out_h = torch.empty(b.q.shape, dtype=torch.bfloat16).pin_memory()
+    pa.decode_append(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.scale, 5000,
+                     b.new_k, b.new_v, out=out_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu())
+    with pytest.raises(TypeError):
+        pa.decode_append(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.scale, 5000,
+                         b.new_k, b.new_v, out=torch.empty(b.q.shape, dtype=torch.bfloat16))
+    pageable = np.zeros(b.q.numel() + 8, dtype=np.uint16)
+    addr = (pageable.ctypes.data + 15) // 16 * 16
+    import ctypes
+    ws = torch.empty(max(256, pa.decode_workspace_size(2, 24, 4, 256, 832, 5000)),
+                     dtype=torch.uint8, device="cuda")
+    rc = pa.load().pa_decode(ctypes.c_void_p(b.q.data_ptr()), ctypes.c_void_p(b.k_cache.data_ptr()),
+                             ctypes.c_void_p(b.v_cache.data_ptr()), b.k_cache.stride(0),
+                             b.k_cache.shape[0], ctypes.c_void_p(b.block_table.data_ptr()),
+                             b.block_table.stride(0), ctypes.c_void_p(b.seq_lens.data_ptr()), 2,
+                             5000, 24, 4, 256, 832, b.scale, ctypes.c_void_p(addr),
+                             ctypes.c_void_p(ws.data_ptr()), ws.numel(), None, None, None,
+                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 1   # PA_ERR_INVALID_ARG
+    assert pa.device_errors() == 0
