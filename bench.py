@@ -24,7 +24,7 @@ replayed after an L2 flush is reported too (config.step_alone_ms): it carries th
 graph's own launch, ~5 us here.
 
 Other legs, reported under "legs": the 4K/8K/16K/32K sweep (1 GiB pool, 5% of K rows
-x8), block_size 784 at 8K, batched decode (16 sequences, 4K-32K, appended token), the
+x8), 32K in generic 16- and 64-token pages, block_size 784 at 8K, batched decode (16 sequences, 4K-32K, appended token), the
 q=4096 prefill chunk over 4096 prior tokens (chunk KV write + prefill; TFLOP/s counts
 the causal work 4*D*Hq*sum_i(4096+i+1) = 6.185e11), and two more chunk shapes of the
 same prompt: the q=1685 tail chunk over 12288 prior tokens and the q=4096 first chunk
@@ -73,7 +73,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all",
-                    help="comma list: sweep,bs784,batched,prefill,prefill_tail,prefill_first,"
+                    help="comma list: sweep,small_pages,bs784,batched,prefill,prefill_tail,prefill_first,"
                          "prefill_mixed,prep or all/none; l2check (not in all) runs the "
                          "stream of 8K steps that an ncu capture of DRAM bytes checks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -626,7 +626,7 @@ def main():
 
     legs = {}
     want = set() if args.legs == "none" else (
-        {"sweep", "bs784", "batched", "prefill", "prefill_tail", "prefill_first",
+        {"sweep", "small_pages", "bs784", "batched", "prefill", "prefill_tail", "prefill_first",
          "prefill_mixed", "prep"}
         if args.legs == "all" else set(args.legs.split(",")))
     if rank == 0 and "sweep" in want:
@@ -642,6 +642,19 @@ def main():
             del c, fns
             torch.cuda.empty_cache()
         legs["decode_sweep_1gib_pool_peaked"] = sweep
+    if rank == 0 and "small_pages" in want:
+        small = {}
+        for bs in (16, 64):
+            c = workloads.decode_sweep_rotation(32768, "cuda", block_size=bs)
+            n = c.q.shape[0]
+            fns = [attn_fn(pa, c, s, 32768) for s in range(n)]
+            small[str(bs)] = decode_leg(
+                pa, fns, 32768, 1, args.steps, args.warmup, flush, peaks,
+                f"{n} sequences of 32768 tokens in {bs}-token pages of one 1 GiB pool, "
+                f"decoded one per step in turn")
+            del c, fns
+            torch.cuda.empty_cache()
+        legs["decode_32k_small_pages"] = small
     if rank == 0 and "bs784" in want:
         reps = headline_replicas("cuda", block_size=784, new_tokens=0)
         fns = [attn_fn(pa, c, 0, 8192) for c in reps]

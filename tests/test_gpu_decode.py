@@ -91,6 +91,17 @@ def test_decode_sweep_peaked_1gib_pool(cuda_lib, context):
     assert pa.device_errors() == 0
 
 
+@pytest.mark.parametrize("bs", [16, 64])
+def test_decode_32k_small_pages(cuda_lib, bs):
+    """Generic small pages: 2048 (16) or 512 (64) scattered pages per 32K sequence; with
+    16-token pages every stage's two tiles lie in different pages."""
+    pa = cuda_lib
+    case = workloads.decode_sweep(32768, "cuda", block_size=bs)
+    out = _gpu_decode(pa, case)
+    assert_attention_close(out, _oracle_decode(case), f"sweep 32K bs={bs}")
+    assert pa.device_errors() == 0
+
+
 def test_batched_decode_fused_write(cuda_lib):
     pa = cuda_lib
     case = workloads.batched_decode("cuda")
