@@ -93,6 +93,31 @@ bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_h
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K or V cache as a 5-D view {64 dims, rows, D / 64 chunks, Hkv, pages} for the decode:
+// one box of 64 dims x 16 rows x all D / 64 chunks x 1 head x 1 page holds a whole
+// 16-token tile of one KV head, laid out [chunk][row][128 B] with the 128-byte swizzle,
+// the same bytes four 64-dim boxes of the {D, Hkv, rows, pages} view would give.  The
+// dims are not in stride order (rows step Hkv * D elements, chunks 64); the tensor map
+// takes each dim's stride as given.
+bool make_tile_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_heads,
+                   int rows, int64_t num_pages, int64_t page_stride, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int chunks = head_dim / pa::kChunkElems;
+    cuuint64_t dims[5] = {(cuuint64_t)pa::kChunkElems, (cuuint64_t)rows, (cuuint64_t)chunks,
+                          (cuuint64_t)num_kv_heads, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)num_kv_heads * head_dim * 2,
+                             (cuuint64_t)pa::kChunkElems * 2, (cuuint64_t)head_dim * 2,
+                             (cuuint64_t)page_stride * 2};
+    cuuint32_t box[5] = {(cuuint32_t)pa::kChunkElems, (cuuint32_t)box_rows, (cuuint32_t)chunks,
+                         1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Query rows [q_len, Hq, D] as {D, Hq, q_len}; boxes of 64 dims x 1 head x box_rows.
 bool make_rows_map(CUtensorMap *m, const void *base, int head_dim, int num_heads, int rows,
                    int box_rows) {
@@ -134,8 +159,8 @@ bool cached_cache_map(CUtensorMap *m, const MapKey &k) {
             *m = e.map;
             return true;
         }
-    if (!make_cache_map(m, k.base, k.head_dim, k.num_kv_heads, k.rows, k.num_pages,
-                        k.page_stride, k.box_rows))
+    if (!make_tile_map(m, k.base, k.head_dim, k.num_kv_heads, k.rows, k.num_pages,
+                       k.page_stride, k.box_rows))
         return false;
     entries[next] = Entry{k, *m, true};
     next = (next + 1) % 16;
@@ -368,25 +393,14 @@ static int decode_impl(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *
     if (workspace_bytes < pa::decode_workspace_bytes(num_seqs, num_q_heads, plan))
         return PA_ERR_INVALID_ARG;
 
-    // Stage-wide boxes, plus tile-high boxes when a page holds an odd number of tiles (a
-    // stage may then straddle two pages).  With one tile per page the stage-wide maps are
-    // never used and take tile-high boxes too.
-    CUtensorMap maps[4];
-    const int box_rows = plan.tiles_per_page > 1 ? pa::kDecBoxRows : pa::kDecTile;
+    // Tile boxes: one 16-row box per tile of K or V (two tiles of a stage may lie in
+    // different pages).
+    CUtensorMap maps[2];
     if (!cached_cache_map(&maps[0], MapKey{k_cache, head_dim, num_kv_heads, block_size,
-                                           box_rows, num_pages, page_stride}) ||
+                                           pa::kDecTile, num_pages, page_stride}) ||
         !cached_cache_map(&maps[1], MapKey{v_cache, head_dim, num_kv_heads, block_size,
-                                           box_rows, num_pages, page_stride}))
+                                           pa::kDecTile, num_pages, page_stride}))
         return PA_ERR_CUDA;
-    if (plan.tiles_per_page % pa::kDecPair == 0) {
-        maps[2] = maps[0];
-        maps[3] = maps[1];
-    } else if (!cached_cache_map(&maps[2], MapKey{k_cache, head_dim, num_kv_heads, block_size,
-                                                  pa::kDecTile, num_pages, page_stride}) ||
-               !cached_cache_map(&maps[3], MapKey{v_cache, head_dim, num_kv_heads, block_size,
-                                                  pa::kDecTile, num_pages, page_stride})) {
-        return PA_ERR_CUDA;
-    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     pa::DecodeArgs a;

@@ -10,12 +10,14 @@
 //     head, so each K/V byte is read from HBM once for the whole group.
 //   * Tiles are 16 page-local tokens; a ring stage holds two consecutive tiles (32 KB).
 //     One producer thread reads each block-table entry once and issues the stage's TMA
-//     loads: 4 x 128-byte-swizzled boxes of 32 rows for K and 4 for V.  A TMA box costs
-//     the SM about the same issue time whatever its height up to 64 rows, and 16-row
-//     boxes capped an SM below its share of HBM bandwidth; 32-row boxes do not.  When
-//     a page holds an odd number of tiles, a stage whose two tiles lie in different
-//     pages is loaded with 16-row boxes.  Rows past a page end come back as zeros and
-//     are masked.  The loads mark their L2 lines evict-first: each is read once.
+//     loads: one box per tile for K and one for V, each all 256 dims of the tile's 16
+//     rows (8 KB, a 5-D view of the cache whose box is laid out as four 128-byte-swizzled
+//     64-dim chunks).  The SM's cost of a TMA box grows slowly with its size, so the box
+//     count sets the issue rate: 16 boxes of 16 rows x 64 dims a stage capped an SM below
+//     its share of HBM bandwidth; 4 boxes a stage leave room to spare, whether or not the
+//     two tiles lie in one page (16-token pages: 32K step 32.3 -> 26.9 us; batched decode
+//     195.7 -> 187.3 us).  Rows past a page end come back as zeros and are masked.  The
+//     loads mark their L2 lines evict-first: each is read once.
 //   * With a new token to append (a decode step), one consumer warp of the CTA holding
 //     that token's tile writes its K/V row at the slot the block table gives (or checks
 //     a given slot) before the producer loads that tile.
@@ -41,9 +43,11 @@ namespace pa {
 
 namespace {
 
-constexpr int kDecTileBytes = kDecTile * 128;               // one tile's rows of a 64-dim chunk
-constexpr int kDecChunkBytes = kDecBoxRows * 128;           // one 64-dim chunk of a stage: 4 KB
-constexpr int kDecHalf = kChunks * kDecChunkBytes;          // K (or V) of one stage: 16 KB
+// A ring stage is [K | V], each [tile of the pair][64-dim chunk][16 rows][128 B]: one TMA
+// box (all 256 dims of a tile's 16 rows) fills one tile's K or V.
+constexpr int kDecTileBytes = kDecTile * 128;               // one tile's rows of a 64-dim chunk: 2 KB
+constexpr int kDecTileKBytes = kChunks * kDecTileBytes;     // one tile's K (or V), all dims: 8 KB
+constexpr int kDecHalf = kDecPair * kDecTileKBytes;         // K (or V) of one stage: 16 KB
 constexpr int kDecStageBytes = 2 * kDecHalf;                // 32 KB
 // Merge buffers, per warp and head: O row (padded by 4 floats, so that the 4 head
 // columns a warp stores at once fall in different banks), max and sum.
@@ -127,46 +131,22 @@ __device__ __forceinline__ void write_newest_token(const DecodeKParams &p, const
 
 // The decode's four tensor maps: K and V with 32-row boxes, and with 16-row boxes.
 struct DecMaps {
-    CUtensorMap k, v, k16, v16;
+    CUtensorMap k, v;
 };
 
-// Loads rows [off, off + 32) of page `page` (K and V of KV head g: both tiles of a
-// stage that lies in one page) into ring stage `st`, completing on `bar`.  Rows past the
-// page end, and a page outside the pool, read as zeros.  A decode reads each K/V line
-// once, so the loads mark their L2 lines evict-first (measured: the 8K step 12.06 ->
-// 11.47 us, the 32K step 26.4 -> 25.3 us).
+// Loads the two tiles of a ring stage, rows [off0, off0 + 16) of page0 and rows
+// [off1, off1 + 16) of page1 (K and V of KV head g), into ring stage `st`, completing on
+// `bar`: four boxes of 8 KB.  Rows past a page end, and a page outside the pool, read as
+// zeros.  A decode reads each K/V line once, so the loads mark their L2 lines
+// evict-first (measured: the 8K step 12.06 -> 11.47 us, the 32K step 26.4 -> 25.3 us).
 __device__ __forceinline__ void load_stage(const DecMaps &mp, uint8_t *st, uint64_t *bar, int g,
-                                           int off, int page) {
+                                           int off0, int page0, int off1, int page1) {
     const uint64_t pol = l2_evict_first_policy();
     mbar_arrive_expect_tx(bar, kDecStageBytes);
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c)
-        tma_load_4d_hint(st + c * kDecChunkBytes, &mp.k, bar, c * kChunkElems, g, off, page,
-                         pol);
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c)
-        tma_load_4d_hint(st + kDecHalf + c * kDecChunkBytes, &mp.v, bar, c * kChunkElems, g,
-                         off, page, pol);
-}
-
-// Loads a stage whose first tile is rows [off, off + 16) of `page` (that page's last
-// tile) and whose second tile is rows [0, 16) of `page2`, with 16-row boxes.
-__device__ __forceinline__ void load_stage_split(const DecMaps &mp, uint8_t *st, uint64_t *bar,
-                                                 int g, int off, int page, int page2) {
-    const uint64_t pol = l2_evict_first_policy();
-    mbar_arrive_expect_tx(bar, kDecStageBytes);
-#pragma unroll
-    for (int h = 0; h < kDecPair; ++h) {
-        const int o = h == 0 ? off : 0, pg = h == 0 ? page : page2;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-            tma_load_4d_hint(st + c * kDecChunkBytes + h * kDecTileBytes, &mp.k16, bar,
-                             c * kChunkElems, g, o, pg, pol);
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-            tma_load_4d_hint(st + kDecHalf + c * kDecChunkBytes + h * kDecTileBytes, &mp.v16,
-                             bar, c * kChunkElems, g, o, pg, pol);
-    }
+    tma_load_5d_hint(st, &mp.k, bar, 0, off0, 0, g, page0, pol);
+    tma_load_5d_hint(st + kDecTileKBytes, &mp.k, bar, 0, off1, 0, g, page1, pol);
+    tma_load_5d_hint(st + kDecHalf, &mp.v, bar, 0, off0, 0, g, page0, pol);
+    tma_load_5d_hint(st + kDecHalf + kDecTileKBytes, &mp.v, bar, 0, off1, 0, g, page1, pol);
 }
 
 __device__ __forceinline__ int seq_tiles(int seq_len, int block_size, int tiles_per_page) {
@@ -215,8 +195,6 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     if (warp == kDecConsumers && lane == 0) {
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
-        tma_prefetch_desc(&maps.k16);
-        tma_prefetch_desc(&maps.v16);
     }
     __syncthreads();
     pdl_wait();
@@ -240,7 +218,8 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     int page0 = 0;
     if (producer) page0 = bt[lp0];
     const int seq_len = checked_seq_len(p, seq, threadIdx.x == 0 && split == 0 && g == 0);
-    if (producer && spec) load_stage(maps, smem, &full[0], g, off0, page0);
+    if (producer && spec)
+        load_stage(maps, smem, &full[0], g, off0, page0, off0 + kDecTile, page0);
     const int ntiles = seq_tiles(seq_len, p.block_size, tpp);
     const int t1 = min(ntiles, t0 + p.tiles_per_split);
     if (t0 >= t1) {
@@ -276,7 +255,8 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                 // before that token was written: load it again once the first load has
                 // landed and the write is done.  Its consumers wait for both loads.
                 if (mbar_wait(&full[0], 0, p.err) && mbar_wait(written, 0, p.err))
-                    load_stage(maps, smem, &full[0], g, off0, page0);
+                    load_stage(maps, smem, &full[0], g, off0, page0, off0 + kDecTile,
+                               page0);
             }
             for (int m = spec ? 1 : 0; m < nst; ++m) {
                 const int s = m % kDecStages;
@@ -298,15 +278,16 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                 if (writes_newest && m == nst - 1 && !mbar_wait(written, 0, p.err)) break;
                 uint8_t *st = smem + s * kDecStageBytes;
                 if (tip + 1 < tpp) {
-                    load_stage(maps, st, &full[s], g, tip * kDecTile, page);
+                    load_stage(maps, st, &full[s], g, tip * kDecTile, page,
+                               (tip + 1) * kDecTile, page);
                 } else {
                     // The first tile closes its page: the second opens the next page, or
                     // lies past the split's end and reads as zeros from page -1.
                     const bool second = j + 1 < t1;
                     if (second && (page_next < 0 || page_next >= p.num_pages))
                         atomicOr(p.err, kErrPage);
-                    load_stage_split(maps, st, &full[s], g, tip * kDecTile, page,
-                                     second ? page_next : -1);
+                    load_stage(maps, st, &full[s], g, tip * kDecTile, page, 0,
+                               second ? page_next : -1);
                 }
             }
         }
@@ -348,19 +329,19 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
         const int off = (j - lp * tpp) * kDecTile;
         const int tok0 = lp * p.block_size + off;
         const int nvalid = min(kDecTile, min(p.block_size - off, seq_len - tok0));
-        const uint32_t kb = sbase + s * kDecStageBytes + h * kDecTileBytes;
+        const uint32_t kb = sbase + s * kDecStageBytes + h * kDecTileKBytes;
         const uint32_t vb = kb + kDecHalf;
 
         if (nvalid < kDecTile) {
             // Rows past the sequence end may hold anything (even NaN): zero them in V
             // so that a zero weight cannot meet a NaN inside the MMA.
-            uint8_t *vp = smem + s * kDecStageBytes + kDecHalf + h * kDecTileBytes;
+            uint8_t *vp = smem + s * kDecStageBytes + kDecHalf + h * kDecTileKBytes;
             const int per_chunk = (kDecTile - nvalid) * 8;
             for (int u = lane; u < per_chunk * kChunks; u += 32) {
                 const int c = u / per_chunk;
                 const int r = nvalid + (u - c * per_chunk) / 8;
                 const int unit = u & 7;
-                *reinterpret_cast<uint4 *>(vp + c * kDecChunkBytes + r * 128 + unit * 16) =
+                *reinterpret_cast<uint4 *>(vp + c * kDecTileBytes + r * 128 + unit * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
@@ -375,9 +356,9 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
 #pragma unroll
             for (int kk = 0; kk < 16; kk += 2) {
                 uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-                ldsm_x4(swz128(kb + (kk >> 2) * kDecChunkBytes, row, (kk & 3) * 2 + uhi), a0,
+                ldsm_x4(swz128(kb + (kk >> 2) * kDecTileBytes, row, (kk & 3) * 2 + uhi), a0,
                         a1, a2, a3);
-                ldsm_x4(swz128(kb + ((kk + 1) >> 2) * kDecChunkBytes, row,
+                ldsm_x4(swz128(kb + ((kk + 1) >> 2) * kDecTileBytes, row,
                                ((kk + 1) & 3) * 2 + uhi),
                         c0, c1, c2, c3);
                 mma_bf16_16816(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
@@ -434,7 +415,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
 #pragma unroll
             for (int mt = 0; mt < 16; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(swz128(vb + (mt >> 2) * kDecChunkBytes, row, (mt & 3) * 2 + ulo), a0,
+                ldsm_x4_t(swz128(vb + (mt >> 2) * kDecTileBytes, row, (mt & 3) * 2 + ulo), a0,
                           a1, a2, a3);
                 mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
                 mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
@@ -704,8 +685,6 @@ cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const D
     DecMaps maps;
     maps.k = tmaps[0];
     maps.v = tmaps[1];
-    maps.k16 = tmaps[2];
-    maps.v16 = tmaps[3];
     e = launch_pdl(split_kernel, grid, dim3(threads), smem, stream, maps, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = record_event(a.ev_stop, stream)) != cudaSuccess) return e;

@@ -118,6 +118,19 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+// 5-D tiled load of one box into shared memory with an L2 cache policy (see
+// l2_evict_first_policy), completing on `bar`.
+__device__ __forceinline__ void tma_load_5d_hint(void *smem_dst, const CUtensorMap *m,
+                                                 uint64_t *bar, int c0, int c1, int c2, int c3,
+                                                 int c4, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // tma_load_4d with an L2 cache policy (see l2_evict_first_policy).
 __device__ __forceinline__ void tma_load_4d_hint(void *smem_dst, const CUtensorMap *m,
                                                  uint64_t *bar, int c0, int c1, int c2, int c3,

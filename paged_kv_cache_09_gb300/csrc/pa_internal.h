@@ -83,7 +83,6 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
 // ----------------------------------------------------------------- decode
 constexpr int kDecTile = 16;       // tokens per MMA tile (page-local)
 constexpr int kDecPair = 2;        // tiles per ring stage
-constexpr int kDecBoxRows = kDecTile * kDecPair;  // rows of the stage-wide TMA boxes
 // Two shapes of the split kernel (consumer warps, 32 KB ring stages): splits of up to
 // kDecShortTiles tiles (the tail of the stream and the CTA merge are a large share of their
 // time) run with four consumer warps and a 4-stage ring; longer splits with three consumer
@@ -139,9 +138,8 @@ struct DecodeArgs {
     int64_t page_stride;            // elements between consecutive pages
 };
 
-// tmaps: K and V with kDecBoxRows-row boxes, then K and V with kDecTile-row boxes (used
-// for a stage whose two tiles lie in different pages; the first two again when a page
-// holds an even number of tiles, since then no stage straddles a page).
+// tmaps: K and V as 5-D views whose boxes hold one 16-token tile of one KV head, all
+// dims (the two tiles of a ring stage are two boxes, from one page or from two).
 cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const DecodePlan &plan,
                           cudaStream_t stream);
 
