@@ -24,10 +24,10 @@ replayed after an L2 flush is reported too (config.step_alone_ms): it carries th
 graph's own launch, ~5 us here.
 
 Other legs, reported under "legs": the 4K/8K/16K/32K sweep (1 GiB pool, 5% of K rows
-x8), 32K in generic 16- and 64-token pages, block_size 784 at 8K, batched decode (16 sequences, 4K-32K, appended token), the
-q=4096 prefill chunk over 4096 prior tokens (chunk KV write + prefill; TFLOP/s counts
-the causal work 4*D*Hq*sum_i(4096+i+1) = 6.185e11), and two more chunk shapes of the
-same prompt: the q=1685 tail chunk over 12288 prior tokens and the q=4096 first chunk
+x8), 32K in generic 16- and 64-token pages, block_size 784 at 8K, batched decode (16
+sequences, 4K-32K, appended token), the q=4096 prefill chunk over 4096 prior tokens
+(chunk KV write + prefill; TFLOP/s counts the causal work 4*D*Hq*sum_i(4096+i+1) =
+6.185e11), and two more chunk shapes of the same prompt: the q=1685 tail chunk over 12288 prior tokens and the q=4096 first chunk
 (no prior tokens); a mixed batch of four sequences' chunks in one varlen call; and the
 decode input preparation of a two-group model.  The prefill and input-preparation legs
 replay a single-step graph after an L2 flush per step (a 512 MiB read outside the
@@ -61,7 +61,7 @@ KV_BYTES_PER_TOKEN = 2 * workloads.HKV * workloads.HEAD_DIM * 2   # K+V, all KV 
 L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one 8K split launch in an ncu capture of the current split
 # kernel (summarised under profiles/); None whenever the kernel changes after a capture.
-SPLIT_8K_DRAM_BYTES = 33_629_952 + 0
+SPLIT_8K_DRAM_BYTES = 33_625_856 + 0
 # The same for one prefill launch of the q=4096 chunk over 4096 prior tokens.
 PREFILL_Q4096_DRAM_BYTES = 86_102_528 + 17_982_976
 
@@ -73,8 +73,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all",
-                    help="comma list: sweep,small_pages,bs784,batched,prefill,prefill_tail,prefill_first,"
-                         "prefill_mixed,prep or all/none; l2check (not in all) runs the "
+                    help="comma list: sweep,small_pages,bs784,batched,prefill,prefill_tail,"
+                         "prefill_first,prefill_mixed,prep or all/none; l2check (not in all) runs the "
                          "stream of 8K steps that an ncu capture of DRAM bytes checks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
