@@ -245,14 +245,19 @@ def stream_graph(fns, steps):
     return graph_of(run)
 
 
-def time_stream(fns, steps, warmup):
+def time_stream(fns, steps, warmup, flush):
     """Device ms per step of `steps` consecutive steps replayed as ONE CUDA graph (so the
     graph's own launch is paid once, as in a serving loop that captures a whole model
     step).  The cycled steps read disjoint inputs that together exceed L2 several times,
-    so no step finds its K/V in L2.  W eager warm-up steps first."""
+    so no step finds its K/V in L2.  W eager warm-up steps first, then one L2 flush: the
+    decode's K/V loads are evict-first, so lines that generating the inputs left in L2 at
+    normal priority would otherwise outlive the stream and be hit on every pass (an ncu
+    capture saw the last-generated copy read 10-26 of its 33.5 MB from L2)."""
     for i in range(warmup):
         fns[i % len(fns)]()
     g = stream_graph(fns, steps)
+    torch.cuda.synchronize()
+    flush()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
@@ -322,7 +327,7 @@ def decode_leg(pa, fns, tokens, seqs, steps, warmup, flush, peaks, rotation):
     """A decode leg timed as a stream of steps (time_stream), fns cycled; each step reads
     `tokens` context tokens of `seqs` sequences.  The split kernel's time: events around
     its launch, the first copy's step run eagerly after an L2 flush."""
-    step_ms = time_stream(fns, steps, warmup)
+    step_ms = time_stream(fns, steps, warmup, flush)
     kms = time_main_kernel(pa, fns[0], steps, warmup, flush)
     nbytes = tokens * KV_BYTES_PER_TOKEN
     k_ms = statistics.mean(kms)
@@ -388,7 +393,7 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     return r
 
 
-def l2check_leg(pa):
+def l2check_leg(pa, flush):
     """For an ncu capture of dram__bytes_read.sum per split launch (--cache-control none):
     32 consecutive 8K decode steps over 16 copies of the workload in turn (the headline
     timing), then 16 steps of one copy (L2 warm, the control).  Small pools (11 pages per
@@ -396,8 +401,8 @@ def l2check_leg(pa):
     reps = [workloads.paged_case(1002 + 1000 * r, [8192], 832, 11, new_tokens=1,
                                  device="cuda") for r in range(16)]
     fns = [append_step_fn(pa, c, 8192)[0] for c in reps]
-    r = {"rotation_us_per_step": time_stream(fns, 32, 0) * 1e3,
-         "one_copy_us_per_step": time_stream(fns[:1], 16, 0) * 1e3}
+    r = {"rotation_us_per_step": time_stream(fns, 32, 0, flush) * 1e3,
+         "one_copy_us_per_step": time_stream(fns[:1], 16, 0, flush) * 1e3}
     del reps, fns
     torch.cuda.empty_cache()
     return r
@@ -434,7 +439,7 @@ def input_prep_leg(pa, steps, warmup, flush):
     return r
 
 
-def e2e_leg(pa, cases, steps, warmup):
+def e2e_leg(pa, cases, steps, warmup, flush):
     """The headline step through the public API with pinned host buffers, timed as a
     stream of steps like the headline: per step, one H2D copy of that step's inputs (q,
     the new token's K/V, block table and seq_lens of its replica, packed in one pinned
@@ -478,7 +483,7 @@ def e2e_leg(pa, cases, steps, warmup):
                              out=out_h, workspace=ws, slot_mapping=slots)
         fns.append(step)
         outs.append((out_h, case, msl))
-    ms = time_stream(fns, steps, warmup)
+    ms = time_stream(fns, steps, warmup, flush)
     torch.cuda.synchronize()
     # Each step's host output equals the same decode written to device memory.
     for out_h, case, msl in outs[:min(len(outs), steps)]:
@@ -605,7 +610,7 @@ def main():
         fns = [append_step_fn(pa, c, 8192)[0] for c in reps]
         barrier(ws)
         torch.cuda.synchronize()
-        step_ms = time_stream(fns, args.steps, args.warmup)
+        step_ms = time_stream(fns, args.steps, args.warmup, flush)
         torch.cuda.synchronize()
         barrier(ws)
         total_ms = max_over_ranks(step_ms * args.steps, ws)
@@ -618,7 +623,7 @@ def main():
         # (its own graph launch included), for comparison with the stream figure.
         alone_ms = statistics.mean(time_steps(graph_of(fns[0]).replay, args.steps,
                                               args.warmup, flush))
-        e2e_ms, h2d, d2h = e2e_leg(pa, reps, args.steps, args.warmup)
+        e2e_ms, h2d, d2h = e2e_leg(pa, reps, args.steps, args.warmup, flush)
         e2e_val = 8192 * KV_BYTES_PER_TOKEN / (e2e_ms * 1e-3) / 1e9
         assert pa.device_errors() == 0, "device error word set during the headline leg"
         del reps, fns
@@ -672,7 +677,7 @@ def main():
         del reps, fns
         torch.cuda.empty_cache()
     if rank == 0 and "l2check" in args.legs.split(","):
-        legs["l2check"] = l2check_leg(pa)
+        legs["l2check"] = l2check_leg(pa, flush)
     if rank == 0 and "prep" in want:
         legs["decode_input_prep_2_groups"] = input_prep_leg(pa, args.steps, args.warmup, flush)
     if rank == 0 and "prefill_mixed" in want:
