@@ -260,9 +260,9 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
             }
             for (int m = spec ? 1 : 0; m < nst; ++m) {
                 const int s = m % kDecStages;
-                if (m >= kDecStages &&
-                    !mbar_wait(&empty[s], ((m / kDecStages) - 1) & 1, p.err))
-                    break;
+                // The stage's block-table entries are read before the wait for its ring
+                // slot, so that their latency overlaps the wait (with small pages a
+                // stage needs one or two fresh entries).
                 const int j = t0 + m * kDecPair;
                 const int l = j / tpp;
                 const int tip = j - l * tpp;
@@ -274,6 +274,9 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                     if (page < 0 || page >= p.num_pages) atomicOr(p.err, kErrPage);
                     if (lp < lp_last) page_next = bt[lp + 1];
                 }
+                if (m >= kDecStages &&
+                    !mbar_wait(&empty[s], ((m / kDecStages) - 1) & 1, p.err))
+                    break;
                 // The last stage holds the token being decoded: wait until it is written.
                 if (writes_newest && m == nst - 1 && !mbar_wait(written, 0, p.err)) break;
                 uint8_t *st = smem + s * kDecStageBytes;
