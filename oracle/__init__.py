@@ -10,7 +10,8 @@ C code decodes them to their exact values itself.
 
 Function -> passage it follows (pages cited by post and section):
   slot_mapping       -- input-prep post §3.2 (slot = block_table[pos // bs] * bs + pos % bs)
-  decode_input_prep  -- input-prep post §4, §5: seq_lens = position + 1, query_start_loc,
+  decode_input_prep  -- input-prep post §2, §4, §5: seq_lens = position + 1 (0 for padding),
+                        query_start_loc = running count of query rows (none for padding),
                         input_ids from the sampled tokens, one slot mapping per KV group
   reshape_and_cache  -- page832 post §4 (cache layout [pages, BS, Hkv, D]) and the slot above
   attend_row         -- page832 post §1 (address translation) and §5 (score = q.k * scale,

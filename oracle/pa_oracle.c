@@ -88,10 +88,15 @@ int pa_oracle_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
     return 0;
 }
 
-/* Decode-step inputs [input-prep §4, §5]: num_seqs sequences decode one token each, at
- * positions[s] (tokens already cached).  The step's metadata is written once:
- * seq_lens[s] = position + 1 (0 for a padding entry), input_ids[s] = the token sampled by
- * the previous step, query_start_loc = 0, 1, ..., num_seqs (one query row per sequence).
+/* Decode-step inputs [input-prep §2, §4, §5]: num_seqs entries, each either a sequence
+ * that decodes one token at positions[s] (tokens already cached) or a padding entry
+ * (positions[s] < 0).  The step's metadata is written once:
+ *   seq_lens[s] = position + 1, and 0 for a padding entry;
+ *   input_ids[s] = the token sampled by the previous step;
+ *   query_start_loc[0] = 0 and query_start_loc[s + 1] = query_start_loc[s] + (query rows
+ *   of entry s): one row for a sequence, none for a padding entry.  With one sequence
+ *   followed by padding this gives the pages' [0, 1, 1, ...] beside [position + 1, 0, 0,
+ *   ...] (§2): a padded entry has no keys and owns no query row.
  * Then every KV-cache group g, with its own block table and block size, gets its slot
  * mapping by the slot formula above (row s of the group's table for sequence s). */
 int pa_oracle_decode_input_prep(const int32_t *positions, const int32_t *sampled_ids,
@@ -99,13 +104,14 @@ int pa_oracle_decode_input_prep(const int32_t *positions, const int32_t *sampled
                                 int32_t *query_start_loc, int num_seqs, int num_groups,
                                 const int32_t *const *block_tables, const int64_t *bt_strides,
                                 const int *block_sizes, int64_t *const *slot_mappings) {
+    query_start_loc[0] = 0;
     for (int s = 0; s < num_seqs; ++s) {
         int32_t pos = positions[s];
+        int query_rows = pos >= 0 ? 1 : 0;
         seq_lens[s] = pos >= 0 ? pos + 1 : 0;
         if (sampled_ids) input_ids[s] = sampled_ids[s];
-        query_start_loc[s] = s;
+        query_start_loc[s + 1] = query_start_loc[s] + query_rows;
     }
-    query_start_loc[num_seqs] = num_seqs;
     for (int g = 0; g < num_groups; ++g) {
         for (int s = 0; s < num_seqs; ++s) {
             int32_t seq = s;

@@ -60,10 +60,16 @@ def test_slot_mapping_hand_worked_table():
         assert int(got[0]) == int(want), (bs, pos)
 
 
+def _golden_lines(name):
+    """Non-empty lines of a golden file, comments (after #) removed, split on blanks."""
+    rows = [ln.split("#")[0].split() for ln in open(os.path.join(GOLDEN, name))]
+    return [r for r in rows if r]
+
+
 def test_decode_input_prep_hand_worked_step():
-    rows = [ln.split("#")[0].split() for ln in
-            open(os.path.join(GOLDEN, "decode_input_prep_hand.txt"))]
-    rows = [list(map(int, r)) for r in rows if r]
+    lines = _golden_lines("decode_input_prep_hand.txt")
+    qsl = [list(map(int, r[1:])) for r in lines if r[0] == "query_start_loc"]
+    rows = [list(map(int, r)) for r in lines if r[0] != "query_start_loc"]
     g0 = np.array([[5, 2, 7, 0], [3, 1, 6, 4], [9, 8, 11, 10]], dtype=np.int32)
     g1 = np.array([[1000 * (s + 1) + j for j in range(256)] for s in range(3)], dtype=np.int32)
     pos = np.array([r[1] for r in rows], np.int32)
@@ -73,7 +79,37 @@ def test_decode_input_prep_hand_worked_step():
     assert got["input_ids"].tolist() == [r[2] for r in rows]
     assert got["slot_mappings"][0].tolist() == [r[4] for r in rows]
     assert got["slot_mappings"][1].tolist() == [r[5] for r in rows]
-    assert got["query_start_loc"].tolist() == [0, 1, 2, 3]
+    assert [got["query_start_loc"].tolist()] == qsl
+
+
+def _expand_runs(tokens):
+    """'N*x' -> N copies of x; plain integers as they are."""
+    out = []
+    for t in tokens:
+        if "*" in t:
+            n, x = t.split("*")
+            out += [int(x)] * int(n)
+        else:
+            out.append(int(t))
+    return out
+
+
+def test_decode_input_prep_the_pages_step():
+    # One request at position 24576, two KV-cache groups of block size 16, buffers for
+    # 128 requests: query_start_loc [0, 1, 1, ...] and seq_lens [position + 1, 0, 0, ...].
+    f = {r[0]: _expand_runs(r[1:]) for r in _golden_lines("decode_input_prep_pages_step.txt")}
+    n = len(f["positions"])
+    rows = np.arange(n)[:, None] * 10000
+    cols = np.arange(1600)[None, :]
+    tables = [(3 * cols + 1 + rows).astype(np.int32), (2 * cols + 7 + rows).astype(np.int32)]
+    got = oracle.decode_input_prep(np.array(f["positions"], np.int32), tables, f["block_sizes"],
+                                   sampled_ids=np.array(f["sampled_ids"], np.int32))
+    assert len(f["query_start_loc"]) == n + 1
+    assert got["query_start_loc"].tolist() == f["query_start_loc"]
+    assert got["seq_lens"].tolist() == f["seq_lens"]
+    assert got["input_ids"].tolist() == f["input_ids"]
+    assert got["slot_mappings"][0].tolist() == f["slot_group0"]
+    assert got["slot_mappings"][1].tolist() == f["slot_group1"]
 
 
 def test_page_geometry_from_pages():
@@ -341,3 +377,76 @@ def test_slot_mapping_padding_position():
     bt = np.array([3, 1], dtype=np.int32)
     got = oracle.slot_mapping(np.array([-1, 5, -7], dtype=np.int32), bt, 4)
     assert [int(x) for x in got] == [-1, 1 * 4 + 1, -1]   # 5//4 = 1 -> page 1, offset 1
+
+
+# ---------------------------------------------------------------- mixed batch (varlen)
+def test_prefill_varlen_hand_worked_batch():
+    # Equal scores (q = 0) make each row the mean of the V rows it sees: the values in
+    # the golden file are those means, worked by hand for each chunk row's position.
+    f = {r[0]: r[1:] for r in _golden_lines("prefill_varlen_hand.txt") if r[0] != "row"}
+    want = [list(map(float, r[2:])) for r in _golden_lines("prefill_varlen_hand.txt")
+            if r[0] == "row"]
+    k_lens = [int(x) for x in f["k_lens"]]
+    cu = [int(x) for x in f["cu_seqlens_q"]]
+    bs, d, npool = 2, 8, 8
+    tables = np.array([[4, 0, 6], [2, 7, -1], [5, 1, -1]], dtype=np.int32)
+    rng = np.random.default_rng(2)
+    k_cache = np.full((npool, bs, 1, d), 0xFFFF, dtype=np.uint16)
+    v_cache = np.full_like(k_cache, 0xFFFF)
+    for s, L in enumerate(k_lens):
+        for t in range(L):  # whole pages enumerated: token t is page t // 2, slot t % 2
+            page, off = tables[s][t // bs], t % bs
+            k_cache[page, off, 0] = _bf16(rng.standard_normal(d))
+            v_cache[page, off, 0] = _bf16(np.full(d, 100.0 * s + t))
+    q = np.zeros((cu[-1], 1, d), dtype=np.uint16)  # BF16 +0
+    for col, causal in ((0, True), (1, False)):
+        got = oracle.prefill_varlen(q, k_cache, v_cache, tables, cu, k_lens, causal, 0.0625)
+        for r in range(cu[-1]):
+            assert np.all(got[r, 0] == want[r][col]), (causal, r, got[r, 0, 0], want[r][col])
+
+
+def test_prefill_varlen_chunk_rows_are_decodes_of_their_prefixes():
+    # A chunk is the last q_len tokens of its sequence: its first row sees
+    # k_len - q_len + 1 keys and its last row all k_len keys, which is what a decode of
+    # that many keys over the same block-table row computes.
+    rng = np.random.default_rng(11)
+    bs, hq, hkv, d = 16, 6, 2, 32
+    k_lens, q_rows = [40, 7, 33, 16], [5, 7, 0, 16]
+    npg = sum(-(-L // bs) for L in k_lens) + 2
+    perm = rng.permutation(npg).astype(np.int32)
+    mb = max(-(-L // bs) for L in k_lens)
+    tables = np.full((len(k_lens), mb), -1, dtype=np.int32)
+    k = 0
+    for s, L in enumerate(k_lens):
+        n = -(-L // bs)
+        tables[s, :n] = perm[k:k + n]
+        k += n
+    k_cache = _bf16(rng.standard_normal((npg, bs, hkv, d)))
+    v_cache = _bf16(rng.standard_normal((npg, bs, hkv, d)))
+    cu = np.concatenate([[0], np.cumsum(q_rows)]).astype(np.int32)
+    q = _bf16(rng.standard_normal((int(cu[-1]), hq, d)))
+    got = oracle.prefill_varlen(q, k_cache, v_cache, tables, cu, k_lens, True, 0.125)
+    for s, L in enumerate(k_lens):
+        r0, r1 = int(cu[s]), int(cu[s + 1])
+        if r1 == r0:
+            continue
+        for row, keys in ((r0, L - (r1 - r0) + 1), (r1 - 1, L)):
+            dec = oracle.decode(q[row:row + 1], k_cache, v_cache, tables[s:s + 1],
+                                np.array([keys], np.int32), 0.125)
+            np.testing.assert_allclose(got[row], dec[0], rtol=0, atol=1e-12)
+    # The rows of an empty chunk's neighbours stay in place: total rows = sum of chunks.
+    assert got.shape[0] == sum(q_rows)
+
+
+def test_prefill_varlen_of_one_sequence_is_its_chunk():
+    rng = np.random.default_rng(12)
+    bs, hq, hkv, d = 8, 4, 1, 16
+    L, ql = 29, 11
+    npg = -(-L // bs) + 1
+    table = rng.permutation(npg)[:-(-L // bs)].astype(np.int32)
+    k_cache = _bf16(rng.standard_normal((npg, bs, hkv, d)))
+    v_cache = _bf16(rng.standard_normal((npg, bs, hkv, d)))
+    q = _bf16(rng.standard_normal((ql, hq, d)))
+    a = oracle.prefill_varlen(q, k_cache, v_cache, table[None, :], [0, ql], [L], True, 0.25)
+    b = oracle.prefill(q, k_cache, v_cache, table, L - ql, True, 0.25)
+    assert np.array_equal(a, b)
