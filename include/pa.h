@@ -81,11 +81,15 @@ int pa_slot_mapping(const int32_t *positions, const int32_t *seq_idx,
 
 /*
  * pa_decode_input_prep -- the inputs of one decode step, computed on the device in one
- * launch for every KV-cache group [input-prep §4, §5]: num_seqs sequences decode one new
- * token each, at positions[s] (the number of tokens already in its cache).  Writes
- *   seq_lens[s]          = positions[s] + 1    (0 for a padding entry, positions[s] < 0)
+ * launch for every KV-cache group [input-prep §2, §4, §5]: num_seqs entries, each a
+ * sequence that decodes one new token at positions[s] (the number of tokens already in
+ * its cache) or a padding entry (positions[s] < 0).  Writes
+ *   seq_lens[s]          = positions[s] + 1    (0 for a padding entry)
  *   input_ids[s]         = sampled_ids[s]      (the token sampled by the previous step)
- *   query_start_loc[s]   = s, query_start_loc[num_seqs] = num_seqs
+ *   query_start_loc[0]   = 0, query_start_loc[s + 1] = query_start_loc[s] + (1 for a
+ *                          sequence, 0 for a padding entry): a padded entry owns no query
+ *                          row, so one request in padded buffers gives [0, 1, 1, ...]
+ *                          beside seq_lens [position + 1, 0, 0, ...] (§2)
  *   slot_mappings[g][s]  = block_tables[g][s * bt_strides[g] + p / block_sizes[g]]
  *                          * block_sizes[g] + p % block_sizes[g],   p = positions[s]
  * for each group g, with the checks of pa_slot_mapping (slot -1 for padding; -1 and

@@ -73,23 +73,50 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ positions,
                               bt_stride, max_blocks, block_size, err);
 }
 
-// Decode input preparation (input-prep post §4, §5): grid (sequence blocks, groups).  The
-// blocks of group 0 also write the step's shared metadata; every group writes its own
-// slots from its own block table and block size.
-__global__ void decode_input_prep_kernel(const __grid_constant__ PrepArgs a) {
+// Decode input preparation (input-prep post §2, §4, §5): grid (sequence blocks, groups)
+// of kPrepThreads threads.  The blocks of group 0 also write the step's shared metadata;
+// every group writes its own slots from its own block table and block size.  An entry
+// with a negative position is padding: seq_lens 0, slot -1, and no query row, so
+// query_start_loc is the running count of query rows ([0, 1, 1, ...] for one request in
+// padded buffers, as §2 gives it).  Block (0, 0) computes that count for all entries,
+// kPrepThreads at a time: a ballot per warp, then the warps' totals in shared memory.
+constexpr int kPrepThreads = 128;
+
+__global__ void __launch_bounds__(kPrepThreads) decode_input_prep_kernel(
+    const __grid_constant__ PrepArgs a) {
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     const int grp = blockIdx.y;
     pdl_wait();
     pdl_trigger();
+    if (grp == 0 && blockIdx.x == 0 && a.query_start_loc) {
+        __shared__ int warp_rows[kPrepThreads / 32];
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        if (threadIdx.x == 0) a.query_start_loc[0] = 0;
+        int carry = 0;  // query rows of the entries before this round
+        for (int base = 0; base < a.num_seqs; base += kPrepThreads) {
+            const int e = base + threadIdx.x;
+            const bool row = e < a.num_seqs && a.positions[e] >= 0;
+            const unsigned b = __ballot_sync(0xffffffffu, row);
+            if (lane == 0) warp_rows[w] = __popc(b);
+            __syncthreads();
+            int before = carry, round = 0;
+#pragma unroll
+            for (int i = 0; i < kPrepThreads / 32; ++i) {
+                before += i < w ? warp_rows[i] : 0;
+                round += warp_rows[i];
+            }
+            // rows of entries base .. e inclusive (lane mask up to and including this lane)
+            const unsigned upto = lane == 31 ? 0xffffffffu : (2u << lane) - 1u;
+            if (e < a.num_seqs) a.query_start_loc[e + 1] = before + __popc(b & upto);
+            __syncthreads();  // warp_rows is rewritten by the next round
+            carry += round;
+        }
+    }
     if (s >= a.num_seqs) return;
     const int32_t pos = a.positions[s];
     if (grp == 0) {
         if (a.input_ids) a.input_ids[s] = a.sampled_ids[s];
         if (a.seq_lens) a.seq_lens[s] = pos >= 0 ? pos + 1 : 0;
-        if (a.query_start_loc) {
-            a.query_start_loc[s] = s;
-            if (s == a.num_seqs - 1) a.query_start_loc[s + 1] = s + 1;
-        }
     }
     const PrepGroup &g = a.g[grp];
     g.slot_mapping[s] = slot_of(pos, s, g.block_table, a.num_seqs, g.bt_stride, g.max_blocks,
@@ -97,9 +124,8 @@ __global__ void decode_input_prep_kernel(const __grid_constant__ PrepArgs a) {
 }
 
 cudaError_t launch_decode_input_prep(const PrepArgs &a, cudaStream_t stream) {
-    const int threads = 128;
-    const dim3 grid((a.num_seqs + threads - 1) / threads, a.num_groups);
-    return launch_pdl(decode_input_prep_kernel, grid, dim3(threads), 0, stream, a);
+    const dim3 grid((a.num_seqs + kPrepThreads - 1) / kPrepThreads, a.num_groups);
+    return launch_pdl(decode_input_prep_kernel, grid, dim3(kPrepThreads), 0, stream, a);
 }
 
 cudaError_t launch_slot_mapping(const int32_t *positions, const int32_t *seq_idx,

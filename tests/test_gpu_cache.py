@@ -133,7 +133,8 @@ def _prep_case(S, block_sizes, seed, pad_every=0):
 
 
 @pytest.mark.parametrize("S,block_sizes", [(1, [832]), (1, [832, 16]), (16, [832, 784, 16]),
-                                           (300, [64, 832]), (5, [1, 7, 832, 784, 64, 16, 2, 3])])
+                                           (300, [64, 832]), (5, [1, 7, 832, 784, 64, 16, 2, 3]),
+                                           (1000, [16, 16])])
 def test_decode_input_prep_matches_oracle(cuda_lib, S, block_sizes):
     pa = cuda_lib
     pos, tables, sampled = _prep_case(S, block_sizes, 50 + S + len(block_sizes), pad_every=4)
@@ -144,6 +145,30 @@ def test_decode_input_prep_matches_oracle(cuda_lib, S, block_sizes):
     for k in ("seq_lens", "query_start_loc", "input_ids"):
         assert np.array_equal(got[k].cpu().numpy(), want[k]), k
     for g in range(len(block_sizes)):
+        assert np.array_equal(got["slot_mappings"][g].cpu().numpy(), want["slot_mappings"][g])
+    assert pa.device_errors() == 0
+
+
+def test_decode_input_prep_one_request_in_padded_buffers(cuda_lib):
+    # The input-prep post's step: one request at position 24576, two groups of block size
+    # 16, buffers for 128 requests.  query_start_loc = [0, 1, 1, ...], seq_lens =
+    # [24577, 0, 0, ...], bit for bit with the oracle.
+    pa = cuda_lib
+    pos = np.full(128, -1, np.int32)
+    pos[0] = 24576
+    cols = np.arange(1600)[None, :]
+    rows = np.arange(128)[:, None] * 10000
+    tables = [(3 * cols + 1 + rows).astype(np.int32), (2 * cols + 7 + rows).astype(np.int32)]
+    sampled = np.zeros(128, np.int32)
+    sampled[0] = 42
+    got = pa.decode_input_prep(torch.from_numpy(pos).cuda(),
+                               [torch.from_numpy(t).cuda() for t in tables], [16, 16],
+                               sampled_ids=torch.from_numpy(sampled).cuda())
+    want = oracle.decode_input_prep(pos, tables, [16, 16], sampled_ids=sampled)
+    assert got["query_start_loc"].tolist() == [0] + [1] * 128
+    for k in ("seq_lens", "query_start_loc", "input_ids"):
+        assert np.array_equal(got[k].cpu().numpy(), want[k]), k
+    for g in range(2):
         assert np.array_equal(got["slot_mappings"][g].cpu().numpy(), want["slot_mappings"][g])
     assert pa.device_errors() == 0
 
