@@ -1,6 +1,8 @@
 """Chunked causal prefill on the GPU vs the fp64 oracle: small shapes compared on every
-element (several query and key tiles, ragged tails, page sizes 784/832/64/16), and the
-q=4096 chunk over 4096 prior tokens at full size on sampled (row, head) outputs."""
+element (several query and key tiles, ragged tails, page sizes 784/832/64/16); the
+full-size chunks (q=4096 over 4096 prior tokens, the q=1685 tail over 12288, the q=4096
+first chunk, a mixed batch of four chunks) on every element, and quick variants of them
+on sampled (row, head) outputs."""
 import numpy as np
 import pytest
 import torch
@@ -206,4 +208,45 @@ def test_prefill_mixed_batch_full_size_sampled(cuda_lib):
                                   k_lens[b] - q_len, True, case.scale, rows, heads)
         got = out[torch.from_numpy(rows + cu[b]).long().cuda(), torch.from_numpy(heads).long().cuda()]
         assert_attention_close(got, ref, f"mixed batch, chunk {b} (sampled)")
+    assert pa.device_errors() == 0
+
+
+# ------------------------------------------------------------------ full size, every element
+def _full_chunk(pa, make):
+    case = getattr(workloads, make)("cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    return case, k_host, v_host
+
+
+@pytest.mark.parametrize("make", ["prefill_chunk", "prefill_tail", "prefill_first"])
+def test_prefill_full_chunk_every_element(cuda_lib, make):
+    # The full-size chunks in the launch the benchmark times (all items of the planned
+    # schedule: several items per CTA, items of up to 55 tiles, the ragged last q tile of
+    # the tail chunk), every output against the oracle.
+    pa = cuda_lib
+    case, k_host, v_host = _full_chunk(pa, make)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
+                           case.q_start, True, case.scale)
+    torch.cuda.synchronize()
+    ref = oracle.prefill(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                         case.q_start, True, case.scale)
+    e = assert_attention_close(out, ref, f"{make} (every element)")
+    print(f"{make}: {ref.size} outputs, max_abs={e['max_abs']:.3g} max_rel={e['max_rel']:.3g} "
+          f"rel_l2={e['rel_l2']:.3g}")
+    assert pa.device_errors() == 0
+
+
+def test_prefill_mixed_batch_full_size_every_element(cuda_lib):
+    pa = cuda_lib
+    case, k_host, v_host = _full_chunk(pa, "prefill_mixed")
+    cu, k_lens = case.meta["cu_seqlens_q"], case.meta["seq_lens"]
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            True, case.scale)
+    torch.cuda.synchronize()
+    ref = oracle.prefill_varlen(bits(case.q), k_host, v_host, case.block_table.cpu().numpy(),
+                                cu, k_lens, True, case.scale)
+    e = assert_attention_close(out, ref, "mixed batch (every element)")
+    print(f"mixed batch: {ref.size} outputs, max_abs={e['max_abs']:.3g} "
+          f"max_rel={e['max_rel']:.3g} rel_l2={e['rel_l2']:.3g}")
     assert pa.device_errors() == 0
