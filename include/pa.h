@@ -51,6 +51,8 @@ enum pa_status {
     PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad workspace */
     PA_ERR_UNSUPPORTED = 2,   /* valid but outside the shapes the kernels are built for */
     PA_ERR_CUDA = 3,          /* the CUDA runtime or driver reported an error */
+    PA_ERR_TIMEOUT = 4,       /* pa_get_device_errors: a bounded wait inside a kernel ran
+                                 out (PA_DEVERR_TIMEOUT is set in the error word) */
 };
 
 /* Bits of the device error word (pa_get_device_errors). */
@@ -210,6 +212,9 @@ int pa_decode_append(const pa_bf16 *q, pa_bf16 *k_cache, pa_bf16 *v_cache, int64
  *     is queued.  Other bad arguments return what pa_decode returns for them.
  *   - The first call on each device looks up the array's device address (with that
  *     device current) and keeps it; make that first call before any stream capture.
+ *     After cudaDeviceReset the device's next context loads the array afresh; the next
+ *     call sees the new context and looks the address up again (so, after a reset too,
+ *     make one call before capturing).
  *   - All calls on a device share the one array, and it keeps whatever the last call
  *     wrote.  Nothing in it needs to start at zero: every value a call reads from it was
  *     written earlier in the same call.  Calls whose work overlaps on the GPU (different
@@ -300,6 +305,13 @@ int pa_copy(void *dst, const void *src, size_t bytes, void *stream);
  * pa_get_device_errors -- waits for `stream`, then returns in *bits the device error
  * word of the current device (PA_DEVERR_* bits set by any call since the last clear)
  * and, if clear != 0, resets it to zero.
+ * Returns PA_ERR_TIMEOUT (with *bits filled in) when PA_DEVERR_TIMEOUT is set: a wait
+ * inside a kernel gave up after its limit (2 s), so some outputs of the calls since the
+ * last clear are incomplete.  The kernel that gave up let every copy it had started
+ * land, freed what it held and returned, so the context stays usable; a decode split
+ * that gave up contributes nothing to its outputs, a prefill CTA that gave up leaves its
+ * remaining rows unwritten.  PA_OK otherwise (PA_ERR_CUDA if the stream or the read
+ * failed).
  */
 int pa_get_device_errors(unsigned int *bits, int clear, void *stream);
 

@@ -36,6 +36,7 @@ __all__ = ["load", "build", "slot_mapping", "decode_input_prep", "reshape_and_ca
 LIB_PATH = _build.LIB
 DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_POSITION = 1, 2, 4, 8, 16
 DEVERR_LAYOUT = 32
+ERR_TIMEOUT = 4  # PA_ERR_TIMEOUT
 
 _lib = None
 _lock = threading.Lock()
@@ -376,9 +377,12 @@ def set_kernel_events(start, stop):
 
 
 def device_errors(clear: bool = True) -> int:
-    """Waits for the current stream and returns (and by default clears) the error bits."""
+    """Waits for the current stream and returns (and by default clears) the error bits.
+    A bounded wait that ran out shows as DEVERR_TIMEOUT among them (the C call then
+    returns PA_ERR_TIMEOUT, which is not raised here)."""
     lib = load()
     v = ctypes.c_uint(0)
-    _raise(lib.pa_get_device_errors(ctypes.byref(v), int(clear), _stream()),
-           "pa_get_device_errors")
+    rc = lib.pa_get_device_errors(ctypes.byref(v), int(clear), _stream())
+    if rc != ERR_TIMEOUT:
+        _raise(rc, "pa_get_device_errors")
     return int(v.value)

@@ -24,7 +24,7 @@ __device__ unsigned int g_pa_device_errors;
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
-    bool ready = false;
+    uintptr_t ctx = 0;  // the context these facts belong to (0: not looked up)
     int num_sms = 0;
     unsigned *err = nullptr;
 };
@@ -32,13 +32,15 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-// Per-device facts, looked up once with the device current.
+// Per-device facts, looked up with the device current, again whenever the device's
+// context has changed (the error word's address belongs to one context's module).
 int device_info(DeviceInfo *out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    const uintptr_t ctx = pa::current_context();  // 0 until the thread has a context
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo &d = g_dev[dev];
-    if (!d.ready) {
+    if (ctx == 0 || d.ctx != ctx) {
         int sms = 0;
         void *ptr = nullptr;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -46,7 +48,7 @@ int device_info(DeviceInfo *out) {
         if (cudaGetSymbolAddress(&ptr, g_pa_device_errors) != cudaSuccess) return PA_ERR_CUDA;
         d.num_sms = sms;
         d.err = static_cast<unsigned *>(ptr);
-        d.ready = true;
+        d.ctx = pa::current_context();  // the symbol lookup made the device's context current
     }
     *out = d;
     return PA_OK;
@@ -214,6 +216,7 @@ const char *pa_status_string(int status) {
         case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
         case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
         case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
         default: return "PA_ERR_UNKNOWN";
     }
 }
@@ -608,7 +611,16 @@ int pa_get_device_errors(unsigned int *bits, int clear, void *stream) {
         return PA_ERR_CUDA;
     if (clear && cudaMemset(dev.err, 0, sizeof v) != cudaSuccess) return PA_ERR_CUDA;
     *bits = v;
+    return (v & pa::kErrTimeout) ? PA_ERR_TIMEOUT : PA_OK;
+}
+
+#ifdef PA_TEST_HOOKS
+int pa_test_hook(int decode_skip_stage, int prefill_skip_unit) {
+    if (pa::set_decode_test_hook(decode_skip_stage) != cudaSuccess ||
+        pa::set_prefill_test_hook(prefill_skip_unit) != cudaSuccess)
+        return PA_ERR_CUDA;
     return PA_OK;
 }
+#endif
 
 }  // extern "C"

@@ -8,6 +8,7 @@
 #include "pa_internal.h"
 
 #include <atomic>
+#include <mutex>
 
 namespace pa {
 
@@ -30,16 +31,40 @@ cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t s
                       n16);
 }
 
+// The calling thread's current CUDA context, through the driver entry point the runtime
+// hands out (the library does not link libcuda).  0 when there is none or on failure.
+uintptr_t current_context() {
+    typedef CUresult (*GetCurrentFn)(CUcontext *);
+    static GetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCurrentFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return 0;
+    return reinterpret_cast<uintptr_t>(c);
+}
+
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
-    static std::atomic<unsigned long long> done[4];  // bit d: device d already set
+    // Per (kernel slot, device): the context in which the limit was last raised.  A new
+    // context for the device (after cudaDeviceReset the module is loaded afresh and the
+    // attribute is gone) raises it again.
+    constexpr int kDevices = 64;
+    static std::atomic<uintptr_t> done[4][kDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 64) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    const unsigned long long bit = 1ull << dev;
-    if (done[slot].load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const uintptr_t ctx = current_context();
+    if (dev >= kDevices || ctx == 0)
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (done[slot][dev].load(std::memory_order_acquire) == ctx) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done[slot].fetch_or(bit, std::memory_order_release);
+    if (e == cudaSuccess) done[slot][dev].store(ctx, std::memory_order_release);
     return e;
 }
 

@@ -56,7 +56,7 @@ template <int kC, int kS>
 constexpr int dec_smem_bytes() {
     static_assert(kC * kDecMaxGroup * (kDecMergeRow + 2) * 4 <= kS * kDecStageBytes,
                   "merge buffers reuse the ring");
-    return 1024 + kS * kDecStageBytes + (2 * kS + 1) * 8;
+    return 1024 + kS * kDecStageBytes + (2 * kS + 1) * 8 + 8;  // + the abort flag
 }
 
 constexpr int kCombineThreads = 256;
@@ -168,6 +168,13 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+#ifdef PA_TEST_HOOKS
+// Test build only: the ring stage whose loads the producer leaves out (-1: none), so
+// that the consumer waiting for it runs into its bounded wait.  Set by
+// set_decode_test_hook through pa_test_hook.
+__device__ int g_test_skip_stage = -1;
+#endif
+
 template <int kDecConsumers, int kDecStages>
 __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     decode_split_kernel(const __grid_constant__ DecMaps maps, const DecodeKParams p) {
@@ -179,6 +186,8 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecRingBytes);
     uint64_t *empty = full + kDecStages;
     uint64_t *written = empty + kDecStages;  // the fused write of the newest token is done
+    // Raised by the first bounded wait that runs out; the others then give up at once.
+    volatile int *abort = reinterpret_cast<volatile int *>(written + 1);
 
     const int split = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,6 +199,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
             mbar_init(&empty[s], kDecPair);  // released by the warps of both tiles
         }
         mbar_init(written, 1);
+        *abort = 0;
         fence_mbar_init();
     }
     if (warp == kDecConsumers && lane == 0) {
@@ -242,6 +252,13 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     if (warp == kDecConsumers) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+#ifdef PA_TEST_HOOKS
+            const int skip_stage = *reinterpret_cast<volatile int *>(&g_test_skip_stage);
+#endif
+            // Ring slots that received a load (bit s) and the phase parity of the last
+            // load issued into each: every one of them lands before the CTA reuses or
+            // leaves its shared memory (below), also when a wait gave up.
+            uint32_t issued = spec ? 1u : 0u, par = 0;
             // A page outside the pool is reported; the TMA boxes then lie outside the
             // tensor and read as zeros, so nothing faults.
             if (page0 < 0 || page0 >= p.num_pages) atomicOr(p.err, kErrPage);
@@ -254,9 +271,12 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                 // The split's only stage holds the token being decoded and was loaded
                 // before that token was written: load it again once the first load has
                 // landed and the write is done.  Its consumers wait for both loads.
-                if (mbar_wait(&full[0], 0, p.err) && mbar_wait(written, 0, p.err))
+                if (mbar_wait_abort(&full[0], 0, p.err, abort) &&
+                    mbar_wait_abort(written, 0, p.err, abort)) {
                     load_stage(maps, smem, &full[0], g, off0, page0, off0 + kDecTile,
                                page0);
+                    par |= 1u;
+                }
             }
             for (int m = spec ? 1 : 0; m < nst; ++m) {
                 const int s = m % kDecStages;
@@ -275,10 +295,16 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                     if (lp < lp_last) page_next = bt[lp + 1];
                 }
                 if (m >= kDecStages &&
-                    !mbar_wait(&empty[s], ((m / kDecStages) - 1) & 1, p.err))
+                    !mbar_wait_abort(&empty[s], ((m / kDecStages) - 1) & 1, p.err, abort))
                     break;
                 // The last stage holds the token being decoded: wait until it is written.
-                if (writes_newest && m == nst - 1 && !mbar_wait(written, 0, p.err)) break;
+                if (writes_newest && m == nst - 1 && !mbar_wait_abort(written, 0, p.err, abort))
+                    break;
+#ifdef PA_TEST_HOOKS
+                if (m == skip_stage) continue;  // its consumer's wait runs out
+#endif
+                issued |= 1u << s;
+                par = (par & ~(1u << s)) | ((uint32_t)((m / kDecStages) & 1) << s);
                 uint8_t *st = smem + s * kDecStageBytes;
                 if (tip + 1 < tpp) {
                     load_stage(maps, st, &full[s], g, tip * kDecTile, page,
@@ -293,7 +319,13 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                                second ? page_next : -1);
                 }
             }
+            // Loads always complete, so this wait ends; in a normal run every stage was
+            // consumed and it returns at once.
+            for (int s = 0; s < kDecStages; ++s)
+                if ((issued >> s) & 1u) mbar_wait(&full[s], (par >> s) & 1u, p.err);
         }
+        __syncwarp();
+        named_bar_sync(1, (kDecConsumers + 1) * 32);  // meets the consumers before the merge
         return;
     }
 
@@ -437,9 +469,11 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
         for (int i = warp; i < n; i += kDecConsumers) {
             const int m = i / kDecPair, h = i - m * kDecPair;
             const int s = m % kDecStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (m / kDecStages) & 1, p.err)))
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_abort(&full[s], (m / kDecStages) & 1, p.err, abort)))
                 break;
-            if (refetch && !__all_sync(0xffffffffu, mbar_wait(&full[0], 1, p.err))) break;
+            if (refetch && !__all_sync(0xffffffffu, mbar_wait_abort(&full[0], 1, p.err, abort)))
+                break;
             tile(s, h, i);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
@@ -447,7 +481,8 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     } else {
         for (int m = warp; m < nst; m += kDecConsumers) {
             const int s = m % kDecStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (m / kDecStages) & 1, p.err)))
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_abort(&full[s], (m / kDecStages) & 1, p.err, abort)))
                 break;
             for (int h = 0; h < kDecPair && m * kDecPair + h < n; ++h) tile(s, h, m * kDecPair + h);
             __syncwarp();
@@ -462,7 +497,16 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     }
 
     // ---------------------------------------------------------------- CTA merge
-    named_bar_sync(1, kDecConsumers * 32);  // every tile consumed: the ring is free
+    // Every tile consumed and (the producer joins here after its last load landed) no
+    // load in flight: the ring is free.  If a wait gave up (PA_DEVERR_TIMEOUT is set),
+    // the split contributes nothing: an empty partial, which the combine skips.
+    named_bar_sync(1, (kDecConsumers + 1) * 32);
+    if (*abort) {
+        if (threadIdx.x < p.group)
+            p.part_ml[((int64_t)seq * p.num_q_heads + g * p.group + threadIdx.x) * p.num_splits +
+                      split] = make_float2(-CUDART_INF_F, 0.f);
+        return;
+    }
     float *red_o = reinterpret_cast<float *>(smem);                     // [warp][head][row]
     float *red_m = red_o + kDecConsumers * kDecMaxGroup * kDecMergeRow;  // [warp][head]
     float *red_l = red_m + kDecConsumers * kDecMaxGroup;
@@ -484,7 +528,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
             w1[d + 8] = o[mt][3];
         }
     }
-    named_bar_sync(1, kDecConsumers * 32);
+    named_bar_sync(2, kDecConsumers * 32);
     // Thread t merges the quads (4 consecutive dims of one head) t, t + 32C, ...  Every
     // thread derives its head's CTA max and the warps' weights exp2(m_w - M) itself, so
     // no further barrier is needed and all loads of a quad are independent.
@@ -612,6 +656,12 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
 }
 
 }  // namespace
+
+#ifdef PA_TEST_HOOKS
+cudaError_t set_decode_test_hook(int skip_stage) {
+    return cudaMemcpyToSymbol(g_test_skip_stage, &skip_stage, sizeof skip_stage);
+}
+#endif
 
 DecodePlan plan_decode(int num_seqs, int num_kv_heads, int block_size, int max_seq_len,
                        int num_sms) {

@@ -18,8 +18,13 @@ constexpr int kChunks = kHeadDim / kChunkElems;
 constexpr unsigned kErrPage = 1u, kErrSeqLen = 2u, kErrSlot = 4u, kErrTimeout = 8u,
                    kErrPosition = 16u, kErrLayout = 32u;
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// A bounded wait gives up after this many nanoseconds of %globaltimer: 2 s in the
+// library.  The test build (PA_TEST_HOOKS) sets a short limit so that its failure-path
+// tests, which make one wait run out on purpose, finish quickly.
+#ifndef PA_WAIT_LIMIT_NS
+#define PA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kWaitLimitNs = PA_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -90,6 +95,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
             if (mbar_try_wait(bar, parity)) return true;
         if (global_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that also gives up at once when another role of the CTA has given up
+// (*abort != 0).  A wait that runs out sets kErrTimeout and raises *abort.
+__device__ __forceinline__ bool mbar_wait_abort(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            *abort = 1;
             return false;
         }
     }

@@ -9,8 +9,13 @@
 
 namespace pa {
 
-// Raises a kernel's dynamic shared-memory limit once per (kernel slot, device), so that
-// later launches (possibly under stream capture) make no attribute call.
+// The calling thread's current CUDA context as a number (0 if none).  Host-side caches
+// of per-device facts (symbol addresses, function attributes) are keyed on it: after
+// cudaDeviceReset the device gets a new primary context with the module loaded afresh.
+uintptr_t current_context();
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel slot, device context),
+// so that later launches (possibly under stream capture) make no attribute call.
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot);
 
 // Launches a kernel with programmatic dependent launch allowed: it may start while the
@@ -210,5 +215,16 @@ struct PrefillArgs {
 
 // tmaps: Q, K, V, then the K and V maps cut at each sequence's last token (2 per sequence).
 cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream);
+
+#ifdef PA_TEST_HOOKS
+// Test build only (libpa_test.so, compiled with -DPA_TEST_HOOKS and a short wait limit):
+// the decode producer leaves out the loads of ring stage `skip_stage` of every CTA, the
+// prefill producer those of ring unit `skip_unit` (-1: none), so that a consumer's
+// bounded wait runs out.  Exported to the failure-path tests as
+//     extern "C" int pa_test_hook(int decode_skip_stage, int prefill_skip_unit);
+// The product library has neither the hooks nor this entry point.
+cudaError_t set_decode_test_hook(int skip_stage);
+cudaError_t set_prefill_test_hook(int skip_unit);
+#endif
 
 }  // namespace pa

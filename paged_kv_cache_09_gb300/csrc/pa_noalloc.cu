@@ -12,7 +12,8 @@
 // Host code cannot use the array's name as a device address: on the host that name is
 // only a stand-in.  So, once per device and with that device current, the first call
 // looks up the real device address with cudaGetSymbolAddress, checks the result, and
-// keeps it.  Every later call on that device reuses the stored address.
+// keeps it with the context it belongs to.  Later calls on that device reuse it while the
+// device's context stays the same, and look it up again after a cudaDeviceReset.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,21 +28,30 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PA_DECODE_NOALLO
 
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxScratchDevices];
+struct ScratchAddr {
+    uintptr_t ctx;  // the context whose module the address belongs to (0: none yet)
+    void *ptr;
+};
+ScratchAddr g_scratch[kMaxScratchDevices];
 
-// Device address of this device's scratch array; looked up on the first call.
+// Device address of this device's scratch array.  It is looked up with the device
+// current on the first call, and again whenever the device's context has changed (after
+// cudaDeviceReset the module, and with it the array, is loaded afresh).
 int scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices)
         return PA_ERR_CUDA;
+    const uintptr_t ctx = pa::current_context();  // 0 until the thread has a context
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchAddr &a = g_scratch[dev];
+    if (ctx == 0 || a.ctx != ctx || !a.ptr) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr)
             return PA_ERR_CUDA;
-        g_scratch_ptr[dev] = ptr;
+        a.ptr = ptr;
+        a.ctx = pa::current_context();  // the lookup made the device's context current
     }
-    *out = g_scratch_ptr[dev];
+    *out = a.ptr;
     return PA_OK;
 }
 

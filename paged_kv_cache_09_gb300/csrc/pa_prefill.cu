@@ -165,22 +165,12 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs> &p, int k, Item &i
     return true;
 }
 
-// Bounded wait that also gives up at once when another role of the CTA has given up.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, unsigned *err,
-                                              volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            atomicOr(err, kErrTimeout);
-            *abort = 1;
-            return false;
-        }
-    }
-}
+#ifdef PA_TEST_HOOKS
+// Test build only: the K/V ring unit (counted over the CTA's whole run) whose loads the
+// producer leaves out (-1: none), so that the MMA thread's wait for it runs out.  Set by
+// set_prefill_test_hook through pa_test_hook.
+__device__ int g_test_skip_unit = -1;
+#endif
 
 template <int kSeqs>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -241,11 +231,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+#ifdef PA_TEST_HOOKS
+            const int skip_unit = *reinterpret_cast<volatile int *>(&g_test_skip_unit);
+#endif
             uint32_t u = 0;
+            // Ring slots that received a load (bit s), the phase parity of the last load
+            // issued into each, and the Q loads issued: all of them land before the CTA
+            // leaves, also when a wait gave up.
+            uint32_t issued = 0, par = 0;
+            int q_loads = 0;
             Item it;
             bool stop = false;
             for (int k = 0; !stop && item_of(p, k, it); ++k) {
-                if (k > 0 && !wait_or_abort(&bars[kQEmpty], (k - 1) & 1, p.err, abort)) break;
+                if (k > 0 && !mbar_wait_abort(&bars[kQEmpty], (k - 1) & 1, p.err, abort)) break;
+                ++q_loads;
                 mbar_arrive_expect_tx(&bars[kQFull], kQBytes);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
@@ -286,11 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < 8; ++x, ++u) {
                         const int s = u % kRing;
                         if (u >= kRing &&
-                            !wait_or_abort(&bars[kRingEmpty + s], ((u / kRing) - 1) & 1, p.err,
+                            !mbar_wait_abort(&bars[kRingEmpty + s], ((u / kRing) - 1) & 1, p.err,
                                            abort)) {
                             stop = true;
                             break;
                         }
+#ifdef PA_TEST_HOOKS
+                        if ((int)u == skip_unit) continue;  // the MMA thread's wait runs out
+#endif
+                        issued |= 1u << s;
+                        par = (par & ~(1u << s)) | (((u / kRing) & 1u) << s);
                         uint8_t *dst = ring + s * kUnit;
                         mbar_arrive_expect_tx(&bars[kRingFull + s], kUnit);
                         if (x < 4) {
@@ -308,6 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // Loads always complete, so these waits end; in a normal run every unit and Q
+            // tile was consumed and they return at once.
+            for (int s = 0; s < kRing; ++s)
+                if ((issued >> s) & 1u) mbar_wait(&bars[kRingFull + s], (par >> s) & 1u, p.err);
+            if (q_loads > 0) mbar_wait(&bars[kQFull], (q_loads - 1) & 1, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -320,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             Item it;
             bool stop = false;
             for (int k = 0; !stop && item_of(p, k, it); ++k) {
-                if (!wait_or_abort(&bars[kQFull], k & 1, p.err, abort)) break;
+                if (!mbar_wait_abort(&bars[kQFull], k & 1, p.err, abort)) break;
                 tc_fence_after();
                 for (int j = 0; j < it.n && !stop; ++j) {
                     // S = Q K^T over the tile's 256 keys.
                     for (int c = 0; c < kChunks; ++c, ++u) {
                         const int s = u % kRing;
-                        if (!wait_or_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
+                        if (!mbar_wait_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
@@ -348,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // between one quarter's MMAs and the next.
                     for (int qq = 0; qq < 4; ++qq, ++u) {
                         const int s = u % kRing;
-                        if (!wait_or_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
+                        if (!mbar_wait_abort(&bars[kRingFull + s], (u / kRing) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
                         if (j == 0 && qq == 0 && k > 0 &&
-                            !wait_or_abort(&bars[kOEmpty], (k - 1) & 1, p.err, abort)) {
+                            !mbar_wait_abort(&bars[kOEmpty], (k - 1) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
@@ -361,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int ks = 0; ks < kBlk / 16; ++ks)
                             vd[ks] = umma_sdesc_sw128(ring_addr + s * kUnit + ks * 2048, kBlkBytes);
-                        if (!wait_or_abort(&bars[kPFull + qq], (jt + j) & 1, p.err, abort)) {
+                        if (!mbar_wait_abort(&bars[kPFull + qq], (jt + j) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
@@ -411,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pair);
-            ok = wait_or_abort(pair, ph, p.err, abort);
+            ok = mbar_wait_abort(pair, ph, p.err, abort);
             tc_fence_after();
             ++pc;
             return xq[ph * 64 + (hf ^ 1) * 32 + lane];
@@ -427,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int blk_tok0 = 0, blk_in = 0;
             for (int j = 0; j < it.n && !stop; ++j) {
                 if (!__all_sync(0xffffffffu,
-                                wait_or_abort(&bars[kSFull], (jt + j) & 1, p.err, abort))) {
+                                mbar_wait_abort(&bars[kSFull], (jt + j) & 1, p.err, abort))) {
                     stop = true;
                     break;
                 }
@@ -513,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // means every tensor op issued before QK_j has completed.  Either way
                     // the parity wait is never two phases behind its barrier.
                     if ((j > 0 || qq > 0) && __any_sync(0xffffffffu, need)) {
-                        ok = qq == 0 || wait_or_abort(&bars[kPvDone + qq - 1], (jt + j) & 1,
+                        ok = qq == 0 || mbar_wait_abort(&bars[kPvDone + qq - 1], (jt + j) & 1,
                                                       p.err, abort);
                         if (!__all_sync(0xffffffffu, ok)) {
                             stop = true;
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             const float lt = l + exchange(l, ok);
             if (!__all_sync(0xffffffffu, ok &&
-                                             wait_or_abort(&bars[kPvDone + 3], (jt + it.n - 1) & 1,
+                                             mbar_wait_abort(&bars[kPvDone + 3], (jt + it.n - 1) & 1,
                                                            p.err, abort)))
                 break;
             tc_fence_after();
@@ -587,6 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+#ifdef PA_TEST_HOOKS
+cudaError_t set_prefill_test_hook(int skip_unit) {
+    return cudaMemcpyToSymbol(g_test_skip_unit, &skip_unit, sizeof skip_unit);
+}
+#endif
 
 namespace {
 

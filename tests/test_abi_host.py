@@ -56,7 +56,19 @@ def test_status_strings_and_build_info(lib):
     assert lib.pa_status_string(1) == b"PA_ERR_INVALID_ARG"
     assert lib.pa_status_string(2) == b"PA_ERR_UNSUPPORTED"
     assert lib.pa_status_string(3) == b"PA_ERR_CUDA"
+    assert lib.pa_status_string(4) == b"PA_ERR_TIMEOUT"
     assert b"sm_103a" in lib.pa_build_info()
+
+
+def test_test_hooks_live_only_in_the_test_library(lib):
+    # The product library has no failure-injection entry point; the failure-path test
+    # library (same sources, PA_TEST_HOOKS) has it beside every declared symbol.
+    from paged_kv_cache_09_gb300 import _build
+    assert not hasattr(lib, "pa_test_hook")
+    test_lib = ctypes.CDLL(_build.build_test())
+    assert hasattr(test_lib, "pa_test_hook")
+    for n in _declared():
+        assert hasattr(test_lib, n), n
 
 
 FAKE = 0x10000  # an aligned, non-null address that is never dereferenced on the host
