@@ -2,37 +2,40 @@
 """Benchmark of the paged-KV GQA attention hot path on GB300.
 
 Metric: paged decode KV GB/s (and % of HBM peak) at 4K-32K context; q=4096 prefill
-TFLOP/s.  One JSON line on stdout (rank 0).
+TFLOP/s.  One JSON line on stdout (rank 0); its last key, "summary", repeats every leg's
+headline figure in a few hundred bytes.
 
-Headline workload (the `value`): decode, batch 1, context 8192 (the new token at
-position 8191 included), 24 query / 4 KV heads, head_dim 256, BF16 N(0,1), block_size
-832, over a shuffled 64-page pool.  One step = one serving-style pass of the hot path
-through pa_decode_append: the new token's slot (derived in the kernel by the
-slot-mapping formula), its KV write, the split-context decode (one launch) and the LSE
-combine (a second launch).  KV GB/s = 4096 bytes per context token / step time (K+V of
-4 KV heads x 256 dims x 2 bytes).
+Headline workload (the `value`): decode, batch 1, context 32768, 24 query / 4 KV heads,
+head_dim 256, BF16 N(0,1) with 5% of K rows scaled x8, block_size 832, pages drawn at
+random from a 1 GiB K+V pool (315 pages).  One step = pa_decode of one sequence: the
+split-context kernel (one launch) and the LSE combine (a second launch).  KV GB/s =
+4096 bytes per context token (K+V of 4 KV heads x 256 dims x 2 bytes) / step time.
 
 Timing of the decode legs: K consecutive steps are captured in ONE CUDA graph and
 replayed once between two CUDA events (a serving loop captures a whole model step, so a
 graph launch is not paid per attention call); ms per step = elapsed / K.  The steps
-cycle over copies of the workload whose K/V are disjoint and together several times the
-129 MB L2 (16 copies of the 8K case; for the sweep, all the sequences a 1 GiB pool
-holds), so no step finds its K/V in L2.  The split kernel's own time: CUDA events the
-library records around its launch, in eager steps each after an L2 flush (event record
-nodes inside the graph measured it ~2 us longer).  The same step as a single-step graph
-replayed after an L2 flush is reported too (config.step_alone_ms): it carries the
-graph's own launch, ~5 us here.
+cycle over sequences whose K/V are disjoint and together several times the 129 MB L2
+(for 32K, the 7 sequences a 1 GiB pool holds: 939 MB), so no step finds its K/V in L2.
+The split kernel's own time: CUDA events the library records around its launch, in
+eager steps each after an L2 flush.  The same step as a single-step graph replayed
+after an L2 flush is reported too (config.step_alone_ms): it carries the graph's own
+launch, ~5 us here.  The end-to-end figure (e2e) is the same stream of steps through
+the public API with the step's inputs copied in from pinned host memory and its output
+written to pinned host memory; it is timed between two timings of the device-resident
+stream (A/B/A), all in this run.
 
-Other legs, reported under "legs": the 4K/8K/16K/32K sweep (1 GiB pool, 5% of K rows
-x8), 32K in generic 16- and 64-token pages, block_size 784 at 8K, batched decode (16
-sequences, 4K-32K, appended token), the q=4096 prefill chunk over 4096 prior tokens
-(chunk KV write + prefill; TFLOP/s counts the causal work 4*D*Hq*sum_i(4096+i+1) =
-6.185e11), and two more chunk shapes of the same prompt: the q=1685 tail chunk over 12288 prior tokens and the q=4096 first chunk
-(no prior tokens); a mixed batch of four sequences' chunks in one varlen call; and the
-decode input preparation of a two-group model.  The prefill and input-preparation legs
-replay a single-step graph after an L2 flush per step (a 512 MiB read outside the
-events), with CUDA events around each step and around the prefill kernel.
---impl reference times the fp64 CPU oracle on the same workload instead.
+Other legs, reported under "legs": the 4K/8K/16K/32K sweep (same pool), 32K in generic
+16- and 64-token pages, the serving step at 8K (new token appended: slot derived in the
+kernel, KV write, decode; 16 copies of a 64-page pool) with its own e2e, block_size 784
+at 8K, batched decode (16 sequences, 4K-32K, appended token), the q=4096 prefill chunk
+over 4096 prior tokens (chunk KV write + prefill; TFLOP/s counts the causal work
+4*D*Hq*sum_i(4096+i+1) = 6.185e11), the q=1685 tail chunk over 12288 prior tokens and
+the q=4096 first chunk (no prior tokens), a mixed batch of four sequences' chunks in one
+varlen call, and the decode input preparation of a two-group model.  The prefill and
+input-preparation legs replay a single-step graph after an L2 flush per step (a 512 MiB
+read outside the events), with CUDA events around each step and around the prefill
+kernel.  cpu_baseline: the fp64 oracle on the headline workload, on all host cores and
+on one.  --impl reference times that oracle on the headline workload instead.
 """
 from __future__ import annotations
 
@@ -55,15 +58,17 @@ if ROOT not in sys.path:
 
 import workloads  # noqa: E402
 
-HEADLINE = ("decode batch 1, context 8192 (new token at 8191 written by slot mapping), "
-            "24 q / 4 kv heads, d=256, BF16 N(0,1), block_size 832, shuffled 64-page pool")
+HEADLINE_CTX = 32768
+HEADLINE = ("decode batch 1, context 32768, 24 q / 4 kv heads, d=256, BF16 N(0,1) with 5% of "
+            "K rows x8, block_size 832, pages drawn at random from a 1 GiB K+V pool")
 KV_BYTES_PER_TOKEN = 2 * workloads.HKV * workloads.HEAD_DIM * 2   # K+V, all KV heads
 L2_FLUSH_BYTES = 512 << 20
-# DRAM bytes (read + write) of one 8K split launch in an ncu capture of the current split
-# kernel (summarised under profiles/); None whenever the kernel changes after a capture.
-SPLIT_8K_DRAM_BYTES = 33_627_392 + 0
+# DRAM bytes (read + write) of one split launch of the headline (32K) step in an ncu
+# capture of the current split kernel (summarised under profiles/); None whenever the
+# kernel changes after a capture.
+SPLIT_32K_DRAM_BYTES = None
 # The same for one prefill launch of the q=4096 chunk over 4096 prior tokens.
-PREFILL_Q4096_DRAM_BYTES = 86_102_528 + 17_982_976
+PREFILL_Q4096_DRAM_BYTES = None
 
 
 def parse():
@@ -73,11 +78,13 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all",
-                    help="comma list: sweep,small_pages,bs784,batched,prefill,prefill_tail,"
-                         "prefill_first,prefill_mixed,prep or all/none; l2check (not in all) runs the "
-                         "stream of 8K steps that an ncu capture of DRAM bytes checks")
+                    help="comma list: sweep,small_pages,step8k,bs784,batched,prefill,"
+                         "prefill_tail,prefill_first,prefill_mixed,prep or all/none; l2check "
+                         "(not in all) runs the stream of 8K steps that an ncu capture of "
+                         "DRAM bytes checks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="host seconds of oracle work per cpu_baseline timing (two timings)")
     ap.add_argument("--contexts", default="4096,8192,16384,32768",
                     help="contexts of the sweep leg")
     ap.add_argument("--skip-headline", action="store_true",
@@ -439,41 +446,74 @@ def input_prep_leg(pa, steps, warmup, flush):
     return r
 
 
-def e2e_leg(pa, cases, steps, warmup, flush):
-    """The headline step through the public API with pinned host buffers, timed as a
-    stream of steps like the headline: per step, one H2D copy of that step's inputs (q,
-    the new token's K/V, block table and seq_lens of its replica, packed in one pinned
-    staging buffer, by a pa_copy kernel: a copy-engine node costs several microseconds
-    more on this system), then the append decode (slot, KV write, split decode,
-    combine), whose combine writes the output straight into a pinned host buffer (the
-    step's D2H transfer); the steps cycle the replicas inside one CUDA graph."""
+def _staged_inputs(srcs):
+    """Pinned host staging buffer and its device twin holding the tensors of `srcs`
+    (name -> tensor) in 256-byte aligned slices; returns (host, device, device views)."""
+    offs, total = {}, 0
+    for k, t in srcs.items():
+        offs[k] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total, dtype=torch.uint8, device="cuda")
+
+    def view(buf, k):
+        t = srcs[k]
+        nb = t.numel() * t.element_size()
+        return buf[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
+    for k, t in srcs.items():  # the host fills the step's inputs into the staging buffer
+        view(stage_h, k).copy_(t.cpu())
+    return stage_h, stage_d, {k: view(stage_d, k) for k in srcs}
+
+
+def e2e_decode_fns(pa, case, max_seq_len):
+    """Steps of the headline stream through the public API with host buffers: per step
+    (sequence s of the rotation), one H2D copy of the step's inputs (q, block-table row
+    and sequence length, packed in one pinned staging buffer, by a pa_copy kernel: a
+    copy-engine node costs several microseconds more on this system), then pa_decode,
+    whose combine writes the output straight into a pinned host buffer (the step's D2H
+    transfer).  Returns (fns, outputs to check, H2D bytes, D2H bytes) per step."""
+    fns, outs = [], []
+    h2d = d2h = 0
+    for s in range(case.q.shape[0]):
+        srcs = {"q": case.q[s:s + 1].contiguous(),
+                "block_table": case.block_table[s:s + 1].contiguous(),
+                "seq_lens": case.seq_lens[s:s + 1].contiguous()}
+        stage_h, stage_d, dev = _staged_inputs(srcs)
+        out_h = torch.empty(srcs["q"].shape, dtype=torch.bfloat16).pin_memory()
+        ws = torch.empty(max(256, pa.decode_workspace_size(1, case.q.shape[1],
+                                                            case.k_cache.shape[2],
+                                                            case.q.shape[2], case.block_size,
+                                                            max_seq_len)),
+                         dtype=torch.uint8, device="cuda")
+        h2d, d2h = stage_h.numel(), out_h.numel() * out_h.element_size()
+
+        def step(stage_h=stage_h, stage_d=stage_d, dev=dev, out_h=out_h, ws=ws):
+            pa.copy(stage_d, stage_h)
+            pa.decode(dev["q"], case.k_cache, case.v_cache, dev["block_table"],
+                      dev["seq_lens"], case.scale, max_seq_len, out=out_h, workspace=ws)
+        fns.append(step)
+        outs.append((out_h, s))
+    return fns, outs, h2d, d2h
+
+
+def e2e_append_fns(pa, cases):
+    """The 8K serving step through the public API with host buffers: per step one H2D
+    copy of q, the new token's K/V, the block table and seq_lens of its replica (one
+    pa_copy kernel from a pinned staging buffer), then pa_decode_append, whose combine
+    writes the output into a pinned host buffer."""
     names = ("q", "new_k", "new_v", "block_table", "seq_lens")
     fns, outs = [], []
     h2d = d2h = 0
     for case in cases:
         S, hq, d = case.q.shape
         msl = int(case.seq_lens.max())
-        srcs = {k: getattr(case, k).contiguous() for k in names}
-        offs, total = {}, 0
-        for k in names:  # 256-byte aligned slices of one staging buffer
-            offs[k] = total
-            total += (srcs[k].numel() * srcs[k].element_size() + 255) // 256 * 256
-        stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
-        stage_d = torch.empty(total, dtype=torch.uint8, device="cuda")
-
-        def view(buf, k, srcs=srcs, offs=offs):
-            t = srcs[k]
-            nb = t.numel() * t.element_size()
-            return buf[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
-        for k in names:  # the host fills the step's inputs into the staging buffer
-            view(stage_h, k).copy_(srcs[k].cpu())
-        dev = {k: view(stage_d, k) for k in names}
+        stage_h, stage_d, dev = _staged_inputs({k: getattr(case, k).contiguous() for k in names})
         out_h = torch.empty((S, hq, d), dtype=torch.bfloat16).pin_memory()
         ws = torch.empty(max(256, pa.decode_workspace_size(S, hq, case.k_cache.shape[2], d,
                                                             case.block_size, msl)),
                          dtype=torch.uint8, device="cuda")
         slots = torch.empty(S, dtype=torch.int64, device="cuda")
-        h2d, d2h = total, out_h.numel() * out_h.element_size()
+        h2d, d2h = stage_h.numel(), out_h.numel() * out_h.element_size()
 
         def step(case=case, stage_h=stage_h, stage_d=stage_d, dev=dev, out_h=out_h, ws=ws,
                  slots=slots, msl=msl):
@@ -483,99 +523,151 @@ def e2e_leg(pa, cases, steps, warmup, flush):
                              out=out_h, workspace=ws, slot_mapping=slots)
         fns.append(step)
         outs.append((out_h, case, msl))
-    ms = time_stream(fns, steps, warmup, flush)
+    return fns, outs, h2d, d2h
+
+
+def step8k_leg(pa, steps, warmup, flush, peaks):
+    """The serving step at 8K: each step appends its sequence's newest token (slot derived
+    in the kernel, KV write) and decodes over 8192 keys; 16 copies of the workload in
+    turn.  Its end-to-end form (host buffers) is timed between two device timings."""
+    reps = headline_replicas("cuda")
+    fns = [append_step_fn(pa, c, 8192)[0] for c in reps]
+    r = decode_leg(pa, fns, 8192, 1, steps, warmup, flush, peaks,
+                   f"{len(reps)} copies of the workload, each its own 64-page pool, in turn")
+    r["step_alone_ms"] = statistics.mean(time_steps(graph_of(fns[0]).replay, steps, warmup,
+                                                    flush))
+    efns, outs, h2d, d2h = e2e_append_fns(pa, reps)
+    e2e_ms = time_stream(efns, steps, warmup, flush)
+    again_ms = time_stream(fns, steps, warmup, flush)
     torch.cuda.synchronize()
-    # Each step's host output equals the same decode written to device memory.
     for out_h, case, msl in outs[:min(len(outs), steps)]:
         ref = pa.decode(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
                         case.scale, msl)
         assert torch.equal(out_h, ref.cpu()), "a step's host output differs from the decode's"
-    return ms, h2d, d2h
+    r["e2e"] = {"ms_per_step": e2e_ms, "kv_gbs": 8192 * KV_BYTES_PER_TOKEN / (e2e_ms * 1e-3) / 1e9,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "device_ms_per_step_before_after": [r["ms_per_step"], again_ms]}
+    del reps, fns, efns, outs
+    torch.cuda.empty_cache()
+    return r
 
 
 # ------------------------------------------------------------------------ CPU oracle
-def oracle_step_fn(case_host):
+def host_decode_case(case, s, kv=None):
+    """Sequence s of a decode case as host arrays for the oracle (raw BF16 bits); kv: the
+    caches' bits if already copied to the host."""
+    from workloads import bits
+    k, v = kv if kv is not None else (bits(case.k_cache), bits(case.v_cache))
+    return dict(q=bits(case.q[s:s + 1]), k=k, v=v,
+                block_table=case.block_table[s:s + 1].cpu().numpy(),
+                seq_lens=case.seq_lens[s:s + 1].cpu().numpy(), scale=case.scale)
+
+
+def oracle_decode_step(c, num_threads=None):
     import oracle
-    c = case_host
 
     def step():
-        slots = oracle.slot_mapping(c["positions"], c["block_table"], c["block_size"],
-                                    c["seq_idx"])
-        oracle.reshape_and_cache(c["new_k"], c["new_v"], c["k"], c["v"], slots, c["block_size"])
-        oracle.decode(c["q"], c["k"], c["v"], c["block_table"], c["seq_lens"], c["scale"])
+        oracle.decode(c["q"], c["k"], c["v"], c["block_table"], c["seq_lens"], c["scale"],
+                      num_threads=num_threads)
     return step
 
 
-def host_case(case):
-    from workloads import bits
-    return dict(q=bits(case.q), k=bits(case.k_cache), v=bits(case.v_cache),
-                new_k=bits(case.new_k), new_v=bits(case.new_v),
-                positions=case.positions.cpu().numpy(), seq_idx=case.seq_idx.cpu().numpy(),
-                block_table=case.block_table.cpu().numpy(),
-                seq_lens=case.seq_lens.cpu().numpy(), block_size=case.block_size,
-                scale=case.scale)
-
-
-def cpu_oracle_timing(case_h, seconds, max_steps=None):
-    import oracle
-    step = oracle_step_fn(case_h)
+def cpu_oracle_timing(case_h, seconds, num_threads=None):
+    """Mean host seconds of one oracle decode step (after one untimed step), repeated
+    until `seconds` have passed."""
+    step = oracle_decode_step(case_h, num_threads)
     step()  # builds / loads the oracle library, first touch of the pages
     n, t0 = 0, time.perf_counter()
     while True:
         step()
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds or (max_steps and n >= max_steps):
+        if el >= seconds:
             break
-    return el / n, n, oracle.max_threads()
+    return el / n, n
 
 
-def headline_case(device):
-    """The headline workload with the new token of position 8191 supplied for writing."""
-    return workloads.paged_case(1002, [8192], 832, 64, new_tokens=1, device=device)
+def headline_workload(device):
+    """The headline: the 7 sequences of 32768 keys a 1 GiB pool holds (BS 832, 5% of K
+    rows x8), on disjoint pages; one step decodes one of them."""
+    return workloads.decode_sweep_rotation(HEADLINE_CTX, device)
 
 
 METRIC = "paged decode KV GB/s (% of HBM peak) at 4K-32K ctx; q=4096 prefill TFLOP/s"
 
 
-def headline_config(step_desc, ws):
-    return {"workload": HEADLINE, "block_size": 832, "context": 8192, "step": step_desc,
-            "parallelism": f"replica per GPU x{ws}"}
+def headline_config(ws, extra=None):
+    c = {"workload": HEADLINE, "block_size": 832, "context": HEADLINE_CTX,
+         "step": "pa_decode of one sequence: split-context kernel (one launch) + LSE "
+                 "combine (one launch)",
+         "parallelism": f"replica per GPU x{ws}"}
+    c.update(extra or {})
+    return c
 
 
 def run_reference(args, rank, ws):
     """The reference arm: the fp64 CPU oracle, as it stands, on the host cores, over the
-    headline workload: W untimed steps, then exactly K timed steps (each a full decode
-    step: slot mapping, KV write of the new token, exact attention of 24 heads over 8192
-    keys).  Under torchrun only rank 0 runs it."""
+    headline workload: W untimed steps, then exactly K timed steps, each the exact
+    attention of 24 heads over the 32768 keys of one sequence (the sequences of the
+    rotation in turn), as the GPU step computes.  Under torchrun only rank 0 runs it."""
     if rank != 0:
         return
     import oracle
-    case = headline_case("cpu")
-    step = oracle_step_fn(host_case(case))
-    for _ in range(max(1, args.warmup)):
-        step()
+    from workloads import bits
+    case = headline_workload("cpu")
+    n = case.q.shape[0]
+    kv = (bits(case.k_cache), bits(case.v_cache))
+    steps = [oracle_decode_step(host_decode_case(case, s, kv)) for s in range(n)]
+    for i in range(max(1, args.warmup)):
+        steps[i % n]()
     times = []
-    for _ in range(args.steps):
+    for i in range(args.steps):
         t0 = time.perf_counter()
-        step()
+        steps[i % n]()
         times.append(time.perf_counter() - t0)
     per_step = sum(times) / len(times)
-    v = 8192 * KV_BYTES_PER_TOKEN / per_step / 1e9
+    v = HEADLINE_CTX * KV_BYTES_PER_TOKEN / per_step / 1e9
     threads = oracle.max_threads()
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": headline_config("fp64 CPU oracle: slot mapping + KV write of the new "
-                                      "token + exact attention", 1),
+            "config": headline_config(1),
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"{args.steps} full decode steps of the headline "
-                                       f"workload (slot mapping + KV write + fp64 attention "
-                                       f"of 24 heads over 8192 keys)"},
+                                       f"workload (fp64 attention of 24 heads over 32768 "
+                                       f"keys each), {threads} threads"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def summary_of(value_frac, legs):
+    """A few hundred bytes that repeat each leg's main figure (printed last)."""
+    out = {"decode_32k_step_frac": value_frac}
+    sw = legs.get("decode_sweep_1gib_pool_peaked", {})
+    for ctx, r in sw.items():
+        out[f"decode_{int(ctx) // 1024}k_frac"] = round(r["kv_pct_of_hbm_peak"] / 100, 4)
+        out[f"decode_{int(ctx) // 1024}k_us"] = round(r["ms_per_step"] * 1e3, 2)
+    for bs, r in legs.get("decode_32k_small_pages", {}).items():
+        out[f"decode_32k_bs{bs}_frac"] = round(r["kv_pct_of_hbm_peak"] / 100, 4)
+    r = legs.get("decode_8k_append_step")
+    if r:
+        out["step_8k_append_us"] = round(r["ms_per_step"] * 1e3, 2)
+        out["step_8k_append_e2e_us"] = round(r["e2e"]["ms_per_step"] * 1e3, 2)
+    r = legs.get("decode_8k_bs784")
+    if r:
+        out["decode_8k_bs784_frac"] = round(r["kv_pct_of_hbm_peak"] / 100, 4)
+    r = legs.get("batched_decode_16_fused_write")
+    if r:
+        out["batched_16_frac"] = round(r["kv_pct_of_hbm_peak"] / 100, 4)
+    for k, name in (("prefill_q4096_over_4096", "prefill_q4096"),
+                    ("prefill_first_q4096_at_0", "prefill_first"),
+                    ("prefill_tail_q1685_over_12288", "prefill_tail"),
+                    ("prefill_mixed_4_chunks", "prefill_mixed")):
+        if k in legs:
+            out[name + "_frac"] = round(legs[k]["roofline"]["frac"], 4)
+    return out
 
 
 # ------------------------------------------------------------------------ main
@@ -602,42 +694,54 @@ def main():
         clocks.start()
 
     # ---- headline: timed K steps, barrier + synchronize on both sides
-    value = kernel_gbs = k_ms = e2e_val = e2e_ms = alone_ms = None
+    value = kernel_gbs = k_ms = e2e_val = e2e_ms = alone_ms = again_ms = None
     step_ms = None
     h2d = d2h = 0
+    head = None
     if not args.skip_headline:
-        reps = headline_replicas("cuda")
-        fns = [append_step_fn(pa, c, 8192)[0] for c in reps]
+        head = headline_workload("cuda")
+        n = head.q.shape[0]
+        fns = [attn_fn(pa, head, s, HEADLINE_CTX) for s in range(n)]
+        for _ in range(args.warmup):  # warm-up outside the timed region
+            fns[0]()
         barrier(ws)
         torch.cuda.synchronize()
         step_ms = time_stream(fns, args.steps, args.warmup, flush)
         torch.cuda.synchronize()
         barrier(ws)
         total_ms = max_over_ranks(step_ms * args.steps, ws)
-        nbytes_rank = 8192 * KV_BYTES_PER_TOKEN * args.steps
+        nbytes_rank = HEADLINE_CTX * KV_BYTES_PER_TOKEN * args.steps
         value = sum_over_ranks(nbytes_rank, ws) / (total_ms * 1e-3) / 1e9
         kms = time_main_kernel(pa, fns[0], args.steps, args.warmup, flush)
         k_ms = statistics.mean(kms)
-        kernel_gbs = 8192 * KV_BYTES_PER_TOKEN / (k_ms * 1e-3) / 1e9
-        # The same step on its own: one single-step graph replayed after an L2 flush
-        # (its own graph launch included), for comparison with the stream figure.
+        kernel_gbs = HEADLINE_CTX * KV_BYTES_PER_TOKEN / (k_ms * 1e-3) / 1e9
         alone_ms = statistics.mean(time_steps(graph_of(fns[0]).replay, args.steps,
                                               args.warmup, flush))
-        e2e_ms, h2d, d2h = e2e_leg(pa, reps, args.steps, args.warmup, flush)
-        e2e_val = 8192 * KV_BYTES_PER_TOKEN / (e2e_ms * 1e-3) / 1e9
+        # End to end through the public API with host buffers, then the device-resident
+        # stream again (A/B/A, back to back in this run).
+        efns, outs, h2d, d2h = e2e_decode_fns(pa, head, HEADLINE_CTX)
+        e2e_ms = time_stream(efns, args.steps, args.warmup, flush)
+        again_ms = time_stream(fns, args.steps, args.warmup, flush)
+        torch.cuda.synchronize()
+        for out_h, s in outs[:min(len(outs), args.steps)]:
+            ref = pa.decode(head.q[s:s + 1], head.k_cache, head.v_cache,
+                            head.block_table[s:s + 1], head.seq_lens[s:s + 1], head.scale,
+                            HEADLINE_CTX)
+            assert torch.equal(out_h, ref.cpu()), "a step's host output differs from the decode's"
+        e2e_val = HEADLINE_CTX * KV_BYTES_PER_TOKEN / (e2e_ms * 1e-3) / 1e9
         assert pa.device_errors() == 0, "device error word set during the headline leg"
-        del reps, fns
-        torch.cuda.empty_cache()
+        del fns, efns, outs
 
     legs = {}
     want = set() if args.legs == "none" else (
-        {"sweep", "small_pages", "bs784", "batched", "prefill", "prefill_tail", "prefill_first",
-         "prefill_mixed", "prep"}
+        {"sweep", "small_pages", "step8k", "bs784", "batched", "prefill", "prefill_tail",
+         "prefill_first", "prefill_mixed", "prep"}
         if args.legs == "all" else set(args.legs.split(",")))
     if rank == 0 and "sweep" in want:
         sweep = {}
         for ctx in [int(x) for x in args.contexts.split(",") if x]:
-            c = workloads.decode_sweep_rotation(ctx, "cuda")
+            c = head if ctx == HEADLINE_CTX and head is not None else \
+                workloads.decode_sweep_rotation(ctx, "cuda")
             n = c.q.shape[0]
             fns = [attn_fn(pa, c, s, ctx) for s in range(n)]
             sweep[str(ctx)] = decode_leg(
@@ -647,6 +751,8 @@ def main():
             del c, fns
             torch.cuda.empty_cache()
         legs["decode_sweep_1gib_pool_peaked"] = sweep
+    head = None
+    torch.cuda.empty_cache()
     if rank == 0 and "small_pages" in want:
         small = {}
         for bs in (16, 64):
@@ -660,6 +766,8 @@ def main():
             del c, fns
             torch.cuda.empty_cache()
         legs["decode_32k_small_pages"] = small
+    if rank == 0 and "step8k" in want:
+        legs["decode_8k_append_step"] = step8k_leg(pa, args.steps, args.warmup, flush, peaks)
     if rank == 0 and "bs784" in want:
         reps = headline_replicas("cuda", block_size=784, new_tokens=0)
         fns = [attn_fn(pa, c, 0, 8192) for c in reps]
@@ -697,54 +805,63 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        c = headline_case("cpu")
-        per_step, n, threads = cpu_oracle_timing(host_case(c), seconds=args.cpu_seconds)
-        cv = 8192 * KV_BYTES_PER_TOKEN / per_step / 1e9
-        cpu = {"value": cv, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} full decode steps of the headline workload (slot mapping + KV "
-                         f"write + fp64 attention, 24 heads x 8192 keys), {per_step*1e3:.1f} ms each"}
+        import oracle
+        c = headline_workload("cuda")
+        ch = host_decode_case(c, 0)
+        del c
+        torch.cuda.empty_cache()
+        per_all, n_all = cpu_oracle_timing(ch, args.cpu_seconds)
+        per_one, n_one = cpu_oracle_timing(ch, args.cpu_seconds, num_threads=1)
+        nbytes = HEADLINE_CTX * KV_BYTES_PER_TOKEN
+        cpu = {"value": nbytes / per_all / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{n_all} full decode steps of the headline workload (fp64 attention "
+                         f"of 24 heads over 32768 keys), {per_all * 1e3:.1f} ms each on "
+                         f"{oracle.max_threads()} threads",
+               "single_thread": {"value": nbytes / per_one / 1e9, "unit": "GB/s", "cores": 1,
+                                 "ms_per_step": per_one * 1e3,
+                                 "sample": f"{n_one} steps of the same workload, one thread"}}
 
     if rank != 0:
         return
+    frac = kernel_gbs / peaks["hbm_gbs"] if kernel_gbs else None
     line = {
         "metric": METRIC,
         "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": HEADLINE, "block_size": 832, "context": 8192,
-                   "step": "pa_decode_append: slot of the new token derived in the kernel + "
-                           "its KV write + split decode (one launch), LSE combine (one launch)",
-                   "timing": f"{args.steps} consecutive steps captured in one CUDA graph, one "
-                             f"replay between two events (the graph's launch paid once)",
-                   "l2": "inputs larger than L2: 16 copies of the workload (own 64-page pools, "
-                         "16 x 33.5 MB of K/V) decoded in turn, so no step finds its K/V in "
-                         "the 129 MB L2",
-                   "step_alone_ms": alone_ms,
-                   "step_alone": "the same step as a single-step graph replayed after an L2 "
-                                 "flush (its graph launch included)",
-                   "kv_pct_of_hbm_peak": (100.0 * value / ws / peaks["hbm_gbs"]
-                                          if value else None),
-                   "parallelism": f"replica per GPU x{ws}"},
+        "config": headline_config(ws, {
+            "timing": f"{args.steps} consecutive steps captured in one CUDA graph, one "
+                      f"replay between two events (the graph's launch paid once)",
+            "l2": "inputs larger than L2: the 7 sequences of 32768 keys the 1 GiB pool holds "
+                  "(939 MB of K/V), decoded one per step in turn, so no step finds its K/V in "
+                  "the 129 MB L2",
+            "step_alone_ms": alone_ms,
+            "step_alone": "the same step as a single-step graph replayed after an L2 flush "
+                          "(its graph launch included)",
+            "device_ms_per_step_after_e2e": again_ms,
+            "kv_pct_of_hbm_peak": (100.0 * value / ws / peaks["hbm_gbs"] if value else None)}),
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "copies": "H2D: one pa_copy kernel from a pinned staging buffer; D2H: the "
-                          "combine kernel writes the output into a pinned host buffer; all "
-                          "inside the steps' CUDA graph"},
-        # per step: the split decode (slot derivation + KV write fused) and the LSE combine
+                "copies": "H2D: one pa_copy kernel from a pinned staging buffer (q, block-table "
+                          "row, sequence length); D2H: the combine kernel writes the output "
+                          "into a pinned host buffer; all inside the steps' CUDA graph, timed "
+                          "between two timings of the device-resident stream"},
+        # per step: the split-context decode and the LSE combine
         "gpu_launches": 0 if args.skip_headline else 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": kernel_gbs / peaks["hbm_gbs"] if kernel_gbs else None,
-                     "traffic": SPLIT_8K_DRAM_BYTES,
+                     "unit": "GB/s", "frac": frac,
+                     "traffic": SPLIT_32K_DRAM_BYTES,
                      "traffic_unit": "bytes per launch",
                      "kernel": "decode_split_kernel",
-                     "algorithmic_bytes_per_launch": 8192 * KV_BYTES_PER_TOKEN,
+                     "algorithmic_bytes_per_launch": HEADLINE_CTX * KV_BYTES_PER_TOKEN,
                      "kernel_ms": k_ms, "peak_source": f"{peaks['source']} hbm_gbs",
                      "kernel_timing": "library events around the split launch of an eager "
-                                      "step after an L2 flush, mean of K launches (events "
-                                      "inside the steps' graph measure it 2 us longer)"},
+                                      "step after an L2 flush, mean of K launches"},
         "cpu_baseline": cpu,
         "legs": legs,
+        "summary": summary_of(round(value / ws / peaks["hbm_gbs"], 4) if value else None, legs),
     }
     print(json.dumps(line), flush=True)
 
