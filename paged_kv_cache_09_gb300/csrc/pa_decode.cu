@@ -685,11 +685,22 @@ DecodePlan plan_decode(int num_seqs, int num_kv_heads, int block_size, int max_s
     return pl;
 }
 
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, const DecodePlan &plan) {
+// Workspace layout, the one place that defines it: fp32 partial sums [S, Hq, splits, D],
+// then (max, sum) pairs [S, Hq, splits], each region 256-byte aligned.
+namespace {
+struct DecodeWsLayout {
+    size_t o_bytes, ml_bytes;
+};
+DecodeWsLayout decode_ws_layout(int num_seqs, int num_q_heads, const DecodePlan &plan) {
     const size_t parts = (size_t)num_seqs * num_q_heads * plan.num_splits;
-    const size_t o_bytes = (parts * kHeadDim * sizeof(float) + 255) & ~size_t(255);
-    const size_t ml_bytes = (parts * sizeof(float2) + 255) & ~size_t(255);
-    return o_bytes + ml_bytes;
+    return {(parts * kHeadDim * sizeof(float) + 255) & ~size_t(255),
+            (parts * sizeof(float2) + 255) & ~size_t(255)};
+}
+}  // namespace
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, const DecodePlan &plan) {
+    const DecodeWsLayout l = decode_ws_layout(num_seqs, num_q_heads, plan);
+    return l.o_bytes + l.ml_bytes;
 }
 
 cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const DecodePlan &plan,
@@ -719,10 +730,9 @@ cudaError_t launch_decode(const CUtensorMap *tmaps, const DecodeArgs &a, const D
     p.num_splits = plan.num_splits;
     p.num_pages = a.num_pages;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const size_t parts = (size_t)a.num_seqs * a.num_q_heads * plan.num_splits;
-    const size_t o_bytes = (parts * kHeadDim * sizeof(float) + 255) & ~size_t(255);
+    const DecodeWsLayout ws = decode_ws_layout(a.num_seqs, a.num_q_heads, plan);
     p.part_o = static_cast<float *>(a.workspace);
-    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(a.workspace) + o_bytes);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(a.workspace) + ws.o_bytes);
     p.out = a.out;
     p.err = a.err;
     p.k_cache_w = a.k_cache_w;

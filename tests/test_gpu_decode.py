@@ -258,3 +258,33 @@ def test_fused_write_checks_the_slot_of_the_newest_token(cuda_lib):
     oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_ref, v_ref,
                              good.cpu().numpy(), 832)
     assert np.array_equal(bits(case.k_cache), k_ref)
+
+
+@pytest.mark.parametrize("fill", ["nan", "finite"])
+@pytest.mark.parametrize("seq_lens", [[8192], [1, 17, 240, 3000, 16000], [1701, 1700]])
+def test_decode_ignores_what_the_workspace_held(cuda_lib, fill, seq_lens):
+    # The workspace's contents on entry do not matter: the combine reads only the
+    # (max, sum) pair and partial sums every split wrote in the same call (an empty split
+    # writes (-inf, 0)).  A workspace full of NaN, or of finite values that would pass
+    # for a real split's partial (every float pair (30, 1): a large max and a unit sum),
+    # must change nothing, with short last splits and splits past a sequence's end among
+    # the lengths.  A stale pair read by the combine would outweigh the real splits.
+    pa = cuda_lib
+    bs = 832
+    npg = sum(-(-L // bs) for L in seq_lens) + 2
+    case = workloads.paged_case(900 + sum(seq_lens), seq_lens, bs, npg, device="cuda")
+    msl = max(seq_lens) + 5000
+    need = pa.decode_workspace_size(len(seq_lens), 24, 4, 256, bs, msl)
+    clean = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    want = _gpu_decode(pa, case, max_seq_len=msl, workspace=clean)
+    dirty = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    if fill == "nan":
+        dirty.fill_(float("nan"))
+    else:
+        dirty.view(-1, 2)[:, 0] = 30.0
+        dirty.view(-1, 2)[:, 1] = 1.0
+    got = _gpu_decode(pa, case, max_seq_len=msl, workspace=dirty.view(torch.uint8))
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    assert_attention_close(got, _oracle_decode(case), f"dirty workspace {fill}")
+    assert pa.device_errors() == 0
