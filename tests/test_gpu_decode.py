@@ -272,8 +272,9 @@ def test_decode_ignores_what_the_workspace_held(cuda_lib, fill, seq_lens):
     pa = cuda_lib
     bs = 832
     npg = sum(-(-L // bs) for L in seq_lens) + 2
-    case = workloads.paged_case(900 + sum(seq_lens), seq_lens, bs, npg, device="cuda")
-    msl = max(seq_lens) + 5000
+    msl = max(seq_lens) + 5000  # splits past every sequence's end
+    case = workloads.paged_case(900 + sum(seq_lens), seq_lens, bs, npg, device="cuda",
+                                max_blocks=-(-msl // bs))
     need = pa.decode_workspace_size(len(seq_lens), 24, 4, 256, bs, msl)
     clean = torch.zeros(need, dtype=torch.uint8, device="cuda")
     want = _gpu_decode(pa, case, max_seq_len=msl, workspace=clean)
