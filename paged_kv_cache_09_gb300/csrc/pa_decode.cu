@@ -164,8 +164,10 @@ __device__ __forceinline__ int checked_seq_len(const DecodeKParams &p, int seq, 
     return L;
 }
 
+// CTA barrier `id` for `threads` threads.  The non-aligned form: the threads may reach it
+// from different places in the code (the producer and the consumers do).
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 #ifdef PA_TEST_HOOKS
