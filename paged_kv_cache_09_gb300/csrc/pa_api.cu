@@ -615,8 +615,9 @@ int pa_get_device_errors(unsigned int *bits, int clear, void *stream) {
 }
 
 #ifdef PA_TEST_HOOKS
-int pa_test_hook(int decode_skip_stage, int prefill_skip_unit) {
-    if (pa::set_decode_test_hook(decode_skip_stage) != cudaSuccess ||
+int pa_test_hook(int decode_skip_stage, int prefill_skip_unit, int decode_consumer_delay_ns) {
+    if (decode_consumer_delay_ns < 0 || decode_consumer_delay_ns > 1000000) return PA_ERR_INVALID_ARG;
+    if (pa::set_decode_test_hook(decode_skip_stage, decode_consumer_delay_ns) != cudaSuccess ||
         pa::set_prefill_test_hook(prefill_skip_unit) != cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;

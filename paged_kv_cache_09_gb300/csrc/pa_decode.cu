@@ -177,15 +177,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 
 #ifdef PA_TEST_HOOKS
 // Test build only: the ring stage whose loads the producer leaves out (-1: none), so
-// that the consumer waiting for it runs into its bounded wait.  Set by
+// that the consumer waiting for it runs into its bounded wait; and a delay (ns) before
+// the consumer warps other than the one writing the newest token start on their tiles,
+// so that every load of the split may land before the first wait.  Set by
 // set_decode_test_hook through pa_test_hook.
 __device__ int g_test_skip_stage = -1;
+__device__ int g_test_consumer_delay_ns = 0;
 #endif
 
 template <int kDecConsumers, int kDecStages>
 __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     decode_split_kernel(const __grid_constant__ DecMaps maps, const DecodeKParams p) {
     (void)DecShape<kDecConsumers, kDecStages>::consumers;  // checks the warp mapping
+    static_assert(kDecStages >= 2, "the reload of a one-stage split completes on full[1]");
     constexpr int kDecRingBytes = kDecStages * kDecStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -267,7 +271,11 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     const int nst = (n + kDecPair - 1) / kDecPair;    // stages of this split
     // This CTA holds the tile of the token being decoded and has to write that token.
     const bool writes_newest = p.new_k != nullptr && t1 == ntiles;
-    // ... and if that tile is in the stage loaded ahead, the stage is loaded twice.
+    // ... and if that tile is in the stage loaded ahead, the stage is loaded twice.  The
+    // second load completes on full[1] (a split of one stage never uses ring slot 1), so
+    // its consumers wait for the first phase of a barrier of its own: an mbarrier wait
+    // tells only two phases apart, and a consumer that reached a wait for the second
+    // phase of full[0] late, after both loads had landed, could not tell.
     const bool refetch = writes_newest && spec && nst == 1;
 
     if (warp == kDecConsumers) {
@@ -290,13 +298,14 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
             int page_next = lp0 < lp_last ? bt[lp0 + 1] : 0;
             if (refetch) {
                 // The split's only stage holds the token being decoded and was loaded
-                // before that token was written: load it again once the first load has
-                // landed and the write is done.  Its consumers wait for both loads.
+                // before that token was written: load it again into the same slot once
+                // the first load has landed and the write is done, completing on full[1].
+                // Its consumers wait for that load only.
                 if (mbar_wait_abort(&full[0], 0, p.err, abort) &&
                     mbar_wait_abort(written, 0, p.err, abort)) {
-                    load_stage(maps, smem, &full[0], g, off0, page0, off0 + kDecTile,
+                    load_stage(maps, smem, &full[1], g, off0, page0, off0 + kDecTile,
                                page0);
-                    par |= 1u;
+                    issued |= 2u;  // full[1], phase parity 0
                 }
             }
             for (int m = spec ? 1 : 0; m < nst; ++m) {
@@ -353,6 +362,14 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     // ---------------------------------------------------------------- consumers
     if (writes_newest && warp == kDecConsumers - 1)
         write_newest_token(p, bt, seq, g, seq_len, lane, written);
+#ifdef PA_TEST_HOOKS
+    else {
+        const unsigned long long delay =
+            (unsigned)*reinterpret_cast<volatile int *>(&g_test_consumer_delay_ns);
+        const unsigned long long t_start = global_ns();
+        while (global_ns() - t_start < delay) __nanosleep(256);  // ends after `delay` ns
+    }
+#endif
 
     // Q^T as the B operand: lane holds head n = lane/4 and dims 2(lane%4)+{0,1} (+8)
     // of every 16-dim k-step.  Heads past the group are zero columns.
@@ -490,11 +507,10 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
         for (int i = warp; i < n; i += kDecConsumers) {
             const int m = i / kDecPair, h = i - m * kDecPair;
             const int s = m % kDecStages;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait_abort(&full[s], (m / kDecStages) & 1, p.err, abort)))
-                break;
-            if (refetch && !__all_sync(0xffffffffu, mbar_wait_abort(&full[0], 1, p.err, abort)))
-                break;
+            // (refetch: the split's one stage, reloaded; its second load completes on full[1])
+            uint64_t *fb = refetch ? &full[1] : &full[s];
+            const uint32_t ph = refetch ? 0u : (uint32_t)(m / kDecStages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait_abort(fb, ph, p.err, abort))) break;
             tile(s, h, i);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
@@ -502,9 +518,9 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     } else {
         for (int m = warp; m < nst; m += kDecConsumers) {
             const int s = m % kDecStages;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait_abort(&full[s], (m / kDecStages) & 1, p.err, abort)))
-                break;
+            uint64_t *fb = refetch ? &full[1] : &full[s];  // (refetch: as above)
+            const uint32_t ph = refetch ? 0u : (uint32_t)(m / kDecStages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait_abort(fb, ph, p.err, abort))) break;
             for (int h = 0; h < kDecPair && m * kDecPair + h < n; ++h) tile(s, h, m * kDecPair + h);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s], kDecPair);
@@ -719,8 +735,11 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
 }  // namespace
 
 #ifdef PA_TEST_HOOKS
-cudaError_t set_decode_test_hook(int skip_stage) {
-    return cudaMemcpyToSymbol(g_test_skip_stage, &skip_stage, sizeof skip_stage);
+cudaError_t set_decode_test_hook(int skip_stage, int consumer_delay_ns) {
+    cudaError_t e = cudaMemcpyToSymbol(g_test_skip_stage, &skip_stage, sizeof skip_stage);
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_test_consumer_delay_ns, &consumer_delay_ns,
+                              sizeof consumer_delay_ns);
 }
 #endif
 

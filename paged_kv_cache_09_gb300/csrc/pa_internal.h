@@ -220,10 +220,13 @@ cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaS
 // Test build only (libpa_test.so, compiled with -DPA_TEST_HOOKS and a short wait limit):
 // the decode producer leaves out the loads of ring stage `skip_stage` of every CTA, the
 // prefill producer those of ring unit `skip_unit` (-1: none), so that a consumer's
-// bounded wait runs out.  Exported to the failure-path tests as
-//     extern "C" int pa_test_hook(int decode_skip_stage, int prefill_skip_unit);
+// bounded wait runs out; and the decode consumer warps (but the one writing the newest
+// token) start `consumer_delay_ns` late, after the split's loads may all have landed.
+// Exported to the failure-path tests as
+//     extern "C" int pa_test_hook(int decode_skip_stage, int prefill_skip_unit,
+//                                 int decode_consumer_delay_ns);
 // The product library has neither the hooks nor this entry point.
-cudaError_t set_decode_test_hook(int skip_stage);
+cudaError_t set_decode_test_hook(int skip_stage, int consumer_delay_ns);
 cudaError_t set_prefill_test_hook(int skip_unit);
 #endif
 

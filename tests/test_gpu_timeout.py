@@ -1,4 +1,5 @@
-"""Failure path of the bounded waits, on the GPU, without faulting it.
+"""Failure path of the bounded waits, on the GPU, without faulting it; and a timing the
+test build can force (consumers that start late).
 
 The test library (libpa_test.so: the same sources built with PA_TEST_HOOKS and a 20 ms
 limit on every bounded wait) can leave out the TMA loads of one ring stage (decode) or
@@ -31,7 +32,7 @@ def test_lib(cuda_lib):
     lib = ctypes.CDLL(_build.build_test())
     P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                             ctypes.c_size_t)
-    lib.pa_test_hook.argtypes = [i32, i32]
+    lib.pa_test_hook.argtypes = [i32, i32, i32]
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode.argtypes = [P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32,
@@ -39,9 +40,9 @@ def test_lib(cuda_lib):
     lib.pa_prefill_chunk.argtypes = [P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32,
                                      f32, P, P]
     lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, P]
-    assert lib.pa_test_hook(-1, -1) == PA_OK
+    assert lib.pa_test_hook(-1, -1, 0) == PA_OK
     yield lib
-    lib.pa_test_hook(-1, -1)
+    lib.pa_test_hook(-1, -1, 0)
 
 
 def _stream():
@@ -86,12 +87,12 @@ def test_decode_wait_that_runs_out_is_reported_and_the_context_stays_usable(test
     lib = test_lib
     case = workloads.decode_8k(device="cuda")
     assert _errors(lib) == (PA_OK, 0)
-    assert lib.pa_test_hook(1, -1) == PA_OK  # every CTA loses its ring stage 1
+    assert lib.pa_test_hook(1, -1, 0) == PA_OK  # every CTA loses its ring stage 1
     bad = _decode(lib, case, 8192)
     rc, errs = _errors(lib)
     assert rc == PA_ERR_TIMEOUT and errs & DEVERR_TIMEOUT, (rc, errs)
     assert torch.isfinite(bad.float()).all()
-    assert lib.pa_test_hook(-1, -1) == PA_OK
+    assert lib.pa_test_hook(-1, -1, 0) == PA_OK
     for _ in range(2):
         good = _decode(lib, case, 8192)
         assert _errors(lib) == (PA_OK, 0)
@@ -114,11 +115,11 @@ def test_prefill_wait_that_runs_out_is_reported_and_the_context_stays_usable(tes
     cuda_lib.reshape_and_cache(case.new_k, case.new_v, case.k_cache, case.v_cache, slots)
     torch.cuda.synchronize()
     assert _errors(lib) == (PA_OK, 0)
-    assert lib.pa_test_hook(-1, 3) == PA_OK  # every CTA loses its K/V ring unit 3
+    assert lib.pa_test_hook(-1, 3, 0) == PA_OK  # every CTA loses its K/V ring unit 3
     _prefill(lib, case)
     rc, errs = _errors(lib)
     assert rc == PA_ERR_TIMEOUT and errs & DEVERR_TIMEOUT, (rc, errs)
-    assert lib.pa_test_hook(-1, -1) == PA_OK
+    assert lib.pa_test_hook(-1, -1, 0) == PA_OK
     good = _prefill(lib, case)
     assert _errors(lib) == (PA_OK, 0)
     want = cuda_lib.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
@@ -128,3 +129,40 @@ def test_prefill_wait_that_runs_out_is_reported_and_the_context_stays_usable(tes
                          case.block_table[0].cpu().numpy(), q_start, True, case.scale)
     assert_attention_close(good, ref, "prefill after a timed-out call")
     assert cuda_lib.device_errors() == 0
+
+
+@pytest.mark.parametrize("seq_len", [1537, 1553, 1665, 1696])
+def test_decode_late_consumers_with_a_reloaded_stage(test_lib, cuda_lib, seq_len):
+    # A split whose only stage holds the token being decoded loads that stage twice (the
+    # second time after the token's K/V are written).  Consumer warps that start only
+    # after both loads have landed must still take the second load: it completes on a
+    # barrier of its own, since an mbarrier wait tells only two phases apart.  The test
+    # build holds the consumers back 30 us; with both loads on one barrier they waited
+    # for a phase that had already passed, until their wait ran out.
+    lib = test_lib
+    bs = 832
+    case = workloads.paged_case(73, [seq_len], bs, 8, new_tokens=1, device="cuda")
+    k_ref, v_ref = bits(case.k_cache).copy(), bits(case.v_cache).copy()
+    slots_h = oracle.slot_mapping(case.positions.cpu().numpy(), case.block_table.cpu().numpy(),
+                                  bs, case.seq_idx.cpu().numpy())
+    oracle.reshape_and_cache(bits(case.new_k), bits(case.new_v), k_ref, v_ref, slots_h, bs)
+    slots = cuda_lib.slot_mapping(case.positions, case.block_table, bs, seq_idx=case.seq_idx)
+    torch.cuda.synchronize()
+    assert lib.pa_test_hook(-1, -1, 30000) == PA_OK
+    S, hq, d = case.q.shape
+    out = torch.empty_like(case.q)
+    ws = torch.empty(max(256, lib.pa_decode_workspace_size(S, hq, 4, d, bs, seq_len)),
+                     dtype=torch.uint8, device="cuda")
+    rc = lib.pa_decode(case.q.data_ptr(), case.k_cache.data_ptr(), case.v_cache.data_ptr(),
+                       case.k_cache.stride(0), case.k_cache.shape[0],
+                       case.block_table.data_ptr(), case.block_table.stride(0),
+                       case.seq_lens.data_ptr(), S, seq_len, hq, 4, d, bs, case.scale,
+                       out.data_ptr(), ws.data_ptr(), ws.numel(), case.new_k.data_ptr(),
+                       case.new_v.data_ptr(), slots.data_ptr(), _stream())
+    assert rc == PA_OK
+    assert _errors(lib) == (PA_OK, 0)
+    assert lib.pa_test_hook(-1, -1, 0) == PA_OK
+    assert np.array_equal(bits(case.k_cache), k_ref) and np.array_equal(bits(case.v_cache), v_ref)
+    ref = oracle.decode(bits(case.q), k_ref, v_ref, case.block_table.cpu().numpy(),
+                        case.seq_lens.cpu().numpy(), case.scale)
+    assert_attention_close(out, ref, f"late consumers, reloaded stage, L={seq_len}")
