@@ -59,11 +59,6 @@ constexpr int dec_smem_bytes() {
     return 1024 + kS * kDecStageBytes + (2 * kS + 1) * 8 + 8;  // + the abort flag
 }
 
-// A split's (max, sum) slot holds this pair from the split kernel's start until the split
-// stores its result there: a sum below zero, which no finished split has.  The combine,
-// launched while the split kernel still runs, waits on it (see decode_combine_kernel).
-#define PA_ML_PENDING make_float2(0.f, -1.f)
-
 constexpr int kCombineThreads = 256;
 constexpr int kCombineParts = 4;                       // CTAs per (query head, sequence)
 constexpr int kCombineDims = kHeadDim / kCombineParts;  // dims one CTA merges: 2 per lane
@@ -219,21 +214,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     }
     __syncthreads();
     pdl_wait();
-    // The combine is launched as soon as every CTA of this grid has triggered, and then
-    // waits on the (max, sum) slots rather than on the whole grid.  So before this CTA
-    // triggers, its slots are marked pending, with a fence that makes the mark visible
-    // to the GPU: the combine can then never take a slot's contents from an earlier call
-    // for this call's result.  One thread's trigger counts for the CTA, so no other
-    // thread triggers.  (Warp 0 is a consumer warp: the producer's loads do not wait.)
-    if (warp == 0) {
-        if (lane < p.group) {
-            p.part_ml[((int64_t)seq * p.num_q_heads + g * p.group + lane) * p.num_splits +
-                      split] = PA_ML_PENDING;
-            __threadfence();
-        }
-        __syncwarp();
-        if (lane == 0) pdl_trigger();
-    }
+    pdl_trigger();
 
     const int32_t *bt = p.block_table + (int64_t)seq * p.bt_stride;
     const int tpp = p.tiles_per_page;
@@ -568,7 +549,7 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
     named_bar_sync(2, kDecConsumers * 32);
     // Thread t merges the quads (4 consecutive dims of one head) t, t + 32C, ...  Every
     // thread derives its head's CTA max and the warps' weights exp2(m_w - M) itself, so
-    // all loads of a quad are independent.
+    // no further barrier is needed and all loads of a quad are independent.
     constexpr int kQuadsPerHead = kHeadDim / 4;
     constexpr int kMergeThreads = kDecConsumers * 32;
     const int nquads = p.group * kQuadsPerHead;
@@ -585,12 +566,14 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
                 mw[w] = red_m[w * kDecMaxGroup + c];
                 M = fmaxf(M, mw[w]);
             }
+            float L = 0.f;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < kDecConsumers; ++w) {
                 const float e = M == -CUDART_INF_F ? 0.f : exp2f(mw[w] - M);
                 const float4 v = *reinterpret_cast<const float4 *>(
                     red_o + (w * kDecMaxGroup + c) * kDecMergeRow + d);
+                L += e * red_l[w * kDecMaxGroup + c];
                 O.x += e * v.x;
                 O.y += e * v.y;
                 O.z += e * v.z;
@@ -599,25 +582,8 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
             const int64_t pi =
                 ((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split;
             *reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim + d) = O;
+            if (d == 0) p.part_ml[pi] = make_float2(M, L);
         }
-    }
-    // The (max, sum) pair of head c is stored last, by thread c, after every partial sum
-    // of the CTA (the barrier orders them, the fence publishes them first): the combine
-    // reads the partial sums once it sees the pair.
-    named_bar_sync(2, kDecConsumers * 32);
-    if (threadIdx.x < p.group) {
-        const int c = threadIdx.x;
-        float M = -CUDART_INF_F, L = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, red_m[w * kDecMaxGroup + c]);
-#pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w) {
-            const float e = M == -CUDART_INF_F ? 0.f : exp2f(red_m[w * kDecMaxGroup + c] - M);
-            L += e * red_l[w * kDecMaxGroup + c];
-        }
-        __threadfence();
-        p.part_ml[((int64_t)seq * p.num_q_heads + g * p.group + c) * p.num_splits + split] =
-            make_float2(M, L);
     }
 }
 
@@ -637,14 +603,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     const int h = blockIdx.x / kCombineParts, d0 = (blockIdx.x % kCombineParts) * kCombineDims;
     const int seq = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    // No wait for the split grid to complete: this kernel is launched once every split
-    // CTA has marked its (max, sum) slots pending (PA_ML_PENDING) and triggered, and it
-    // waits on those slots instead, so its loads and merging overlap the split kernel's
-    // last tiles.  A split stores its partial sums, fences, then stores its pair; an
-    // empty split stores (-inf, 0) and no sums.  Nothing else this kernel reads is
-    // written by the split kernel, and the work before that kernel had completed before
-    // it triggered.
+    pdl_wait();
     pdl_trigger();
+    // Every split wrote its (max, sum); an empty one (max -inf) gets weight 0 and its
+    // partial sums, never written, are skipped.
     const int nsplit = p.num_splits;
     const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.num_splits;
     const float2 *po = reinterpret_cast<const float2 *>(p.part_o + base * kHeadDim + d0) + lane;
@@ -652,28 +614,6 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     float acc0 = 0.f, acc1 = 0.f;
     // Split j of this warp's k-th batch element: warp + kWarps * (b0 + k).
     for (int b0 = 0; warp + kWarps * b0 < nsplit; b0 += kBatch) {
-        // Lane k < kBatch watches the (max, sum) slot of the batch's k-th split until it
-        // is stored (bounded; a split that never stores it is left out and the wait
-        // reports PA_DEVERR_TIMEOUT).
-        const int jl = warp + kWarps * (b0 + lane);
-        const bool mine = lane < kBatch && jl < nsplit;
-        bool pending = mine && ld_f2_ordered(p.part_ml + base + jl).y < 0.f;
-        if (__any_sync(0xffffffffu, pending)) {
-            const unsigned long long t0 = global_ns();
-            bool late = false;
-            for (;;) {
-                __nanosleep(64);
-                if (pending) pending = ld_f2_ordered(p.part_ml + base + jl).y < 0.f;
-                if (!__any_sync(0xffffffffu, pending)) break;
-                late = global_ns() - t0 > kWaitLimitNs;
-                if (__any_sync(0xffffffffu, late)) break;
-            }
-            if (__any_sync(0xffffffffu, late)) {
-                if (lane == 0) atomicOr(p.err, kErrTimeout);
-                break;
-            }
-        }
-        __threadfence();  // acquire: the partial sums stored before the pairs are visible
         float2 va[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
@@ -681,10 +621,11 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
             va[k] = j < nsplit ? ld_f2_ordered(po + (int64_t)j * (kHeadDim / 2))
                                : make_float2(0.f, 0.f);
         }
-        // Lane k < kBatch holds the (max, sum) of the batch's k-th split, read again (its
-        // final value) together with the sums.
-        const float2 ml = mine ? ld_f2_ordered(p.part_ml + base + jl)
-                               : make_float2(-CUDART_INF_F, 0.f);
+        // Lane k < kBatch holds the (max, sum) of the batch's k-th split (loaded after
+        // the sums, so that all of the batch's loads are in flight together).
+        const int jl = warp + kWarps * (b0 + lane);
+        const float2 ml = lane < kBatch && jl < nsplit ? ld_f2_ordered(p.part_ml + base + jl)
+                                                       : make_float2(-CUDART_INF_F, 0.f);
         float bm = ml.x;
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, sh));
