@@ -361,23 +361,28 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     out = torch.empty_like(case.q)
     slots = torch.empty(case.positions.numel(), dtype=torch.int64, device="cuda")
     cu = case.meta.get("cu_seqlens_q")
+    hq, d, hkv, bs = case.q.shape[1], case.q.shape[2], case.k_cache.shape[2], case.block_size
     if cu is None:  # one sequence's chunk
         q_len, q_start = case.q.shape[0], case.q_start
         flops = causal_flops(q_len, q_start)
         bt0 = case.block_table[0].contiguous()
+        need = pa.prefill_workspace_size(q_len, q_start, True, hq, hkv, d, bs)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
 
         def attn():
             pa.prefill_chunk(case.q, case.k_cache, case.v_cache, bt0, case.q_start, True,
-                             case.scale, out=out)
+                             case.scale, out=out, workspace=ws)
     else:  # a mixed batch of chunks
         k_lens = case.meta["seq_lens"]
         q_len = int(cu[-1])
         q_start = [L - (cu[b + 1] - cu[b]) for b, L in enumerate(k_lens)]
         flops = sum(causal_flops(cu[b + 1] - cu[b], q_start[b]) for b in range(len(k_lens)))
+        need = pa.prefill_varlen_workspace_size(cu, k_lens, True, hq, hkv, d, bs)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
 
         def attn():
             pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
-                              True, case.scale, out=out)
+                              True, case.scale, out=out, workspace=ws)
 
     def step():
         pa.slot_mapping(case.positions, case.block_table, case.block_size,
@@ -388,7 +393,7 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     ms = time_steps(g.replay, steps, warmup, flush)
     kms = time_main_kernel(pa, attn, steps, warmup, flush)
     step_ms, k_ms = statistics.mean(ms), statistics.mean(kms)
-    r = {"q_len": q_len, "q_start": q_start, "causal_flops": flops,
+    r = {"q_len": q_len, "q_start": q_start, "causal_flops": flops, "workspace_bytes": need,
          "ms_per_step": step_ms, "step_tflops": flops / (step_ms * 1e-3) / 1e12,
          "kernel_ms": k_ms, "kernel_ms_min": min(kms),
          "kernel_tflops": flops / (k_ms * 1e-3) / 1e12}

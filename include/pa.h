@@ -230,6 +230,18 @@ int pa_decode_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v
                       int block_size, float scale, pa_bf16 *out, void *stream);
 
 /*
+ * pa_prefill_workspace_size -- bytes of device workspace with which pa_prefill_chunk
+ * may split work items along the keys for this chunk shape on the current device; 0 when
+ * no split would pay (or for invalid sizes).  The kernel's work item is 128 query rows of
+ * one head; when the items do not divide evenly over the SMs (the q=1685 tail chunk over
+ * 12288 tokens has 336 items of ~52 key tiles for 152 SMs; a short chunk over a long
+ * context has fewer items than SMs), pieces of the longest items run on different SMs
+ * and a merge kernel combines them (about 129 KB per piece).  At most a few tens of MB.
+ */
+size_t pa_prefill_workspace_size(int q_len, int q_start, int causal, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size);
+
+/*
  * pa_prefill_chunk -- attention of a chunk of q_len query rows of ONE sequence over
  * that sequence's paged cache [page832 §6].  Row i sits at absolute position
  * q_start + i; with causal != 0 it sees keys 0..q_start+i (diagonal included),
@@ -237,12 +249,18 @@ int pa_decode_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v
  * (pa_slot_mapping + pa_reshape_and_cache first).
  *   q, out       BF16 [q_len, num_q_heads, head_dim], contiguous
  *   block_table  int32, the sequence's row: ceil((q_start + q_len) / block_size) entries
+ *   workspace    device scratch of workspace_bytes bytes, 256-byte aligned, or NULL (then
+ *                no item is split).  With at least pa_prefill_workspace_size(...) bytes
+ *                the call may split items (its contents on entry do not matter); with
+ *                less it runs as with NULL.  Calls that run at the same time need
+ *                separate workspaces.
  * Shapes accepted: 1 <= q_len, 0 <= q_start, q_start + q_len <= 2^31 - 1.
  */
 int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
                      int64_t page_stride, int64_t num_pages, const int32_t *block_table,
                      int q_len, int q_start, int causal, int num_q_heads, int num_kv_heads,
-                     int head_dim, int block_size, float scale, pa_bf16 *out, void *stream);
+                     int head_dim, int block_size, float scale, pa_bf16 *out, void *workspace,
+                     size_t workspace_bytes, void *stream);
 
 /*
  * pa_prefill_varlen -- pa_prefill_chunk for a mixed batch: the chunks of num_seqs
@@ -258,21 +276,28 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
  *                  >= ceil(seq_lens_k[b] / block_size) for every b
  *   cu_seqlens_q   int32 [num_seqs + 1], HOST, cu_seqlens_q[0] = 0, non-decreasing
  *   seq_lens_k     int32 [num_seqs], HOST, each >= its chunk's rows
+ *   workspace      as for pa_prefill_chunk, sized by pa_prefill_varlen_workspace_size
  * The lengths are host arrays because the library plans the work on the host (which
  * CTA runs which 128-row tile of which sequence and head).  Sequences with an empty chunk
  * are skipped; more than 32 non-empty chunks run as several launches, 32 chunks each,
  * one after another on the stream.  num_seqs == 0 or no rows at all is a no-op.
  */
+size_t pa_prefill_varlen_workspace_size(const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                                        int num_seqs, int causal, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size);
+
 int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
                       int64_t page_stride, int64_t num_pages, const int32_t *block_table,
                       int64_t bt_stride, const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
                       int num_seqs, int causal, int num_q_heads, int num_kv_heads, int head_dim,
-                      int block_size, float scale, pa_bf16 *out, void *stream);
+                      int block_size, float scale, pa_bf16 *out, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
- * pa_prefill_plan -- the static work assignment pa_prefill_chunk uses, for inspection.
- * The pages have no counterpart: it describes how this library spreads one chunk over
- * the GPU, not what the attention computes.  Host only; touches no device.
+ * pa_prefill_plan -- the static work assignment pa_prefill_chunk uses without a workspace
+ * (whole items only), for inspection.  The pages have no counterpart: it describes how
+ * this library spreads one chunk over the GPU, not what the attention computes.  Host
+ * only; touches no device.
  *
  * Work item i (0 <= i < ceil(q_len / 128) * num_q_heads) is the 128 query rows of tile
  * ceil(q_len / 128) - 1 - i / num_q_heads (the longest first) of head i % num_q_heads.
@@ -287,6 +312,23 @@ int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v
  */
 int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads, int block_size,
                     int num_ctas, int32_t *cta_of_item, int *num_items, int *max_cost);
+
+/*
+ * pa_prefill_plan_pieces -- the plan pa_prefill_chunk uses when given a workspace of
+ * pa_prefill_workspace_size bytes, for inspection (host only; the pages have no
+ * counterpart).  cta_of_item[i] (num_items entries) is the CTA that runs item i whole, or
+ * -1 for an item split into pieces: piece p covers 256-key tiles [piece_tile_begin[p],
+ * piece_tile_end[p]) of item piece_item[p] (items numbered as for pa_prefill_plan) and
+ * runs on CTA piece_cta[p].  *num_pieces is 0 when no split pays (the plan is then that
+ * of pa_prefill_plan); *max_cost is the busiest CTA's cost (tiles + 1 per whole item,
+ * tiles + 2 per piece).  Any array may be NULL; the piece arrays hold max_pieces entries
+ * (PA_ERR_INVALID_ARG if the plan has more pieces).
+ */
+int pa_prefill_plan_pieces(int q_len, int q_start, int causal, int num_q_heads,
+                           int block_size, int num_ctas, int max_pieces, int32_t *cta_of_item,
+                           int32_t *piece_item, int32_t *piece_tile_begin,
+                           int32_t *piece_tile_end, int32_t *piece_cta, int *num_items,
+                           int *num_pieces, int *max_cost);
 
 /*
  * pa_copy -- copies `bytes` bytes from src to dst with a kernel on `stream` (ordered like

@@ -12,8 +12,10 @@ Functions (names follow the C ABI):
                                                                       -> step inputs
     reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)     (in place)
     decode_workspace_size(...), decode(q, k_cache, v_cache, block_table, seq_lens, ...)
-    prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale)
-    prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, causal, scale)
+    prefill_workspace_size(...), prefill_chunk(q, k_cache, v_cache, block_table, q_start,
+                                               causal, scale, workspace=None)
+    prefill_varlen_workspace_size(...), prefill_varlen(q, k_cache, v_cache, block_table,
+                                               cu_seqlens_q, seq_lens_k, causal, scale)
     prefill_plan(q_len, q_start, causal, num_q_heads, block_size, num_ctas)  (host only)
     device_errors(clear=True)
 """
@@ -29,7 +31,8 @@ from . import _build
 
 __all__ = ["load", "build", "slot_mapping", "decode_input_prep", "reshape_and_cache",
            "decode_workspace_size",
-           "decode", "decode_append", "prefill_chunk", "prefill_varlen", "prefill_plan", "device_errors", "set_kernel_events", "build_info", "PAError",
+           "decode", "decode_append", "prefill_chunk", "prefill_varlen", "prefill_plan",
+           "prefill_workspace_size", "prefill_varlen_workspace_size", "prefill_plan_pieces", "device_errors", "set_kernel_events", "build_info", "PAError",
            "DEVERR_PAGE", "DEVERR_SEQLEN", "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_POSITION", "DEVERR_LAYOUT",
            "LIB_PATH"]
 
@@ -74,11 +77,15 @@ def load():
                            sz, P, P, P, P], i32),
             "pa_decode_append": ([P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32,
                                   P, P, sz, P, P, P, P], i32),
+            "pa_prefill_workspace_size": ([i32, i32, i32, i32, i32, i32, i32], sz),
             "pa_prefill_chunk": ([P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32, f32,
-                                  P, P], i32),
+                                  P, P, sz, P], i32),
+            "pa_prefill_varlen_workspace_size": ([P, P, i32, i32, i32, i32, i32, i32], sz),
             "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, P, P, P], i32),
+            "pa_prefill_plan_pieces": ([i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P,
+                                        P], i32),
             "pa_prefill_varlen": ([P, P, P, i64, i64, P, i64, P, P, i32, i32, i32, i32, i32,
-                                   i32, f32, P, P], i32),
+                                   i32, f32, P, P, sz, P], i32),
             "pa_copy": ([P, P, sz, P], i32),
             "pa_get_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32, P], i32),
             "pa_set_kernel_events": ([P, P], i32),
@@ -305,8 +312,29 @@ def decode_append(q, k_cache, v_cache, block_table, seq_lens, scale, max_seq_len
     return out
 
 
-def prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale, out=None):
-    """Causal (or full) chunk attention of one sequence (see pa_prefill_chunk)."""
+def prefill_workspace_size(q_len, q_start, causal, num_q_heads, num_kv_heads, head_dim,
+                           block_size):
+    """Bytes of workspace with which pa_prefill_chunk may split items (0: none would pay)."""
+    return int(load().pa_prefill_workspace_size(int(q_len), int(q_start), int(bool(causal)),
+                                                num_q_heads, num_kv_heads, head_dim,
+                                                block_size))
+
+
+def _workspace_arg(workspace, need, device):
+    """(pointer, bytes) of a caller's workspace, or of a fresh one of `need` bytes."""
+    if workspace is None:
+        if need == 0:
+            return None, 0
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale, out=None,
+                  workspace=None):
+    """Causal (or full) chunk attention of one sequence (see pa_prefill_chunk).  Without a
+    workspace, one of pa_prefill_workspace_size bytes is allocated for the call."""
     lib = load()
     _check(q, "q", torch.bfloat16, 3)
     _check(block_table, "block_table", torch.int32)
@@ -317,16 +345,32 @@ def prefill_chunk(q, k_cache, v_cache, block_table, q_start, causal, scale, out=
     _, bs, hkv, _ = k_cache.shape
     if out is None:
         out = torch.empty_like(q)
+    if workspace is None:
+        need = prefill_workspace_size(q_len, q_start, causal, hq, hkv, d, bs)
+    ws, ws_bytes = _workspace_arg(workspace, need if workspace is None else 0, q.device)
     _raise(lib.pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
                                 _ptr(bt), q_len, int(q_start), int(bool(causal)), hq, hkv, d,
-                                bs, float(scale), _ptr(out), _stream()), "pa_prefill_chunk")
+                                bs, float(scale), _ptr(out), _ptr(ws), ws_bytes, _stream()),
+           "pa_prefill_chunk")
     return out
 
 
+def prefill_varlen_workspace_size(cu_seqlens_q, seq_lens_k, causal, num_q_heads, num_kv_heads,
+                                  head_dim, block_size):
+    """Bytes of workspace with which pa_prefill_varlen may split items."""
+    B = len(seq_lens_k)
+    cu = (ctypes.c_int32 * (B + 1))(*[int(x) for x in cu_seqlens_q])
+    sk = (ctypes.c_int32 * max(B, 1))(*[int(x) for x in seq_lens_k])
+    return int(load().pa_prefill_varlen_workspace_size(cu, sk, B, int(bool(causal)),
+                                                       num_q_heads, num_kv_heads, head_dim,
+                                                       block_size))
+
+
 def prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, causal, scale,
-                   out=None):
+                   out=None, workspace=None):
     """Chunks of several sequences stacked row-wise in q (see pa_prefill_varlen).
-    cu_seqlens_q and seq_lens_k are host sequences of ints (lists or arrays)."""
+    cu_seqlens_q and seq_lens_k are host sequences of ints (lists or arrays).  Without a
+    workspace, one of pa_prefill_varlen_workspace_size bytes is allocated for the call."""
     lib = load()
     _check(q, "q", torch.bfloat16, 3)
     _check(block_table, "block_table", torch.int32, 2)
@@ -343,10 +387,15 @@ def prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, c
     _, bs, hkv, _ = k_cache.shape
     if out is None:
         out = torch.empty_like(q)
+    need = 0
+    if workspace is None:
+        need = int(lib.pa_prefill_varlen_workspace_size(cu, sk, B, int(bool(causal)), hq, hkv,
+                                                        d, bs))
+    ws, ws_bytes = _workspace_arg(workspace, need, q.device)
     _raise(lib.pa_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), ps, k_cache.shape[0],
                                  _ptr(block_table), block_table.stride(0), cu, sk, B,
                                  int(bool(causal)), hq, hkv, d, bs, float(scale), _ptr(out),
-                                 _stream()), "pa_prefill_varlen")
+                                 _ptr(ws), ws_bytes, _stream()), "pa_prefill_varlen")
     return out
 
 
@@ -364,6 +413,23 @@ def prefill_plan(q_len, q_start, causal, num_q_heads, block_size, num_ctas):
            "pa_prefill_plan")
     return list(cta), mc.value
 
+
+
+def prefill_plan_pieces(q_len, q_start, causal, num_q_heads, block_size, num_ctas,
+                        max_pieces=480):
+    """The plan used with a workspace (host only, see pa_prefill_plan_pieces): returns
+    (cta_of_item with -1 for split items, [(item, tile_begin, tile_end, cta), ...], max_cost)."""
+    lib = load()
+    ni, npc, mc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    nqt = -(-int(q_len) // 128)
+    items = (ctypes.c_int32 * (nqt * num_q_heads))()
+    arrs = [(ctypes.c_int32 * max(1, max_pieces))() for _ in range(4)]
+    _raise(lib.pa_prefill_plan_pieces(int(q_len), int(q_start), int(bool(causal)), num_q_heads,
+                                      block_size, num_ctas, max_pieces, items, *arrs,
+                                      ctypes.byref(ni), ctypes.byref(npc), ctypes.byref(mc)),
+           "pa_prefill_plan_pieces")
+    pieces = [(arrs[0][p], arrs[1][p], arrs[2][p], arrs[3][p]) for p in range(npc.value)]
+    return list(items)[:ni.value], pieces, mc.value
 
 def set_kernel_events(start, stop):
     """Measurement hook: the next decode / prefill_chunk call records these

@@ -463,14 +463,34 @@ int pa_decode_append(const pa_bf16 *q, pa_bf16 *k_cache, pa_bf16 *v_cache, int64
                        nullptr, slot_mapping, stream);
 }
 
+// The schedule of one prefill launch over nseq chunks: with split items when the
+// workspace (workspace_bytes; 0 for none) holds their pieces' partials.
+static bool prefill_schedule(const pa::PrefillSeq *seqs, int nseq, int causal, int num_q_heads,
+                             int block_size, int num_sms, size_t workspace_bytes,
+                             pa::PrefillSchedule *sched) {
+    int q_lens[pa::kPfMaxSeqs], q_starts[pa::kPfMaxSeqs];
+    for (int b = 0; b < nseq; ++b) {
+        q_lens[b] = seqs[b].q_len;
+        q_starts[b] = seqs[b].q_start;
+    }
+    if (workspace_bytes >= pa::kPfSlotBytes &&
+        pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads, block_size, num_sms, true,
+                         sched, nullptr) &&
+        (size_t)sched->num_pieces * pa::kPfSlotBytes <= workspace_bytes)
+        return true;
+    return pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads, block_size, num_sms,
+                            false, sched, nullptr);
+}
+
 // One prefill launch over 1 .. kPfMaxSeqs chunks whose rows lie in q / out of total_q rows.
 static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
                           const pa_bf16 *v_cache, int64_t page_stride, int64_t num_pages,
                           const int32_t *block_table, int64_t bt_stride,
                           const pa::PrefillSeq *seqs, int nseq, int causal, int num_q_heads,
                           int num_kv_heads, int head_dim, int block_size, float scale,
-                          pa_bf16 *out, const DeviceInfo &dev, cudaEvent_t ev_start,
-                          cudaEvent_t ev_stop, cudaStream_t stream) {
+                          pa_bf16 *out, void *workspace, size_t workspace_bytes,
+                          const DeviceInfo &dev, cudaEvent_t ev_start, cudaEvent_t ev_stop,
+                          cudaStream_t stream) {
     CUtensorMap maps[3 + 2 * pa::kPfMaxSeqs];
     if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, total_q, pa::kPfQRows) ||
         !make_cache_map(&maps[1], k_cache, head_dim, num_kv_heads, block_size, num_pages,
@@ -478,7 +498,6 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
         !make_cache_map(&maps[2], v_cache, head_dim, num_kv_heads, block_size, num_pages,
                         page_stride, pa::kPfBlock))
         return PA_ERR_CUDA;
-    int q_lens[pa::kPfMaxSeqs], q_starts[pa::kPfMaxSeqs];
     for (int b = 0; b < nseq; ++b) {
         // The sequence's last page is read through maps whose rows end at its last token,
         // so rows past it come back as zeros.
@@ -489,16 +508,15 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
             !make_cache_map(&maps[4 + 2 * b], v_cache, head_dim, num_kv_heads, last_rows,
                             num_pages, page_stride, pa::kPfBlock))
             return PA_ERR_CUDA;
-        q_lens[b] = seqs[b].q_len;
-        q_starts[b] = seqs[b].q_start;
     }
     // The static work assignment (cached per shape); problems too large for its arrays
     // run without one.
     static thread_local pa::PrefillSchedule sched;
-    const bool planned = pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads,
-                                          block_size, dev.num_sms, &sched, nullptr);
+    const bool planned = prefill_schedule(seqs, nseq, causal, num_q_heads, block_size,
+                                          dev.num_sms, workspace ? workspace_bytes : 0, &sched);
     pa::PrefillArgs a;
     a.sched = planned ? &sched : nullptr;
+    a.workspace = workspace;
     a.block_table = block_table;
     a.bt_stride = bt_stride;
     a.num_seqs = nseq;
@@ -521,11 +539,29 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
     return pa::launch_prefill(maps, a, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+size_t pa_prefill_workspace_size(int q_len, int q_start, int causal, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size) {
+    if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > 0x7fffffffLL ||
+        num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads ||
+        head_dim != pa::kHeadDim || block_size < 1)
+        return 0;
+    DeviceInfo dev;
+    if (device_info(&dev)) return 0;
+    const pa::PrefillSeq seq{0, q_len, q_start, 0};
+    static thread_local pa::PrefillSchedule sched;
+    if (!prefill_schedule(&seq, 1, causal ? 1 : 0, num_q_heads, block_size, dev.num_sms,
+                          (size_t)pa::kPfMaxPieces * pa::kPfSlotBytes, &sched))
+        return 0;
+    return (size_t)sched.num_pieces * pa::kPfSlotBytes;
+}
+
 int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
                      int64_t page_stride, int64_t num_pages, const int32_t *block_table,
                      int q_len, int q_start, int causal, int num_q_heads, int num_kv_heads,
-                     int head_dim, int block_size, float scale, pa_bf16 *out, void *stream) {
+                     int head_dim, int block_size, float scale, pa_bf16 *out, void *workspace,
+                     size_t workspace_bytes, void *stream) {
     if (!q || !k_cache || !v_cache || !block_table || !out) return PA_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_INVALID_ARG;
     if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > 0x7fffffffLL)
         return PA_ERR_INVALID_ARG;
     if (int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
@@ -541,15 +577,53 @@ int pa_prefill_chunk(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_
     const pa::PrefillSeq seq{0, q_len, q_start, 0};
     return prefill_launch(q, q_len, k_cache, v_cache, page_stride, num_pages, block_table, 0,
                           &seq, 1, causal ? 1 : 0, num_q_heads, num_kv_heads, head_dim,
-                          block_size, scale, out, dev, e0, e1, static_cast<cudaStream_t>(stream));
+                          block_size, scale, out, workspace, workspace ? workspace_bytes : 0, dev,
+                          e0, e1, static_cast<cudaStream_t>(stream));
+}
+
+// The non-empty chunks of a mixed batch, in launch order; false for bad lengths.
+static bool varlen_chunks(const int32_t *cu_seqlens_q, const int32_t *seq_lens_k, int num_seqs,
+                          std::vector<pa::PrefillSeq> *seqs) {
+    if (num_seqs < 0 || !cu_seqlens_q || (num_seqs > 0 && !seq_lens_k) || cu_seqlens_q[0] != 0)
+        return false;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int64_t ql = (int64_t)cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        if (ql < 0 || seq_lens_k[b] < 0 || ql > seq_lens_k[b]) return false;
+        if (ql > 0) seqs->push_back(pa::PrefillSeq{cu_seqlens_q[b], (int)ql, seq_lens_k[b] - (int)ql, b});
+    }
+    return true;
+}
+
+size_t pa_prefill_varlen_workspace_size(const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                                        int num_seqs, int causal, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size) {
+    std::vector<pa::PrefillSeq> seqs;
+    if (!varlen_chunks(cu_seqlens_q, seq_lens_k, num_seqs, &seqs) || num_q_heads < 1 ||
+        num_kv_heads < 1 || num_q_heads % num_kv_heads || head_dim != pa::kHeadDim ||
+        block_size < 1)
+        return 0;
+    DeviceInfo dev;
+    if (device_info(&dev)) return 0;
+    static thread_local pa::PrefillSchedule sched;
+    size_t need = 0;
+    const int n = (int)seqs.size();
+    for (int s0 = 0; s0 < n; s0 += pa::kPfMaxSeqs) {
+        const int cnt = std::min(pa::kPfMaxSeqs, n - s0);
+        if (prefill_schedule(&seqs[s0], cnt, causal ? 1 : 0, num_q_heads, block_size,
+                             dev.num_sms, (size_t)pa::kPfMaxPieces * pa::kPfSlotBytes, &sched))
+            need = std::max(need, (size_t)sched.num_pieces * pa::kPfSlotBytes);
+    }
+    return need;
 }
 
 int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
                       int64_t page_stride, int64_t num_pages, const int32_t *block_table,
                       int64_t bt_stride, const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
                       int num_seqs, int causal, int num_q_heads, int num_kv_heads, int head_dim,
-                      int block_size, float scale, pa_bf16 *out, void *stream) {
+                      int block_size, float scale, pa_bf16 *out, void *workspace,
+                      size_t workspace_bytes, void *stream) {
     if (num_seqs < 0 || !cu_seqlens_q || (num_seqs > 0 && !seq_lens_k)) return PA_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_INVALID_ARG;
     if (cu_seqlens_q[0] != 0) return PA_ERR_INVALID_ARG;
     int64_t max_pages = 0;
     for (int b = 0; b < num_seqs; ++b) {
@@ -573,19 +647,18 @@ int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v
     cudaEvent_t e0, e1;
     take_kernel_events(&e0, &e1);
     // The non-empty chunks, kPfMaxSeqs per launch (each launch spreads its chunks over all
-    // SMs; the launches run back to back on the stream).
+    // SMs; the launches run back to back on the stream, and a later one reuses the
+    // workspace only after the one before has been merged).
     std::vector<pa::PrefillSeq> seqs;
-    for (int b = 0; b < num_seqs; ++b) {
-        const int ql = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-        if (ql > 0) seqs.push_back(pa::PrefillSeq{cu_seqlens_q[b], ql, seq_lens_k[b] - ql, b});
-    }
+    varlen_chunks(cu_seqlens_q, seq_lens_k, num_seqs, &seqs);
     const int n = (int)seqs.size();
     for (int s0 = 0; s0 < n; s0 += pa::kPfMaxSeqs) {
         const int cnt = std::min(pa::kPfMaxSeqs, n - s0);
         if (int rc = prefill_launch(q, total_q, k_cache, v_cache, page_stride, num_pages,
                                     block_table, bt_stride, &seqs[s0], cnt, causal ? 1 : 0,
                                     num_q_heads, num_kv_heads, head_dim, block_size, scale, out,
-                                    dev, s0 == 0 ? e0 : nullptr,
+                                    workspace, workspace ? workspace_bytes : 0, dev,
+                                    s0 == 0 ? e0 : nullptr,
                                     s0 + cnt == n ? e1 : nullptr,
                                     static_cast<cudaStream_t>(stream)))
             return rc;

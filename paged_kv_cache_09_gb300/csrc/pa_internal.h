@@ -169,21 +169,48 @@ __host__ __device__ inline int prefill_item_tiles(int q_len, int q_start, int ca
 
 // Static assignment of prefill work items to the persistent CTAs.  Item index i stands
 // for query tile (num_q_tiles - 1 - i / Hq) of head i % Hq (the longest items first).
+// When a workspace is given and the items do not divide evenly over the CTAs, some
+// items are split along the keys into pieces (ranges of their 256-key tiles) that run on
+// different CTAs; each piece writes an unnormalised partial (fp32 O rows, and per row
+// the running max and the sum of weights) into its workspace slot, and a merge kernel
+// combines an item's pieces afterwards.
 constexpr int kPfSchedMaxCtas = 256;
-constexpr int kPfSchedMaxItems = 6144;
+constexpr int kPfSchedMaxItems = 6144;     // schedule entries (whole items and pieces)
+constexpr int kPfMaxPieces = 480;          // pieces of split items
+constexpr int kPfMaxSplitItems = 160;      // split items
+constexpr uint16_t kPfPieceBit = 0x8000;   // schedule entry kPfPieceBit | p: piece p
+constexpr int kPfMinPieceTiles = 4;        // no piece is shorter
+
+struct PrefillPiece {
+    uint16_t item;                  // the split item
+    uint16_t tile_begin, tile_end;  // its 256-key tiles [tile_begin, tile_end)
+    uint16_t slot;                  // its partial's workspace slot
+};
+
 struct PrefillSchedule {
     int num_ctas;                        // 0: none (the kernel walks a snake order)
+    int num_pieces, num_split;           // pieces, and the items they split
     uint16_t off[kPfSchedMaxCtas + 1];   // CTA b runs items[off[b] .. off[b+1]) in order
-    uint16_t items[kPfSchedMaxItems];
+    uint16_t items[kPfSchedMaxItems];    // an item index, or kPfPieceBit | piece index
+    PrefillPiece pieces[kPfMaxPieces];
+    // Split item s: item split_item[s], whose pieces own slots split_slot0[s] .. + split_n[s].
+    uint16_t split_item[kPfMaxSplitItems], split_slot0[kPfMaxSplitItems],
+        split_n[kPfMaxSplitItems];
 };
+
+// Bytes of one piece's partial in the prefill workspace: 128 rows x 256 fp32 O values,
+// plus a (running max, sum of weights) pair per row.
+constexpr size_t kPfSlotBytes = (size_t)kPfQRows * 256 * 4 + (size_t)kPfQRows * 8;  // head dim 256
 
 // Plans the schedule (cached per shape) for one launch over num_seqs chunks (chunk b:
 // q_lens[b] rows at positions q_starts[b]..; work items numbered sequence by sequence,
 // each sequence's longest query tile first); false when the problem exceeds the arrays.
-// max_cost (optional): the largest per-CTA cost, in tiles plus one per item.
+// allow_split: items may be split into pieces (the launch has a workspace of
+// s->num_pieces * kPfSlotBytes bytes).  max_cost (optional): the largest per-CTA cost, in
+// tiles plus one per item (two per piece).
 bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int causal,
-                  int num_q_heads, int block_size, int num_ctas, PrefillSchedule *s,
-                  int *max_cost);
+                  int num_q_heads, int block_size, int num_ctas, bool allow_split,
+                  PrefillSchedule *s, int *max_cost);
 
 // Sequences one prefill launch takes (their chunks' tensor maps travel in the launch's
 // parameters); a larger batch is split into several launches.
@@ -198,6 +225,7 @@ struct PrefillSeq {
 
 struct PrefillArgs {
     const PrefillSchedule *sched;  // host copy, passed to the kernel by value (or NULL)
+    void *workspace;               // piece partials (sched->num_pieces slots), or NULL
     const int32_t *block_table;    // [num_seqs, bt_stride]: row b for sequence b
     int64_t bt_stride;
     int num_seqs;                  // 1 .. kPfMaxSeqs

@@ -11,8 +11,18 @@
 //   3. local search: while some move of one item off the most loaded CTA, or swap of one
 //      of its items with a cheaper item of another CTA, lowers that CTA's cost without
 //      raising the other one's to the same level, apply the best such change.
-// Each CTA then runs its items longest first.  Plans are cached per shape, since a
-// serving loop prefills chunks of the same few shapes over and over.
+// Whole items cannot always be balanced: the q=1685 tail chunk has 336 items of ~52
+// tiles for 152 CTAs, so some CTAs run three items and most two (149 tiles against a
+// mean of 114), and a short chunk over a long context has fewer items than CTAs.  When
+// the caller provides a workspace, a second plan may split items along the keys:
+//   4. with a target T (the mean cost rounded up, then raised step by step until the
+//      plan fits), items go by decreasing cost to the least loaded CTA while that stays
+//      within T; an item that does not fit is cut into pieces of at least
+//      kPfMinPieceTiles tiles that fill the least loaded CTAs up to T (a piece costs its
+//      tiles + 2: its Q load, its epilogue and the partial it writes).
+// The split plan is taken when its busiest CTA is at least 3% cheaper.  Each CTA then
+// runs its items and pieces longest first.  Plans are cached per shape, since a serving
+// loop prefills chunks of the same few shapes over and over.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -29,9 +39,10 @@ namespace {
 struct PlanKey {
     std::vector<std::pair<int, int>> chunks;  // (q_len, q_start) of each sequence
     int causal, hq, bs, ctas;
+    bool allow_split;
     bool operator==(const PlanKey &o) const {
         return chunks == o.chunks && causal == o.causal && hq == o.hq && bs == o.bs &&
-               ctas == o.ctas;
+               ctas == o.ctas && allow_split == o.allow_split;
     }
 };
 
@@ -39,7 +50,105 @@ struct CachedPlan {
     PlanKey key;
     int max_cost;
     std::vector<uint16_t> off, items;
+    std::vector<PrefillPiece> pieces;
+    std::vector<uint16_t> split_item, split_slot0, split_n;
 };
+
+// A CTA's list: whole items (index) and pieces (kPfPieceBit | piece), with their costs.
+struct Entry {
+    uint16_t code;
+    int cost;
+};
+
+// Fills out.off / out.items from per-CTA lists, each run longest first.
+void emit(std::vector<std::vector<Entry>> &bins, CachedPlan &out) {
+    const int G = (int)bins.size();
+    out.off.assign(G + 1, 0);
+    out.items.clear();
+    int mx = 0;
+    for (int b = 0; b < G; ++b) {
+        std::stable_sort(bins[b].begin(), bins[b].end(), [](const Entry &x, const Entry &y) {
+            return x.cost != y.cost ? x.cost > y.cost : x.code < y.code;
+        });
+        int load = 0;
+        for (const Entry &e : bins[b]) {
+            out.items.push_back(e.code);
+            load += e.cost;
+        }
+        mx = std::max(mx, load);
+        out.off[b + 1] = (uint16_t)out.items.size();
+    }
+    out.max_cost = mx;
+}
+
+// Plan 4 of the header: whole items while they fit under the target, pieces otherwise.
+// Returns false when no target up to the largest whole-item plan gives a plan within
+// the schedule's limits.
+bool split_plan(const std::vector<int> &tiles, int G, int limit, CachedPlan &out) {
+    const int n = (int)tiles.size();
+    long long total = 0;
+    for (int t : tiles) total += t + 1;
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return tiles[a] > tiles[b]; });
+    using Slot = std::pair<long long, int>;
+    for (long long target = (total + G - 1) / G; target < limit; ++target) {
+        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+        for (int b = 0; b < G; ++b) heap.push({0, b});
+        std::vector<std::vector<Entry>> bins(G);
+        std::vector<long long> load(G, 0);
+        std::vector<PrefillPiece> pieces;
+        std::vector<uint16_t> si, s0, sn;
+        bool ok = true;
+        for (int i : order) {
+            const int t = tiles[i];
+            const int b0 = heap.top().second;
+            if (load[b0] + t + 1 <= target) {
+                heap.pop();
+                bins[b0].push_back({(uint16_t)i, t + 1});
+                load[b0] += t + 1;
+                heap.push({load[b0], b0});
+                continue;
+            }
+            // Cut the item into pieces that fill the least loaded CTAs up to the target.
+            si.push_back((uint16_t)i);
+            s0.push_back((uint16_t)pieces.size());
+            int begin = 0;
+            std::vector<int> used;
+            while (begin < t) {
+                if (heap.empty()) { ok = false; break; }
+                const int b = heap.top().second;
+                heap.pop();
+                used.push_back(b);
+                int take = (int)std::min<long long>(t - begin, target - load[b] - 2);
+                if (t - begin - take > 0 && t - begin - take < kPfMinPieceTiles)
+                    take = t - begin - kPfMinPieceTiles;
+                if (take < kPfMinPieceTiles) { ok = false; break; }
+                if ((int)pieces.size() == kPfMaxPieces) { ok = false; break; }
+                const uint16_t code = (uint16_t)(kPfPieceBit | pieces.size());
+                pieces.push_back({(uint16_t)i, (uint16_t)begin, (uint16_t)(begin + take),
+                                  (uint16_t)pieces.size()});
+                bins[b].push_back({code, take + 2});
+                load[b] += take + 2;
+                begin += take;
+            }
+            for (int b : used) heap.push({load[b], b});
+            sn.push_back((uint16_t)(pieces.size() - s0.back()));
+            if (!ok || (int)si.size() > kPfMaxSplitItems) { ok = false; break; }
+        }
+        if (!ok) continue;
+        long long entries = 0;
+        for (auto &bn : bins) entries += (long long)bn.size();
+        if (entries > kPfSchedMaxItems) return false;
+        emit(bins, out);
+        out.pieces = std::move(pieces);
+        out.split_item = std::move(si);
+        out.split_slot0 = std::move(s0);
+        out.split_n = std::move(sn);
+        return true;
+    }
+    return false;
+}
 
 constexpr int kPlanCacheSize = 8;
 std::mutex g_plan_mu;
@@ -117,27 +226,35 @@ void compute_plan(const PlanKey &k, CachedPlan &out) {
         load[bj] += cost[a];
     }
     out.key = k;
-    out.max_cost = (int)*std::max_element(load.begin(), load.end());
-    out.off.assign(G + 1, 0);
-    out.items.clear();
-    out.items.reserve(n);
-    for (int b = 0; b < G; ++b) {
-        std::stable_sort(bins[b].begin(), bins[b].end(), [&](int x, int y) {
-            return cost[x] != cost[y] ? cost[x] > cost[y] : x < y;
-        });
-        for (int x : bins[b]) out.items.push_back((uint16_t)x);
-        out.off[b + 1] = (uint16_t)out.items.size();
+    std::vector<std::vector<Entry>> entries(G);
+    for (int b = 0; b < G; ++b)
+        for (int x : bins[b]) entries[b].push_back({(uint16_t)x, cost[x]});
+    emit(entries, out);
+    out.pieces.clear();
+    out.split_item.clear();
+    out.split_slot0.clear();
+    out.split_n.clear();
+    // 4. The split plan, if allowed and at least 3% better.
+    if (k.allow_split) {
+        std::vector<int> tiles(n);
+        for (int i = 0; i < n; ++i) tiles[i] = cost[i] - 1;
+        CachedPlan alt;
+        if (split_plan(tiles, k.ctas, out.max_cost, alt) &&
+            alt.max_cost * 100 <= out.max_cost * 97 && !alt.pieces.empty()) {
+            alt.key = k;
+            out = std::move(alt);
+        }
     }
 }
 
 }  // namespace
 
 bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int causal,
-                  int num_q_heads, int block_size, int num_ctas, PrefillSchedule *s,
-                  int *max_cost) {
+                  int num_q_heads, int block_size, int num_ctas, bool allow_split,
+                  PrefillSchedule *s, int *max_cost) {
     if (num_seqs < 1 || num_q_heads < 1 || block_size < 1 || num_ctas < 1) return false;
     long long n = 0;
-    PlanKey key{{}, causal ? 1 : 0, num_q_heads, block_size, num_ctas};
+    PlanKey key{{}, causal ? 1 : 0, num_q_heads, block_size, num_ctas, allow_split};
     for (int b = 0; b < num_seqs; ++b) {
         if (q_lens[b] < 1 || q_starts[b] < 0) return false;
         n += (long long)((q_lens[b] + kPfQRows - 1) / kPfQRows) * num_q_heads;
@@ -163,6 +280,15 @@ bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int caus
         s->num_ctas = G;
         std::memcpy(s->off, it->off.data(), (G + 1) * sizeof(uint16_t));
         std::memcpy(s->items, it->items.data(), it->items.size() * sizeof(uint16_t));
+        s->num_pieces = (int)it->pieces.size();
+        s->num_split = (int)it->split_item.size();
+        if (s->num_pieces)
+            std::memcpy(s->pieces, it->pieces.data(), s->num_pieces * sizeof(PrefillPiece));
+        for (int x = 0; x < s->num_split; ++x) {
+            s->split_item[x] = it->split_item[x];
+            s->split_slot0[x] = it->split_slot0[x];
+            s->split_n[x] = it->split_n[x];
+        }
     }
     if (max_cost) *max_cost = it->max_cost;
     return true;
@@ -178,8 +304,8 @@ extern "C" int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_hea
         return PA_ERR_INVALID_ARG;
     static thread_local pa::PrefillSchedule s;
     int mc = 0;
-    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, block_size, num_ctas, &s,
-                          &mc))
+    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, block_size, num_ctas, false,
+                          &s, &mc))
         return PA_ERR_UNSUPPORTED;
     const int n = s.off[s.num_ctas];
     if (num_items) *num_items = n;
@@ -187,5 +313,41 @@ extern "C" int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_hea
     if (cta_of_item)
         for (int b = 0; b < s.num_ctas; ++b)
             for (int x = s.off[b]; x < s.off[b + 1]; ++x) cta_of_item[s.items[x]] = b;
+    return PA_OK;
+}
+
+extern "C" int pa_prefill_plan_pieces(int q_len, int q_start, int causal, int num_q_heads,
+                                      int block_size, int num_ctas, int max_pieces,
+                                      int32_t *cta_of_item, int32_t *piece_item,
+                                      int32_t *piece_tile_begin, int32_t *piece_tile_end,
+                                      int32_t *piece_cta, int *num_items, int *num_pieces,
+                                      int *max_cost) {
+    if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > INT32_MAX || num_q_heads < 1 ||
+        block_size < 1 || num_ctas < 1 || max_pieces < 0)
+        return PA_ERR_INVALID_ARG;
+    static thread_local pa::PrefillSchedule s;
+    int mc = 0;
+    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, block_size, num_ctas, true,
+                          &s, &mc))
+        return PA_ERR_UNSUPPORTED;
+    const int items = ((q_len + pa::kPfQRows - 1) / pa::kPfQRows) * num_q_heads;
+    if (num_items) *num_items = items;
+    if (num_pieces) *num_pieces = s.num_pieces;
+    if (max_cost) *max_cost = mc;
+    if (s.num_pieces > max_pieces) return PA_ERR_INVALID_ARG;
+    if (cta_of_item)
+        for (int i = 0; i < items; ++i) cta_of_item[i] = -1;
+    for (int b = 0; b < s.num_ctas; ++b)
+        for (int x = s.off[b]; x < s.off[b + 1]; ++x) {
+            if (!(s.items[x] & pa::kPfPieceBit)) {
+                if (cta_of_item) cta_of_item[s.items[x]] = b;
+                continue;
+            }
+            const int pc = s.items[x] & ~pa::kPfPieceBit;
+            if (piece_item) piece_item[pc] = s.pieces[pc].item;
+            if (piece_tile_begin) piece_tile_begin[pc] = s.pieces[pc].tile_begin;
+            if (piece_tile_end) piece_tile_end[pc] = s.pieces[pc].tile_end;
+            if (piece_cta) piece_cta[pc] = b;
+        }
     return PA_OK;
 }

@@ -115,6 +115,8 @@ struct TcParams {
     int neg;              // scale < 0
     uint16_t *out;
     unsigned *err;
+    float *ws_o;    // piece partials: O [slot][128 rows][256] (only with split items)
+    float2 *ws_ml;  // piece partials: (running max, sum of weights) [slot][128 rows]
     SeqInfo seq[kSeqs];
     PrefillSchedule sched;  // static item -> CTA assignment (num_ctas 0: snake order)
 };
@@ -125,19 +127,30 @@ struct TcMaps {
     CUtensorMap k_last[kSeqs], v_last[kSeqs];  // cut at each sequence's last token
 };
 
+static_assert(sizeof(TcMaps<kPfMaxSeqs>) + sizeof(TcParams<kPfMaxSeqs>) <= 32764,
+              "the kernel's parameters fit the 32 KB parameter space");
+
 struct Item {
     int h, g, r0, rows, nblocks, n;  // head, KV head, first row, rows present, blocks, tiles
     int b, q_off, q_start, seq_len_k, last_page, bt_row;  // its sequence
+    // The tiles [jb, je) this CTA runs: all n of a whole item, or one piece's range; a
+    // piece writes its partial to workspace slot `slot` (-1: a whole item, normalised
+    // output stored to out).
+    int jb, je, slot;
 };
 
 template <int kSeqs>
 __device__ __forceinline__ bool item_of(const TcParams<kSeqs> &p, int k, Item &it) {
     const int G = gridDim.x, b = blockIdx.x;
-    int idx;
+    int idx, piece = -1;
     if (p.sched.num_ctas) {
         const int x = p.sched.off[b] + k;
         if (x >= p.sched.off[b + 1]) return false;
         idx = p.sched.items[x];
+        if (idx & kPfPieceBit) {
+            piece = idx & ~kPfPieceBit;
+            idx = p.sched.pieces[piece].item;
+        }
     } else {
         idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
         if (idx >= p.num_items) return false;
@@ -162,6 +175,15 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs> &p, int k, Item &i
     const int rem = nkeys - full * p.block_size;
     it.nblocks = full * p.blocks_per_page + (rem + kBlk - 1) / kBlk;
     it.n = (it.nblocks + 3) / 4;
+    if (piece < 0) {
+        it.jb = 0;
+        it.je = it.n;
+        it.slot = -1;
+    } else {
+        it.jb = p.sched.pieces[piece].tile_begin;
+        it.je = p.sched.pieces[piece].tile_end;
+        it.slot = p.sched.pieces[piece].slot;
+    }
     return true;
 }
 
@@ -252,9 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 it.q_off + it.r0);
                 const int32_t *bt = p.block_table + (int64_t)it.bt_row * p.bt_stride;
                 // Page and in-page index of block kb, advanced block by block: a division
-                // here would take the MUFU, which the softmax warps keep busy.
-                int blk_lp = 0, blk_in = 0;
-                for (int j = 0; j < it.n && !stop; ++j) {
+                // per block would take the MUFU, which the softmax warps keep busy (one
+                // per item places the first block of a piece).
+                int blk_lp = (4 * it.jb) / p.blocks_per_page;
+                int blk_in = 4 * it.jb - blk_lp * p.blocks_per_page;
+                for (int j = it.jb; j < it.je && !stop; ++j) {
                     // Page, offset and map of each of the tile's four blocks; blocks past the
                     // item's last are read from outside the pool (zeros) and masked.
                     int pg[4], of[4];
@@ -331,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; !stop && item_of(p, k, it); ++k) {
                 if (!mbar_wait_abort(&bars[kQFull], k & 1, p.err, abort)) break;
                 tc_fence_after();
-                for (int j = 0; j < it.n && !stop; ++j) {
+                for (int j = it.jb; j < it.je && !stop; ++j) {
+                    const uint32_t jr = (uint32_t)(j - it.jb);  // tile of this item or piece
                     // S = Q K^T over the tile's 256 keys.
                     for (int c = 0; c < kChunks; ++c, ++u) {
                         const int s = u % kRing;
@@ -348,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_commit(&bars[kRingEmpty + s]);
                     }
                     if (stop) break;
-                    if (j == it.n - 1) umma_commit(&bars[kQEmpty]);
+                    if (j == it.je - 1) umma_commit(&bars[kQEmpty]);
                     umma_commit(&bars[kSFull]);
                     // O += P V, one 64-key quarter (one V unit) at a time.  The V unit and
                     // the O buffer are usually ready long before P: their waits (each
@@ -361,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             stop = true;
                             break;
                         }
-                        if (j == 0 && qq == 0 && k > 0 &&
+                        if (jr == 0 && qq == 0 && k > 0 &&
                             !mbar_wait_abort(&bars[kOEmpty], (k - 1) & 1, p.err, abort)) {
                             stop = true;
                             break;
@@ -370,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int ks = 0; ks < kBlk / 16; ++ks)
                             vd[ks] = umma_sdesc_sw128(ring_addr + s * kUnit + ks * 2048, kBlkBytes);
-                        if (!mbar_wait_abort(&bars[kPFull + qq], (jt + j) & 1, p.err, abort)) {
+                        if (!mbar_wait_abort(&bars[kPFull + qq], (jt + jr) & 1, p.err, abort)) {
                             stop = true;
                             break;
                         }
@@ -378,14 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t phi = sbuf + 64 * qq;
 #pragma unroll
                         for (int ks = 0; ks < kBlk / 16; ++ks) {
-                            umma_ts(obuf, phi + 8 * ks, vd[ks], kIdPV, (j | qq | ks) != 0);
+                            umma_ts(obuf, phi + 8 * ks, vd[ks], kIdPV, (jr | qq | ks) != 0);
                             umma_ts(obuf, phi + 32 + 8 * ks, vd[ks], kIdPV, 1);
                         }
                         umma_commit(&bars[kRingEmpty + s]);
                         umma_commit(&bars[kPvDone + qq]);
                     }
                 }
-                jt += it.n;
+                jt += it.je - it.jb;
             }
             // Drain: every tensor-core operation issued by this thread is complete before
             // the CTA frees TMEM.
@@ -433,10 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -CUDART_INF_F, l = 0.f;
             // First token of block kb = 4j + qq and its in-page index, advanced quarter by
             // quarter (no division: it would wait behind the partner warp's exps on the MUFU).
-            int blk_tok0 = 0, blk_in = 0;
-            for (int j = 0; j < it.n && !stop; ++j) {
+            int blk_in = (4 * it.jb) % blocks_per_page;
+            int blk_tok0 = ((4 * it.jb) / blocks_per_page) * block_size + blk_in * kBlk;
+            for (int j = it.jb; j < it.je && !stop; ++j) {
+                const uint32_t jr = (uint32_t)(j - it.jb);  // tile of this item or piece
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_abort(&bars[kSFull], (jt + j) & 1, p.err, abort))) {
+                                mbar_wait_abort(&bars[kSFull], (jt + jr) & 1, p.err, abort))) {
                     stop = true;
                     break;
                 }
@@ -521,8 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // earlier tensor op).  At quarter 0 no wait is needed: S_j being ready
                     // means every tensor op issued before QK_j has completed.  Either way
                     // the parity wait is never two phases behind its barrier.
-                    if ((j > 0 || qq > 0) && __any_sync(0xffffffffu, need)) {
-                        ok = qq == 0 || mbar_wait_abort(&bars[kPvDone + qq - 1], (jt + j) & 1,
+                    if ((jr > 0 || qq > 0) && __any_sync(0xffffffffu, need)) {
+                        ok = qq == 0 || mbar_wait_abort(&bars[kPvDone + qq - 1], (jt + jr) & 1,
                                                       p.err, abort);
                         if (!__all_sync(0xffffffffu, ok)) {
                             stop = true;
@@ -552,10 +579,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             const float lt = l + exchange(l, ok);
             if (!__all_sync(0xffffffffu, ok &&
-                                             mbar_wait_abort(&bars[kPvDone + 3], (jt + it.n - 1) & 1,
+                                             mbar_wait_abort(&bars[kPvDone + 3],
+                                                             (jt + (it.je - it.jb) - 1) & 1,
                                                            p.err, abort)))
                 break;
             tc_fence_after();
+            if (it.slot >= 0) {
+                // A piece of a split item: this warp's half of the row's unnormalised O
+                // and, from one warp of the pair, the row's running max (base-2 units) and
+                // sum of weights go to the piece's workspace slot; the merge kernel
+                // combines the item's pieces.
+                if (row < it.rows) {
+                    float *po = p.ws_o + ((int64_t)it.slot * kBM + row) * kHeadDim + 128 * hf;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(obase + 32 * c, r);
+                        tc_wait_ld();
+                        float4 *d4 = reinterpret_cast<float4 *>(po + 32 * c);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            d4[q4] = make_float4(__uint_as_float(r[4 * q4]),
+                                                 __uint_as_float(r[4 * q4 + 1]),
+                                                 __uint_as_float(r[4 * q4 + 2]),
+                                                 __uint_as_float(r[4 * q4 + 3]));
+                    }
+                    if (hf == 0) p.ws_ml[(int64_t)it.slot * kBM + row] = make_float2(m_used, lt);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kOEmpty]);
+                jt += it.je - it.jb;
+                continue;
+            }
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             uint16_t *dst =
                 p.out + ((int64_t)(it.q_off + it.r0 + row) * p.num_q_heads + it.h) * kHeadDim +
@@ -581,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kOEmpty]);
-            jt += it.n;
+            jt += it.je - it.jb;
         }
     }
 
@@ -596,6 +652,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+// Merge of split items: item s's pieces each left, per query row, an unnormalised O row
+// (sum over the piece's keys of 2^(score - m) v) with its running max m and sum of
+// weights l.  The row's output is sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k with
+// M = max_k m_k (a piece in which the row sees no key has m = -inf and weight 0), stored
+// as BF16.  One CTA per kMergeRows rows of a split item, one thread per output dim.
+constexpr int kMergeRows = 16;
+struct MergeSplit {
+    int out_row0;   // the item's first row in out
+    int rows;       // its rows present
+    int head;
+    int slot0, npieces;
+};
+struct MergeParams {
+    const float *ws_o;
+    const float2 *ws_ml;
+    uint16_t *out;
+    int num_q_heads, num_split;
+    MergeSplit s[kPfMaxSplitItems];
+};
+
+__global__ void __launch_bounds__(kHeadDim) prefill_merge_kernel(const __grid_constant__ MergeParams p) {
+    pdl_wait();  // the pieces' partials come from the prefill kernel before it
+    pdl_trigger();
+    const int si = blockIdx.x / (kBM / kMergeRows);
+    const int r0 = (blockIdx.x % (kBM / kMergeRows)) * kMergeRows;
+    if (si >= p.num_split) return;
+    const MergeSplit d = p.s[si];
+    const int dim = threadIdx.x;
+    const int r1 = min(r0 + kMergeRows, d.rows);
+    for (int r = r0; r < r1; ++r) {
+        float M = -CUDART_INF_F;
+        for (int k = 0; k < d.npieces; ++k)
+            M = fmaxf(M, p.ws_ml[(int64_t)(d.slot0 + k) * kBM + r].x);
+        float L = 0.f, O = 0.f;
+        for (int k = 0; k < d.npieces; ++k) {
+            const int64_t row = (int64_t)(d.slot0 + k) * kBM + r;
+            const float2 ml = p.ws_ml[row];
+            if (ml.x == -CUDART_INF_F) continue;  // no key of this piece is visible to the row
+            const float e = exp2f(ml.x - M);
+            L += e * ml.y;
+            O += e * p.ws_o[row * kHeadDim + dim];
+        }
+        const __nv_bfloat16 b = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        p.out[((int64_t)(d.out_row0 + r) * p.num_q_heads + d.head) * kHeadDim + dim] =
+            *reinterpret_cast<const uint16_t *>(&b);
+    }
+}
 
 #ifdef PA_TEST_HOOKS
 cudaError_t set_prefill_test_hook(int skip_unit) {
@@ -647,12 +751,26 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     p.out = a.out;
     p.err = a.err;
     int grid = min(p.num_items, a.num_sms > 0 ? a.num_sms : 1);
+    int num_split = 0;
+    p.sched.num_pieces = p.sched.num_split = 0;
+    p.ws_o = nullptr;
+    p.ws_ml = nullptr;
     if (a.sched && a.sched->num_ctas > 0) {
-        const int G = a.sched->num_ctas;
+        const PrefillSchedule &sc = *a.sched;
+        const int G = sc.num_ctas;
         p.sched.num_ctas = G;
-        memcpy(p.sched.off, a.sched->off, (G + 1) * sizeof(uint16_t));
-        memcpy(p.sched.items, a.sched->items, a.sched->off[G] * sizeof(uint16_t));
+        memcpy(p.sched.off, sc.off, (G + 1) * sizeof(uint16_t));
+        memcpy(p.sched.items, sc.items, sc.off[G] * sizeof(uint16_t));
         grid = G;
+        if (sc.num_pieces > 0) {
+            if (!a.workspace) return cudaErrorInvalidValue;
+            p.sched.num_pieces = sc.num_pieces;
+            p.sched.num_split = sc.num_split;
+            memcpy(p.sched.pieces, sc.pieces, sc.num_pieces * sizeof(PrefillPiece));
+            p.ws_o = static_cast<float *>(a.workspace);
+            p.ws_ml = reinterpret_cast<float2 *>(p.ws_o + (size_t)sc.num_pieces * kBM * kHeadDim);
+            num_split = sc.num_split;
+        }
     } else {
         p.sched.num_ctas = 0;
     }
@@ -660,6 +778,31 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     e = launch_pdl(prefill_tc_kernel<kSeqs>, dim3(grid), dim3(kThreads), kSmemBytes, stream,
                    maps, p);
     if (e != cudaSuccess) return e;
+    if (num_split > 0) {
+        // The split items' pieces are merged into their rows of out.
+        MergeParams mp;
+        mp.ws_o = p.ws_o;
+        mp.ws_ml = p.ws_ml;
+        mp.out = a.out;
+        mp.num_q_heads = a.num_q_heads;
+        mp.num_split = num_split;
+        for (int x = 0; x < num_split; ++x) {
+            const int idx = a.sched->split_item[x];
+            int b = 0;
+            while (b + 1 < a.num_seqs && idx >= p.seq[b + 1].item_off) ++b;
+            const SeqInfo &sq = p.seq[b];
+            const int local = idx - sq.item_off;
+            const int qt = sq.num_q_tiles - 1 - local / a.num_q_heads;
+            mp.s[x].out_row0 = sq.q_off + qt * kBM;
+            mp.s[x].rows = min(kBM, sq.q_len - qt * kBM);
+            mp.s[x].head = local % a.num_q_heads;
+            mp.s[x].slot0 = a.sched->split_slot0[x];
+            mp.s[x].npieces = a.sched->split_n[x];
+        }
+        e = launch_pdl(prefill_merge_kernel, dim3(num_split * (kBM / kMergeRows)),
+                       dim3(kHeadDim), 0, stream, mp);
+        if (e != cudaSuccess) return e;
+    }
     if (a.ev_stop) e = record_event(a.ev_stop, stream);
     return e;
 }

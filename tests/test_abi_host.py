@@ -89,11 +89,12 @@ def _decode(lib, **kw):
 def _prefill(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, page_stride=832 * 4 * 256, num_pages=64, bt=FAKE,
              q_len=4096, q_start=4096, causal=1, hq=24, hkv=4, d=256, bs=832, scale=0.0625,
-             out=FAKE)
+             out=FAKE, ws=None, ws_bytes=0)
     a.update(kw)
     return lib.pa_prefill_chunk(a["q"], a["k"], a["v"], a["page_stride"], a["num_pages"],
                                 a["bt"], a["q_len"], a["q_start"], a["causal"], a["hq"],
-                                a["hkv"], a["d"], a["bs"], a["scale"], a["out"], None)
+                                a["hkv"], a["d"], a["bs"], a["scale"], a["out"], a["ws"],
+                                a["ws_bytes"], None)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -151,6 +152,7 @@ def test_decode_append_rejects_bad_arguments(lib, kw, want):
     (dict(q_start=2**31 - 100, q_len=200), PA_ERR_INVALID_ARG),
     (dict(hkv=5), PA_ERR_INVALID_ARG),
     (dict(k=FAKE + 8), PA_ERR_INVALID_ARG),
+    (dict(ws=FAKE + 16, ws_bytes=1 << 20), PA_ERR_INVALID_ARG),  # workspace 256-byte aligned
     (dict(d=64, page_stride=832 * 4 * 64), PA_ERR_UNSUPPORTED),
 ])
 def test_prefill_rejects_bad_arguments(lib, kw, want):
@@ -220,7 +222,7 @@ def _varlen(lib, cu=(0, 10, 30), k_lens=(10, 40), bt_stride=1, num_seqs=None, **
     a.update(kw)
     return lib.pa_prefill_varlen(a["q"], a["k"], a["v"], a["page_stride"], a["num_pages"],
                                  a["bt"], bt_stride, cua, ska, B, 1, a["hq"], a["hkv"], a["d"],
-                                 a["bs"], a["scale"], a["out"], None)
+                                 a["bs"], a["scale"], a["out"], None, 0, None)
 
 
 @pytest.mark.parametrize("kw,want", [

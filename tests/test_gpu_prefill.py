@@ -34,6 +34,9 @@ def _oracle_caches_after_write(case, k_host, v_host):
 @pytest.mark.parametrize("bs,q_len,q_start", [
     (832, 1, 0), (832, 64, 0), (832, 65, 3), (832, 200, 100), (832, 130, 1000),
     (784, 300, 700), (784, 64, 784), (64, 129, 63), (16, 77, 40), (16, 1, 500),
+    # fewer items than SMs over long contexts: items split along the keys into pieces on
+    # different SMs, merged afterwards
+    (832, 1, 8192), (832, 64, 8192), (784, 200, 3000), (16, 40, 5000),
 ])
 def test_prefill_small_every_element(cuda_lib, bs, q_len, q_start):
     pa = cuda_lib
@@ -249,4 +252,51 @@ def test_prefill_mixed_batch_full_size_every_element(cuda_lib):
     e = assert_attention_close(out, ref, "mixed batch (every element)")
     print(f"mixed batch: {ref.size} outputs, max_abs={e['max_abs']:.3g} "
           f"max_rel={e['max_rel']:.3g} rel_l2={e['rel_l2']:.3g}")
+    assert pa.device_errors() == 0
+
+
+@pytest.mark.parametrize("bs,q_len,q_start", [(832, 64, 8192), (784, 200, 3000)])
+def test_prefill_split_items_match_the_unsplit_plan(cuda_lib, bs, q_len, q_start):
+    # The same chunk with a workspace (items split into pieces and merged) and without
+    # (whole items): both within the tolerance of the oracle and of each other, and the
+    # split form deterministic.
+    pa = cuda_lib
+    npg = -(-(q_start + q_len) // bs) + 2
+    case = workloads.paged_case(600 + q_len, [q_start + q_len], bs, npg, q_rows=q_len,
+                                q_start=q_start, device="cuda")
+    _write_chunk(pa, case)
+    need = pa.prefill_workspace_size(q_len, q_start, True, 24, 4, 256, bs)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    split = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                             True, case.scale, workspace=ws)
+    ws.fill_(0xFF)  # NaN bytes: the next call must not read what this one left
+    again = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                             True, case.scale, workspace=ws)
+    whole = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                             True, case.scale, workspace=torch.empty(0, dtype=torch.uint8,
+                                                                     device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(split, again)
+    e = (split.float() - whole.float()).abs().max().item()
+    assert e <= 1e-2, e
+    assert pa.device_errors() == 0
+
+
+def test_prefill_varlen_split_items(cuda_lib):
+    # Three one-row chunks and a 40-row chunk over 5000-7000 keys: 96 items for 152 SMs,
+    # split into pieces; every element against the oracle.
+    pa = cuda_lib
+    k_lens, q_rows, bs = [6000, 5000, 7000, 5500], [1, 1, 40, 1], 832
+    npg = sum(-(-L // bs) for L in k_lens) + 2
+    case = workloads.paged_case(4242, k_lens, bs, npg, q_rows=q_rows, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    cu = case.meta["cu_seqlens_q"]
+    assert pa.prefill_varlen_workspace_size(cu, k_lens, True, 24, 4, 256, bs) > 0
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            True, case.scale)
+    ref = oracle.prefill_varlen(bits(case.q), k_host, v_host, case.block_table.cpu().numpy(),
+                                cu, k_lens, True, case.scale)
+    assert_attention_close(out, ref, "varlen with split items")
     assert pa.device_errors() == 0

@@ -38,7 +38,7 @@ def test_lib(cuda_lib):
     lib.pa_decode.argtypes = [P, P, P, i64, i64, P, i64, P, i32, i32, i32, i32, i32, i32, f32,
                               P, P, sz, P, P, P, P]
     lib.pa_prefill_chunk.argtypes = [P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32,
-                                     f32, P, P]
+                                     f32, P, P, sz, P]
     lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, P]
     assert lib.pa_test_hook(-1, -1, 0) == PA_OK
     yield lib
@@ -77,7 +77,7 @@ def _prefill(lib, case):
                               case.v_cache.data_ptr(), case.k_cache.stride(0),
                               case.k_cache.shape[0], case.block_table[0].data_ptr(), q_len,
                               case.q_start, 1, hq, case.k_cache.shape[2], d, case.block_size,
-                              case.scale, out.data_ptr(), _stream())
+                              case.scale, out.data_ptr(), None, 0, _stream())
     assert rc == PA_OK
     return out
 

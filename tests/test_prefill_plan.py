@@ -90,3 +90,59 @@ def test_plan_refuses_bad_sizes_and_oversized_problems(lib):
         pa.prefill_plan(128, -1, True, 24, 832, 152)
     with pytest.raises(pa.PAError):  # 33000 rows x 24 heads: 6192 items > 6144
         pa.prefill_plan(33000, 0, True, 24, 832, 152)
+
+
+SPLIT_SHAPES = SHAPES + [
+    (1, 8192, True, 24, 832, 152),      # one row per head over a long context
+    (64, 8192, True, 24, 832, 152),
+    (200, 3000, True, 24, 784, 152),
+    (1685, 12288, True, 24, 832, 148),
+]
+
+
+@pytest.mark.parametrize("q_len,q_start,causal,hq,bs,G", SPLIT_SHAPES)
+def test_split_plan_covers_every_key_tile_once(lib, q_len, q_start, causal, hq, bs, G):
+    # With a workspace, items may be cut along their key tiles into pieces on different
+    # CTAs.  Every split item's pieces must tile [0, n) exactly, in order, each at least 4
+    # tiles; every other item runs whole on one CTA; the busiest CTA's cost (tiles + 1 per
+    # whole item, + 2 per piece) is the reported one, and never above the unsplit plan's.
+    import paged_kv_cache_09_gb300 as pa
+    cta, pieces, max_cost = pa.prefill_plan_pieces(q_len, q_start, causal, hq, bs, G)
+    costs = item_costs(q_len, q_start, causal, hq, bs)
+    assert len(cta) == len(costs)
+    _, unsplit = pa.prefill_plan(q_len, q_start, causal, hq, bs, G)
+    load = [0] * G
+    for i, b in enumerate(cta):
+        if b >= 0:
+            load[b] += costs[i]
+    by_item = {}
+    for item, t0, t1, b in pieces:
+        assert 0 <= b < G and cta[item] == -1
+        assert t1 - t0 >= 4
+        load[b] += (t1 - t0) + 2
+        by_item.setdefault(item, []).append((t0, t1))
+    for item, rs in by_item.items():
+        rs.sort()
+        assert len(rs) >= 2
+        assert rs[0][0] == 0 and rs[-1][1] == costs[item] - 1
+        assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
+    assert set(by_item) == {i for i, b in enumerate(cta) if b < 0}
+    assert max(load) == max_cost
+    assert max_cost <= unsplit
+    if pieces:
+        assert max_cost * 100 <= unsplit * 97
+
+
+def test_split_plan_balances_the_tail_chunk_and_short_chunks(lib):
+    import paged_kv_cache_09_gb300 as pa
+    # The q=1685 tail: 336 items of ~52 tiles on 152 CTAs; whole items leave the busiest
+    # CTA at 149 (three items); pieces bring it near the mean.
+    _, pieces, split = pa.prefill_plan_pieces(1685, 12288, True, 24, 832, 152)
+    _, whole = pa.prefill_plan(1685, 12288, True, 24, 832, 152)
+    mean = sum(item_costs(1685, 12288, True, 24, 832)) / 152
+    assert whole >= 140 and pieces and split <= mean + 10
+    # 24 one-row items over 8192 keys (33 tiles each) on 152 CTAs: whole items leave 128
+    # CTAs idle; pieces spread each item over several CTAs.
+    _, pieces, split = pa.prefill_plan_pieces(1, 8192, True, 24, 832, 152)
+    _, whole = pa.prefill_plan(1, 8192, True, 24, 832, 152)
+    assert pieces and split * 3 <= whole
