@@ -589,13 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // and, from one warp of the pair, the row's running max (base-2 units) and
                 // sum of weights go to the piece's workspace slot; the merge kernel
                 // combines the item's pieces.
-                if (row < it.rows) {
-                    float *po = p.ws_o + ((int64_t)it.slot * kBM + row) * kHeadDim + 128 * hf;
+                // (tcgen05.ld is warp-wide: every lane loads; only rows present store.)
+                float *po = p.ws_o + ((int64_t)it.slot * kBM + row) * kHeadDim + 128 * hf;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(obase + 32 * c, r);
-                        tc_wait_ld();
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(obase + 32 * c, r);
+                    tc_wait_ld();
+                    if (row < it.rows) {
                         float4 *d4 = reinterpret_cast<float4 *>(po + 32 * c);
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
@@ -604,8 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  __uint_as_float(r[4 * q4 + 2]),
                                                  __uint_as_float(r[4 * q4 + 3]));
                     }
-                    if (hf == 0) p.ws_ml[(int64_t)it.slot * kBM + row] = make_float2(m_used, lt);
                 }
+                if (hf == 0 && row < it.rows)
+                    p.ws_ml[(int64_t)it.slot * kBM + row] = make_float2(m_used, lt);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kOEmpty]);
