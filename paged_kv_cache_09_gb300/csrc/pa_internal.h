@@ -180,6 +180,7 @@ constexpr int kPfMaxPieces = 480;          // pieces of split items
 constexpr int kPfMaxSplitItems = 160;      // split items
 constexpr uint16_t kPfPieceBit = 0x8000;   // schedule entry kPfPieceBit | p: piece p
 constexpr int kPfMinPieceTiles = 4;        // no piece is shorter
+constexpr int kPfMaxPiecesPerItem = 16;    // no item is cut into more pieces
 
 struct PrefillPiece {
     uint16_t item;                  // the split item

@@ -19,7 +19,8 @@
 //      plan fits), items go by decreasing cost to the least loaded CTA while that stays
 //      within T; an item that does not fit is cut into pieces of at least
 //      kPfMinPieceTiles tiles that fill the least loaded CTAs up to T (a piece costs its
-//      tiles + 2: its Q load, its epilogue and the partial it writes).
+//      tiles + 2: its Q load, its epilogue and the partial it writes), at most
+//      kPfMaxPiecesPerItem pieces per item.
 // The split plan is taken when its busiest CTA is at least 3% cheaper.  Each CTA then
 // runs its items and pieces longest first.  Plans are cached per shape, since a serving
 // loop prefills chunks of the same few shapes over and over.
@@ -134,7 +135,10 @@ bool split_plan(const std::vector<int> &tiles, int G, int limit, CachedPlan &out
             }
             for (int b : used) heap.push({load[b], b});
             sn.push_back((uint16_t)(pieces.size() - s0.back()));
-            if (!ok || (int)si.size() > kPfMaxSplitItems) { ok = false; break; }
+            if (!ok || (int)si.size() > kPfMaxSplitItems || sn.back() > kPfMaxPiecesPerItem) {
+                ok = false;
+                break;
+            }
         }
         if (!ok) continue;
         long long entries = 0;
