@@ -55,7 +55,8 @@ cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
     // context for the device (after cudaDeviceReset the module is loaded afresh and the
     // attribute is gone) raises it again.
     constexpr int kDevices = 64;
-    static std::atomic<uintptr_t> done[4][kDevices];
+    if (slot < 0 || slot >= kSmemSlots) return cudaErrorInvalidValue;
+    static std::atomic<uintptr_t> done[kSmemSlots][kDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

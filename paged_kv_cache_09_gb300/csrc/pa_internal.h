@@ -15,7 +15,9 @@ namespace pa {
 uintptr_t current_context();
 
 // Raises a kernel's dynamic shared-memory limit once per (kernel slot, device context),
-// so that later launches (possibly under stream capture) make no attribute call.
+// so that later launches (possibly under stream capture) make no attribute call.  Slots:
+// 0 and 3 the two decode kernel shapes, 1, 2, 4, 5 the four prefill kernel variants.
+constexpr int kSmemSlots = 8;
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot);
 
 // Launches a kernel with programmatic dependent launch allowed: it may start while the
