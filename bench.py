@@ -708,8 +708,10 @@ def main():
         head = headline_workload("cuda")
         n = head.q.shape[0]
         fns = [attn_fn(pa, head, s, HEADLINE_CTX) for s in range(n)]
-        for _ in range(args.warmup):  # warm-up outside the timed region
-            fns[0]()
+        # Warm-up outside the timed region: the first heavy GPU work of the process ran
+        # ~4% slower than the same stream timed later in the run (clocks and power
+        # settle), so a whole untimed stream of steps comes first.
+        time_stream(fns, args.steps, args.warmup, flush)
         barrier(ws)
         torch.cuda.synchronize()
         step_ms = time_stream(fns, args.steps, args.warmup, flush)
