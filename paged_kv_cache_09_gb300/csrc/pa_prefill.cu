@@ -656,13 +656,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (sum over the piece's keys of 2^(score - m) v) with its running max m and sum of
 // weights l.  The row's output is sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k with
 // M = max_k m_k (a piece in which the row sees no key has m = -inf and weight 0), stored
-// as BF16.  A CTA takes kMergeRows rows of one split item, 8 threads per row, each
-// thread 32 dims: it reads its row's (m, l) pairs of all pieces at once, then the
-// pieces' O values 16 bytes at a time, so that a warp keeps many loads in flight (the
-// partials are read once; one thread per dim and row at a time measured ~44 us for the
-// tail chunk's 22 MB).
-constexpr int kMergeRows = 32;
-constexpr int kMergeThreads = kMergeRows * 8;
+// as BF16.  A CTA takes kMergeRows rows of one split item, 16 threads per row, each
+// thread 16 dims: it reads its row's (m, l) pairs of all pieces at once, then four
+// pieces' O values per round, 16 bytes at a time, so that many loads are in flight (the
+// partials are read once).  Measured on the tail chunk's 22 MB (ncu, cold L2): one
+// thread per dim and row ~44 us, 8 threads per row with two pieces per round ~14.6 us.
+constexpr int kMergeRows = 16;
+constexpr int kMergeThreadsPerRow = 16;
+constexpr int kMergeDims = kHeadDim / kMergeThreadsPerRow;  // 16 dims per thread
+constexpr int kMergeThreads = kMergeRows * kMergeThreadsPerRow;
+constexpr int kMergeRound = 4;  // pieces whose loads are in flight together
 struct MergeSplit {
     int out_row0;   // the item's first row in out
     int rows;       // its rows present
@@ -680,11 +683,13 @@ struct MergeParams {
 __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(
     const __grid_constant__ MergeParams p) {
     static_assert(kPfMaxPiecesPerItem <= 16, "a row's (m, l) pairs are kept in registers");
+    static_assert(kPfMaxPiecesPerItem % kMergeRound == 0, "whole rounds of pieces");
     pdl_wait();  // the pieces' partials come from the prefill kernel before it
     pdl_trigger();
     const int si = blockIdx.x / (kBM / kMergeRows);
-    const int r = (blockIdx.x % (kBM / kMergeRows)) * kMergeRows + threadIdx.x / 8;
-    const int d0 = (threadIdx.x % 8) * 32;
+    const int r = (blockIdx.x % (kBM / kMergeRows)) * kMergeRows +
+                  threadIdx.x / kMergeThreadsPerRow;
+    const int d0 = (threadIdx.x % kMergeThreadsPerRow) * kMergeDims;
     if (si >= p.num_split) return;
     const MergeSplit d = p.s[si];
     if (r >= d.rows) return;
@@ -704,39 +709,40 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(
         w[k] = w[k] == -CUDART_INF_F ? 0.f : exp2f(w[k] - M);  // no key of piece k: weight 0
         L += w[k] * lk[k];
     }
-    float acc[32];
+    float acc[kMergeDims];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-    // Two pieces per round, their 16 loads issued together.  A piece in which the row
-    // sees no key holds zeros there (its weights were all 0), so weight 0 times its
-    // values is 0; a slot past the item's pieces is not read.
+    for (int i = 0; i < kMergeDims; ++i) acc[i] = 0.f;
+    // A piece in which the row sees no key holds zeros there (its weights were all 0),
+    // so weight 0 times its values is 0; a slot past the item's pieces is not read.
 #pragma unroll
-    for (int k = 0; k < kPfMaxPiecesPerItem; k += 2) {
-        if (k >= d.npieces) break;  // the same for every thread of the CTA
-        const bool second = k + 1 < d.npieces;
-        const float4 *s0 = reinterpret_cast<const float4 *>(
-            p.ws_o + ((int64_t)(d.slot0 + k) * kBM + r) * kHeadDim + d0);
-        const float4 *s1 = s0 + (kBM * kHeadDim) / 4;  // the next slot, same row and dims
-        float4 a[8], b[8];
+    for (int k0 = 0; k0 < kPfMaxPiecesPerItem; k0 += kMergeRound) {
+        if (k0 >= d.npieces) break;  // the same for every thread of the CTA
+        float4 v[kMergeRound][kMergeDims / 4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            a[i] = s0[i];
-            b[i] = second ? s1[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < kMergeRound; ++k) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.ws_o + ((int64_t)(d.slot0 + k0 + k) * kBM + r) * kHeadDim + d0);
+#pragma unroll
+            for (int i = 0; i < kMergeDims / 4; ++i)
+                v[k][i] = k0 + k < d.npieces ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float wa = w[k], wb = second ? w[k + 1] : 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            acc[4 * i] += wa * a[i].x + wb * b[i].x;
-            acc[4 * i + 1] += wa * a[i].y + wb * b[i].y;
-            acc[4 * i + 2] += wa * a[i].z + wb * b[i].z;
-            acc[4 * i + 3] += wa * a[i].w + wb * b[i].w;
+        for (int k = 0; k < kMergeRound; ++k) {
+            const float wk = k0 + k < d.npieces ? w[k0 + k] : 0.f;
+#pragma unroll
+            for (int i = 0; i < kMergeDims / 4; ++i) {
+                acc[4 * i] += wk * v[k][i].x;
+                acc[4 * i + 1] += wk * v[k][i].y;
+                acc[4 * i + 2] += wk * v[k][i].z;
+                acc[4 * i + 3] += wk * v[k][i].w;
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint4 *dst = reinterpret_cast<uint4 *>(
         p.out + ((int64_t)(d.out_row0 + r) * p.num_q_heads + d.head) * kHeadDim + d0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kMergeDims / 8; ++i)
         dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv),
                             pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
                             pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
