@@ -103,7 +103,22 @@ struct SeqInfo {
     int bt_row;       // its row of the block table
 };
 
-template <int kSeqs>
+// The schedule as the kernel reads it: the CTA -> entries lists, and the pieces only in
+// the build with piece support (the kernel parameters stay as small as before for
+// whole-item plans).
+struct DevSchedule {
+    int num_ctas;                        // 0: none (the kernel walks a snake order)
+    uint16_t off[kPfSchedMaxCtas + 1];
+    uint16_t items[kPfSchedMaxItems];
+};
+template <bool kPieces>
+struct DevPieces {
+    PrefillPiece pieces[kPfMaxPieces];
+};
+template <>
+struct DevPieces<false> {};
+
+template <int kSeqs, bool kPieces>
 struct TcParams {
     const int32_t *block_table;  // row b of sequence b, bt_stride entries apart
     int64_t bt_stride;
@@ -118,7 +133,8 @@ struct TcParams {
     float *ws_o;    // piece partials: O [slot][128 rows][256] (only with split items)
     float2 *ws_ml;  // piece partials: (running max, sum of weights) [slot][128 rows]
     SeqInfo seq[kSeqs];
-    PrefillSchedule sched;  // static item -> CTA assignment (num_ctas 0: snake order)
+    DevSchedule sched;       // static item -> CTA assignment
+    DevPieces<kPieces> pc;   // pieces of split items (kPieces builds only)
 };
 
 template <int kSeqs>
@@ -127,7 +143,7 @@ struct TcMaps {
     CUtensorMap k_last[kSeqs], v_last[kSeqs];  // cut at each sequence's last token
 };
 
-static_assert(sizeof(TcMaps<kPfMaxSeqs>) + sizeof(TcParams<kPfMaxSeqs>) <= 32764,
+static_assert(sizeof(TcMaps<kPfMaxSeqs>) + sizeof(TcParams<kPfMaxSeqs, true>) <= 32764,
               "the kernel's parameters fit the 32 KB parameter space");
 
 struct Item {
@@ -143,16 +159,18 @@ struct Item {
 // use the kernel built without them, so whole-item plans run the plain code (piece
 // support measured 1.6% slower on the q=4096 chunk when always compiled in).
 template <int kSeqs, bool kPieces>
-__device__ __forceinline__ bool item_of(const TcParams<kSeqs> &p, int k, Item &it) {
+__device__ __forceinline__ bool item_of(const TcParams<kSeqs, kPieces> &p, int k, Item &it) {
     const int G = gridDim.x, b = blockIdx.x;
     int idx, piece = -1;
     if (p.sched.num_ctas) {
         const int x = p.sched.off[b] + k;
         if (x >= p.sched.off[b + 1]) return false;
         idx = p.sched.items[x];
-        if (kPieces && (idx & kPfPieceBit)) {
-            piece = idx & ~kPfPieceBit;
-            idx = p.sched.pieces[piece].item;
+        if constexpr (kPieces) {
+            if (idx & kPfPieceBit) {
+                piece = idx & ~kPfPieceBit;
+                idx = p.pc.pieces[piece].item;
+            }
         }
     } else {
         idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
@@ -178,14 +196,15 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs> &p, int k, Item &i
     const int rem = nkeys - full * p.block_size;
     it.nblocks = full * p.blocks_per_page + (rem + kBlk - 1) / kBlk;
     it.n = (it.nblocks + 3) / 4;
-    if (!kPieces || piece < 0) {
-        it.jb = 0;
-        it.je = it.n;
-        it.slot = -1;
-    } else {
-        it.jb = p.sched.pieces[piece].tile_begin;
-        it.je = p.sched.pieces[piece].tile_end;
-        it.slot = p.sched.pieces[piece].slot;
+    it.jb = 0;
+    it.je = it.n;
+    it.slot = -1;
+    if constexpr (kPieces) {
+        if (piece >= 0) {
+            it.jb = p.pc.pieces[piece].tile_begin;
+            it.je = p.pc.pieces[piece].tile_end;
+            it.slot = p.pc.pieces[piece].slot;
+        }
     }
     return true;
 }
@@ -200,7 +219,7 @@ __device__ int g_test_skip_unit = -1;
 template <int kSeqs, bool kPieces>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps<kSeqs> maps,
-                      const __grid_constant__ TcParams<kSeqs> p) {
+                      const __grid_constant__ TcParams<kSeqs, kPieces> p) {
     extern __shared__ __align__(16) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // CTA-uniform; nothing has been set up yet
         if (threadIdx.x == 0) atomicOr(p.err, kErrLayout);
@@ -767,7 +786,7 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     maps.q = tmaps[0];
     maps.k = tmaps[1];
     maps.v = tmaps[2];
-    TcParams<kSeqs> p;
+    TcParams<kSeqs, kPieces> p;
     p.block_table = a.block_table;
     p.bt_stride = a.bt_stride;
     p.causal = a.causal;
@@ -800,7 +819,6 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     p.err = a.err;
     int grid = min(p.num_items, a.num_sms > 0 ? a.num_sms : 1);
     int num_split = 0;
-    p.sched.num_pieces = p.sched.num_split = 0;
     p.ws_o = nullptr;
     p.ws_ml = nullptr;
     if (a.sched && a.sched->num_ctas > 0) {
@@ -811,10 +829,9 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
         memcpy(p.sched.items, sc.items, sc.off[G] * sizeof(uint16_t));
         grid = G;
         if (sc.num_pieces > 0) {
-            if (!a.workspace) return cudaErrorInvalidValue;
-            p.sched.num_pieces = sc.num_pieces;
-            p.sched.num_split = sc.num_split;
-            memcpy(p.sched.pieces, sc.pieces, sc.num_pieces * sizeof(PrefillPiece));
+            if (!kPieces || !a.workspace) return cudaErrorInvalidValue;
+            if constexpr (kPieces)
+                memcpy(p.pc.pieces, sc.pieces, sc.num_pieces * sizeof(PrefillPiece));
             p.ws_o = static_cast<float *>(a.workspace);
             p.ws_ml = reinterpret_cast<float2 *>(p.ws_o + (size_t)sc.num_pieces * kBM * kHeadDim);
             num_split = sc.num_split;
