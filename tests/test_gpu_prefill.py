@@ -300,3 +300,43 @@ def test_prefill_varlen_split_items(cuda_lib):
                                 cu, k_lens, True, case.scale)
     assert_attention_close(out, ref, "varlen with split items")
     assert pa.device_errors() == 0
+
+
+def test_prefill_non_causal_split_items(cuda_lib):
+    # Non-causal rows see every key; 24 items of ~28 tiles on 152 SMs are split.
+    pa = cuda_lib
+    q_len, q_start, bs = 100, 6000, 832
+    assert pa.prefill_workspace_size(q_len, q_start, False, 24, 4, 256, bs) > 0
+    npg = -(-(q_start + q_len) // bs) + 2
+    case = workloads.paged_case(7100, [q_start + q_len], bs, npg, q_rows=q_len, q_start=q_start,
+                                device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], q_start,
+                           False, case.scale)
+    ref = oracle.prefill(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                         q_start, False, case.scale)
+    assert_attention_close(out, ref, "non-causal, split items")
+    assert pa.device_errors() == 0
+
+
+def test_prefill_varlen_split_items_over_two_launches(cuda_lib):
+    # 40 one-row chunks over 2000-4000 keys: two launches (32 + 8 chunks), each with split
+    # items, one after the other on the same workspace; every element against the oracle.
+    pa = cuda_lib
+    rng = np.random.default_rng(40)
+    k_lens = rng.integers(2000, 4001, 40).tolist()
+    q_rows = [1] * 40
+    bs = 832
+    npg = sum(-(-L // bs) for L in k_lens) + 2
+    case = workloads.paged_case(4040, k_lens, bs, npg, q_rows=q_rows, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    cu = case.meta["cu_seqlens_q"]
+    assert pa.prefill_varlen_workspace_size(cu, k_lens, True, 24, 4, 256, bs) > 0
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            True, case.scale)
+    ref = oracle.prefill_varlen(bits(case.q), k_host, v_host, case.block_table.cpu().numpy(),
+                                cu, k_lens, True, case.scale)
+    assert_attention_close(out, ref, "varlen, two launches with split items")
+    assert pa.device_errors() == 0
