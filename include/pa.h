@@ -299,19 +299,26 @@ int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v
  * this library spreads one chunk over the GPU, not what the attention computes.  Host
  * only; touches no device.
  *
- * Work item i (0 <= i < ceil(q_len / 128) * num_q_heads) is the 128 query rows of tile
- * ceil(q_len / 128) - 1 - i / num_q_heads (the longest first) of head i % num_q_heads.
- * Its cost is the number of 256-key tiles it reads (64-key page-local blocks, four per
- * tile) plus one.  pa_prefill_chunk runs min(num_ctas, items) persistent CTAs, with
- * num_ctas = the device's SM count.
+ * Work items run from the chunk's last query tile (the longest under causal masking) to
+ * its first; within a tile, one item per query head: item i is the 128 query rows of tile
+ * ceil(q_len / 128) - 1 - i / num_q_heads of head i % num_q_heads.  One exception, with
+ * G = num_q_heads / num_kv_heads > 1: when the last tile's r rows satisfy r <= 128 / G,
+ * that tile runs as num_kv_heads packed items (items 0 .. num_kv_heads - 1, then the
+ * other tiles as above, shifted): packed item g holds the r rows of all G query heads of
+ * KV head g (its row x is tile row x / G of query head g * G + x % G).  An item's cost is
+ * the number of 256-key tiles it reads (64-key page-local blocks, four per tile) plus
+ * one.  pa_prefill_chunk runs min(num_ctas, items) persistent CTAs, with num_ctas = the
+ * device's SM count.
  *   cta_of_item  int32 [items] (host) or NULL: the CTA each item runs on
  *   num_items    (host, or NULL) the item count
  *   max_cost     (host, or NULL) the largest per-CTA total cost
- * Returns PA_ERR_INVALID_ARG for bad sizes, PA_ERR_UNSUPPORTED when the problem has more
- * than 6144 items or 256 CTAs (pa_prefill_chunk then walks the items in a fixed order).
+ * Returns PA_ERR_INVALID_ARG for bad sizes (num_q_heads not a multiple of num_kv_heads
+ * included), PA_ERR_UNSUPPORTED when the problem has more than 6144 items or 256 CTAs
+ * (pa_prefill_chunk then walks the items in a fixed order).
  */
-int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads, int block_size,
-                    int num_ctas, int32_t *cta_of_item, int *num_items, int *max_cost);
+int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads, int num_kv_heads,
+                    int block_size, int num_ctas, int32_t *cta_of_item, int *num_items,
+                    int *max_cost);
 
 /*
  * pa_prefill_plan_pieces -- the plan pa_prefill_chunk uses when given a workspace of
@@ -325,7 +332,8 @@ int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads, int blo
  * (PA_ERR_INVALID_ARG if the plan has more pieces).
  */
 int pa_prefill_plan_pieces(int q_len, int q_start, int causal, int num_q_heads,
-                           int block_size, int num_ctas, int max_pieces, int32_t *cta_of_item,
+                           int num_kv_heads, int block_size, int num_ctas, int max_pieces,
+                           int32_t *cta_of_item,
                            int32_t *piece_item, int32_t *piece_tile_begin,
                            int32_t *piece_tile_end, int32_t *piece_cta, int *num_items,
                            int *num_pieces, int *max_cost);

@@ -81,8 +81,9 @@ def load():
             "pa_prefill_chunk": ([P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                   P, P, sz, P], i32),
             "pa_prefill_varlen_workspace_size": ([P, P, i32, i32, i32, i32, i32, i32], sz),
-            "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, P, P, P], i32),
-            "pa_prefill_plan_pieces": ([i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P,
+            "pa_prefill_plan": ([i32, i32, i32, i32, i32, i32, i32, P, P, P], i32),
+            "pa_prefill_plan_pieces": ([i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P,
+                                        P,
                                         P], i32),
             "pa_prefill_varlen": ([P, P, P, i64, i64, P, i64, P, P, i32, i32, i32, i32, i32,
                                    i32, f32, P, P, sz, P], i32),
@@ -399,37 +400,36 @@ def prefill_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, c
     return out
 
 
-def prefill_plan(q_len, q_start, causal, num_q_heads, block_size, num_ctas):
+def prefill_plan(q_len, q_start, causal, num_q_heads, num_kv_heads, block_size, num_ctas):
     """The static work assignment of prefill_chunk (see pa_prefill_plan): returns
     (cta_of_item, max_cost) with cta_of_item a list indexed by work item."""
     lib = load()
     n = ctypes.c_int(0)
     mc = ctypes.c_int(0)
-    _raise(lib.pa_prefill_plan(q_len, q_start, int(bool(causal)), num_q_heads, block_size,
-                               num_ctas, None, ctypes.byref(n), None), "pa_prefill_plan")
+    args = (int(q_len), int(q_start), int(bool(causal)), int(num_q_heads), int(num_kv_heads),
+            int(block_size), int(num_ctas))
+    _raise(lib.pa_prefill_plan(*args, None, ctypes.byref(n), None), "pa_prefill_plan")
     cta = (ctypes.c_int32 * n.value)()
-    _raise(lib.pa_prefill_plan(q_len, q_start, int(bool(causal)), num_q_heads, block_size,
-                               num_ctas, cta, ctypes.byref(n), ctypes.byref(mc)),
-           "pa_prefill_plan")
+    _raise(lib.pa_prefill_plan(*args, cta, ctypes.byref(n), ctypes.byref(mc)), "pa_prefill_plan")
     return list(cta), mc.value
 
 
-
-def prefill_plan_pieces(q_len, q_start, causal, num_q_heads, block_size, num_ctas,
-                        max_pieces=480):
+def prefill_plan_pieces(q_len, q_start, causal, num_q_heads, num_kv_heads, block_size,
+                        num_ctas, max_pieces=480):
     """The plan used with a workspace (host only, see pa_prefill_plan_pieces): returns
     (cta_of_item with -1 for split items, [(item, tile_begin, tile_end, cta), ...], max_cost)."""
     lib = load()
     ni, npc, mc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    nqt = -(-int(q_len) // 128)
-    items = (ctypes.c_int32 * (nqt * num_q_heads))()
+    items = (ctypes.c_int32 * (-(-int(q_len) // 128) * num_q_heads))()  # an upper bound
     arrs = [(ctypes.c_int32 * max(1, max_pieces))() for _ in range(4)]
     _raise(lib.pa_prefill_plan_pieces(int(q_len), int(q_start), int(bool(causal)), num_q_heads,
-                                      block_size, num_ctas, max_pieces, items, *arrs,
-                                      ctypes.byref(ni), ctypes.byref(npc), ctypes.byref(mc)),
+                                      num_kv_heads, block_size, num_ctas, max_pieces, items,
+                                      *arrs, ctypes.byref(ni), ctypes.byref(npc),
+                                      ctypes.byref(mc)),
            "pa_prefill_plan_pieces")
     pieces = [(arrs[0][p], arrs[1][p], arrs[2][p], arrs[3][p]) for p in range(npc.value)]
     return list(items)[:ni.value], pieces, mc.value
+
 
 def set_kernel_events(start, stop):
     """Measurement hook: the next decode / prefill_chunk call records these

@@ -120,14 +120,16 @@ bool make_tile_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_he
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Query rows [q_len, Hq, D] as {D, Hq, q_len}; boxes of 64 dims x 1 head x box_rows.
+// Query rows [q_len, Hq, D] as {D, Hq, q_len}; boxes of 64 dims x box_heads heads x
+// box_rows rows (in shared memory: box_heads * box_rows rows of 128 bytes, heads fastest).
 bool make_rows_map(CUtensorMap *m, const void *base, int head_dim, int num_heads, int rows,
-                   int box_rows) {
+                   int box_heads, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
-    cuuint32_t box[3] = {(cuuint32_t)pa::kChunkElems, 1, (cuuint32_t)box_rows};
+    cuuint32_t box[3] = {(cuuint32_t)pa::kChunkElems, (cuuint32_t)box_heads,
+                         (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -466,7 +468,7 @@ int pa_decode_append(const pa_bf16 *q, pa_bf16 *k_cache, pa_bf16 *v_cache, int64
 // The schedule of one prefill launch over nseq chunks: with split items when the
 // workspace (workspace_bytes; 0 for none) holds their pieces' partials.
 static bool prefill_schedule(const pa::PrefillSeq *seqs, int nseq, int causal, int num_q_heads,
-                             int block_size, int num_sms, size_t workspace_bytes,
+                             int group, int block_size, int num_sms, size_t workspace_bytes,
                              pa::PrefillSchedule *sched) {
     int q_lens[pa::kPfMaxSeqs], q_starts[pa::kPfMaxSeqs];
     for (int b = 0; b < nseq; ++b) {
@@ -474,12 +476,12 @@ static bool prefill_schedule(const pa::PrefillSeq *seqs, int nseq, int causal, i
         q_starts[b] = seqs[b].q_start;
     }
     if (workspace_bytes >= pa::kPfSlotBytes &&
-        pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads, block_size, num_sms, true,
-                         sched, nullptr) &&
+        pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads, group, block_size, num_sms,
+                         true, sched, nullptr) &&
         (size_t)sched->num_pieces * pa::kPfSlotBytes <= workspace_bytes)
         return true;
-    return pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads, block_size, num_sms,
-                            false, sched, nullptr);
+    return pa::plan_prefill(nseq, q_lens, q_starts, causal, num_q_heads, group, block_size,
+                            num_sms, false, sched, nullptr);
 }
 
 // One prefill launch over 1 .. kPfMaxSeqs chunks whose rows lie in q / out of total_q rows.
@@ -491,11 +493,16 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
                           pa_bf16 *out, void *workspace, size_t workspace_bytes,
                           const DeviceInfo &dev, cudaEvent_t ev_start, cudaEvent_t ev_stop,
                           cudaStream_t stream) {
-    CUtensorMap maps[3 + 2 * pa::kPfMaxSeqs];
-    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, total_q, pa::kPfQRows) ||
-        !make_cache_map(&maps[1], k_cache, head_dim, num_kv_heads, block_size, num_pages,
+    CUtensorMap maps[4 + 2 * pa::kPfMaxSeqs];
+    const int group = num_q_heads / num_kv_heads;
+    const int pack_rows = pa::prefill_pack_rows(group);
+    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, total_q, 1, pa::kPfQRows) ||
+        !(pack_rows > 0
+              ? make_rows_map(&maps[1], q, head_dim, num_q_heads, total_q, group, pack_rows)
+              : make_rows_map(&maps[1], q, head_dim, num_q_heads, total_q, 1, pa::kPfQRows)) ||
+        !make_cache_map(&maps[2], k_cache, head_dim, num_kv_heads, block_size, num_pages,
                         page_stride, pa::kPfBlock) ||
-        !make_cache_map(&maps[2], v_cache, head_dim, num_kv_heads, block_size, num_pages,
+        !make_cache_map(&maps[3], v_cache, head_dim, num_kv_heads, block_size, num_pages,
                         page_stride, pa::kPfBlock))
         return PA_ERR_CUDA;
     for (int b = 0; b < nseq; ++b) {
@@ -503,16 +510,16 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
         // so rows past it come back as zeros.
         const int seq_len_k = seqs[b].q_start + seqs[b].q_len;
         const int last_rows = seq_len_k - ((seq_len_k - 1) / block_size) * block_size;
-        if (!make_cache_map(&maps[3 + 2 * b], k_cache, head_dim, num_kv_heads, last_rows,
+        if (!make_cache_map(&maps[4 + 2 * b], k_cache, head_dim, num_kv_heads, last_rows,
                             num_pages, page_stride, pa::kPfBlock) ||
-            !make_cache_map(&maps[4 + 2 * b], v_cache, head_dim, num_kv_heads, last_rows,
+            !make_cache_map(&maps[5 + 2 * b], v_cache, head_dim, num_kv_heads, last_rows,
                             num_pages, page_stride, pa::kPfBlock))
             return PA_ERR_CUDA;
     }
     // The static work assignment (cached per shape); problems too large for its arrays
     // run without one.
     static thread_local pa::PrefillSchedule sched;
-    const bool planned = prefill_schedule(seqs, nseq, causal, num_q_heads, block_size,
+    const bool planned = prefill_schedule(seqs, nseq, causal, num_q_heads, group, block_size,
                                           dev.num_sms, workspace ? workspace_bytes : 0, &sched);
     pa::PrefillArgs a;
     a.sched = planned ? &sched : nullptr;
@@ -524,7 +531,7 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
     a.causal = causal;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
-    a.group = num_q_heads / num_kv_heads;
+    a.group = group;
     a.block_size = block_size;
     a.num_pages = num_pages;
     a.scale = scale;
@@ -549,7 +556,8 @@ size_t pa_prefill_workspace_size(int q_len, int q_start, int causal, int num_q_h
     if (device_info(&dev)) return 0;
     const pa::PrefillSeq seq{0, q_len, q_start, 0};
     static thread_local pa::PrefillSchedule sched;
-    if (!prefill_schedule(&seq, 1, causal ? 1 : 0, num_q_heads, block_size, dev.num_sms,
+    if (!prefill_schedule(&seq, 1, causal ? 1 : 0, num_q_heads, num_q_heads / num_kv_heads,
+                          block_size, dev.num_sms,
                           (size_t)pa::kPfMaxPieces * pa::kPfSlotBytes, &sched))
         return 0;
     return (size_t)sched.num_pieces * pa::kPfSlotBytes;
@@ -609,7 +617,8 @@ size_t pa_prefill_varlen_workspace_size(const int32_t *cu_seqlens_q, const int32
     const int n = (int)seqs.size();
     for (int s0 = 0; s0 < n; s0 += pa::kPfMaxSeqs) {
         const int cnt = std::min(pa::kPfMaxSeqs, n - s0);
-        if (prefill_schedule(&seqs[s0], cnt, causal ? 1 : 0, num_q_heads, block_size,
+        if (prefill_schedule(&seqs[s0], cnt, causal ? 1 : 0, num_q_heads,
+                             num_q_heads / num_kv_heads, block_size,
                              dev.num_sms, (size_t)pa::kPfMaxPieces * pa::kPfSlotBytes, &sched))
             need = std::max(need, (size_t)sched.num_pieces * pa::kPfSlotBytes);
     }

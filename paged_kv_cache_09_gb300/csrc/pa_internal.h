@@ -169,8 +169,47 @@ __host__ __device__ inline int prefill_item_tiles(int q_len, int q_start, int ca
     return (nblocks + kPfKvTile / kPfBlock - 1) / (kPfKvTile / kPfBlock);
 }
 
-// Static assignment of prefill work items to the persistent CTAs.  Item index i stands
-// for query tile (num_q_tiles - 1 - i / Hq) of head i % Hq (the longest items first).
+// Packed last query tile.  A chunk's last query tile holds r = q_len - 128 * (tiles - 1)
+// rows.  When r <= 128 / G (G = Hq / Hkv query heads per KV head, G > 1), those rows of
+// all G query heads of one KV head fit one 128-row item: item row x is tile row x / G of
+// query head g * G + x % G (Q read as one box of G heads x 128 / G rows).  The tile then
+// runs as Hkv items instead of Hq items that would be mostly empty rows (the q=1685 tail
+// chunk: 21 rows, 4 items instead of 24; a one-row chunk: 4 items of 6 rows).
+__host__ __device__ inline int prefill_pack_rows(int group) {
+    return group > 1 ? kPfQRows / group : 0;
+}
+__host__ __device__ inline bool prefill_last_tile_packed(int q_len, int group) {
+    return q_len - ((q_len - 1) / kPfQRows) * kPfQRows <= prefill_pack_rows(group);
+}
+// Work items of one chunk, and what item i of it is: query tile *qt, and query head *h
+// (for the packed item, KV head *h); returns whether item i is the packed one.  Items run
+// from the chunk's last (longest, under causal masking) query tile to its first.
+__host__ __device__ inline int prefill_chunk_items(int q_len, int num_q_heads, int group) {
+    const int nqt = (q_len + kPfQRows - 1) / kPfQRows;
+    return prefill_last_tile_packed(q_len, group) ? (nqt - 1) * num_q_heads + num_q_heads / group
+                                                  : nqt * num_q_heads;
+}
+__host__ __device__ inline bool prefill_item_at(int i, int q_len, int num_q_heads, int group,
+                                                int *qt, int *h) {
+    const int nqt = (q_len + kPfQRows - 1) / kPfQRows;
+    if (prefill_last_tile_packed(q_len, group)) {
+        const int num_kv_heads = num_q_heads / group;
+        if (i < num_kv_heads) {
+            *qt = nqt - 1;
+            *h = i;
+            return true;
+        }
+        i -= num_kv_heads;
+        *qt = nqt - 2 - i / num_q_heads;
+    } else {
+        *qt = nqt - 1 - i / num_q_heads;
+    }
+    *h = i % num_q_heads;
+    return false;
+}
+
+// Static assignment of prefill work items to the persistent CTAs (items numbered as
+// prefill_item_at gives them, sequence by sequence).
 // When a workspace is given and the items do not divide evenly over the CTAs, some
 // items are split along the keys into pieces (ranges of their 256-key tiles) that run on
 // different CTAs; each piece writes an unnormalised partial (fp32 O rows, and per row
@@ -212,7 +251,7 @@ constexpr size_t kPfSlotBytes = (size_t)kPfQRows * 256 * 4 + (size_t)kPfQRows * 
 // s->num_pieces * kPfSlotBytes bytes).  max_cost (optional): the largest per-CTA cost, in
 // tiles plus one per item (two per piece).
 bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int causal,
-                  int num_q_heads, int block_size, int num_ctas, bool allow_split,
+                  int num_q_heads, int group, int block_size, int num_ctas, bool allow_split,
                   PrefillSchedule *s, int *max_cost);
 
 // Sequences one prefill launch takes (their chunks' tensor maps travel in the launch's
@@ -244,7 +283,9 @@ struct PrefillArgs {
     int num_sms;                    // persistent grid size bound
 };
 
-// tmaps: Q, K, V, then the K and V maps cut at each sequence's last token (2 per sequence).
+// tmaps: Q (boxes of 1 head x 128 rows), Q for packed items (G heads x 128 / G rows;
+// a copy of the first when the group does not pack), K, V, then the K and V maps cut at
+// each sequence's last token (2 per sequence).
 cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream);
 
 #ifdef PA_TEST_HOOKS

@@ -1,7 +1,8 @@
 // pa_plan.cu -- static work assignment for the persistent prefill kernel (host only).
 //
-// The causal chunk's work items (128 query rows of one head) differ in length: row tile
-// r of a chunk at q_start reads q_start + r*128 + 128 keys.  With about five items per
+// The causal chunk's work items (128 query rows of one head, or of the GQA group's heads
+// for a packed last tile) differ in length: row tile r of a chunk at q_start reads
+// q_start + r*128 + 128 keys.  With about five items per
 // CTA, walking them in a fixed order leaves some CTAs well above the mean (the q=4096
 // chunk over 4096 prior tokens: 138 tiles on the busiest CTA against a mean of 123.8).
 // This planner assigns items to CTAs up front:
@@ -39,11 +40,11 @@ namespace {
 
 struct PlanKey {
     std::vector<std::pair<int, int>> chunks;  // (q_len, q_start) of each sequence
-    int causal, hq, bs, ctas;
+    int causal, hq, group, bs, ctas;
     bool allow_split;
     bool operator==(const PlanKey &o) const {
-        return chunks == o.chunks && causal == o.causal && hq == o.hq && bs == o.bs &&
-               ctas == o.ctas && allow_split == o.allow_split;
+        return chunks == o.chunks && causal == o.causal && hq == o.hq && group == o.group &&
+               bs == o.bs && ctas == o.ctas && allow_split == o.allow_split;
     }
 };
 
@@ -159,13 +160,13 @@ std::mutex g_plan_mu;
 std::vector<CachedPlan> g_plan_cache;  // most recently used last
 
 void compute_plan(const PlanKey &k, CachedPlan &out) {
-    // Items sequence by sequence; within a sequence item i is query tile nqt - 1 - i / hq
-    // of head i % hq.
+    // Items sequence by sequence, numbered as prefill_item_at gives them.
     std::vector<int> cost;
     for (const auto &c : k.chunks) {
-        const int nqt = (c.first + kPfQRows - 1) / kPfQRows;
-        for (int i = 0; i < nqt * k.hq; ++i) {
-            const int qt = nqt - 1 - i / k.hq;
+        const int n = prefill_chunk_items(c.first, k.hq, k.group);
+        for (int i = 0; i < n; ++i) {
+            int qt, h;
+            prefill_item_at(i, c.first, k.hq, k.group, &qt, &h);
             cost.push_back(prefill_item_tiles(c.first, c.second, k.causal, qt * kPfQRows, k.bs) +
                            1);
         }
@@ -254,14 +255,16 @@ void compute_plan(const PlanKey &k, CachedPlan &out) {
 }  // namespace
 
 bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int causal,
-                  int num_q_heads, int block_size, int num_ctas, bool allow_split,
+                  int num_q_heads, int group, int block_size, int num_ctas, bool allow_split,
                   PrefillSchedule *s, int *max_cost) {
-    if (num_seqs < 1 || num_q_heads < 1 || block_size < 1 || num_ctas < 1) return false;
+    if (num_seqs < 1 || num_q_heads < 1 || group < 1 || num_q_heads % group || block_size < 1 ||
+        num_ctas < 1)
+        return false;
     long long n = 0;
-    PlanKey key{{}, causal ? 1 : 0, num_q_heads, block_size, num_ctas, allow_split};
+    PlanKey key{{}, causal ? 1 : 0, num_q_heads, group, block_size, num_ctas, allow_split};
     for (int b = 0; b < num_seqs; ++b) {
-        if (q_lens[b] < 1 || q_starts[b] < 0) return false;
-        n += (long long)((q_lens[b] + kPfQRows - 1) / kPfQRows) * num_q_heads;
+        if (q_lens[b] < 1 || q_starts[b] < 0 || q_lens[b] > (1 << 30)) return false;
+        n += (long long)prefill_chunk_items(q_lens[b], num_q_heads, group);
         key.chunks.emplace_back(q_lens[b], q_starts[b]);
     }
     if (n > kPfSchedMaxItems || std::min<long long>(num_ctas, n) > kPfSchedMaxCtas)
@@ -301,15 +304,15 @@ bool plan_prefill(int num_seqs, const int *q_lens, const int *q_starts, int caus
 }  // namespace pa
 
 extern "C" int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_heads,
-                               int block_size, int num_ctas, int32_t *cta_of_item,
-                               int *num_items, int *max_cost) {
+                               int num_kv_heads, int block_size, int num_ctas,
+                               int32_t *cta_of_item, int *num_items, int *max_cost) {
     if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > INT32_MAX || num_q_heads < 1 ||
-        block_size < 1 || num_ctas < 1)
+        num_kv_heads < 1 || num_q_heads % num_kv_heads || block_size < 1 || num_ctas < 1)
         return PA_ERR_INVALID_ARG;
     static thread_local pa::PrefillSchedule s;
     int mc = 0;
-    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, block_size, num_ctas, false,
-                          &s, &mc))
+    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, num_q_heads / num_kv_heads,
+                          block_size, num_ctas, false, &s, &mc))
         return PA_ERR_UNSUPPORTED;
     const int n = s.off[s.num_ctas];
     if (num_items) *num_items = n;
@@ -321,20 +324,23 @@ extern "C" int pa_prefill_plan(int q_len, int q_start, int causal, int num_q_hea
 }
 
 extern "C" int pa_prefill_plan_pieces(int q_len, int q_start, int causal, int num_q_heads,
-                                      int block_size, int num_ctas, int max_pieces,
+                                      int num_kv_heads, int block_size, int num_ctas,
+                                      int max_pieces,
                                       int32_t *cta_of_item, int32_t *piece_item,
                                       int32_t *piece_tile_begin, int32_t *piece_tile_end,
                                       int32_t *piece_cta, int *num_items, int *num_pieces,
                                       int *max_cost) {
     if (q_len < 1 || q_start < 0 || (int64_t)q_start + q_len > INT32_MAX || num_q_heads < 1 ||
-        block_size < 1 || num_ctas < 1 || max_pieces < 0)
+        num_kv_heads < 1 || num_q_heads % num_kv_heads || block_size < 1 || num_ctas < 1 ||
+        max_pieces < 0)
         return PA_ERR_INVALID_ARG;
     static thread_local pa::PrefillSchedule s;
     int mc = 0;
-    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, block_size, num_ctas, true,
-                          &s, &mc))
+    const int group = num_q_heads / num_kv_heads;
+    if (!pa::plan_prefill(1, &q_len, &q_start, causal, num_q_heads, group, block_size, num_ctas,
+                          true, &s, &mc))
         return PA_ERR_UNSUPPORTED;
-    const int items = ((q_len + pa::kPfQRows - 1) / pa::kPfQRows) * num_q_heads;
+    const int items = pa::prefill_chunk_items(q_len, num_q_heads, group);
     if (num_items) *num_items = items;
     if (num_pieces) *num_pieces = s.num_pieces;
     if (max_cost) *max_cost = mc;

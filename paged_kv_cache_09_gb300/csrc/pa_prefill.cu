@@ -15,7 +15,11 @@
 // the PV of quarter q runs while the softmax of quarter q+1 is computed, and the tensor
 // core only waits for the softmax of each tile's first quarter.
 //
-// Work item = (128 query rows of one head).  Persistent CTAs, one per SM, run the items
+// Work item = (128 query rows of one head).  A chunk's last query tile, when its r rows
+// times the GQA group G fit 128 rows, runs instead as one packed item per KV head: its
+// TMEM lane x holds tile row x / G of query head g*G + x % G (Q comes in as boxes of G
+// heads x 128/G rows), so the six heads of a group share one pass over their K/V rather
+// than each taking a 128-row item with r rows present.  Persistent CTAs, one per SM, run the items
 // the host planner assigned to them (a static schedule that balances the causal items'
 // unequal lengths across CTAs, passed in the kernel parameters), longest first.
 // Problems too large for the schedule arrays walk the items longest first in a snake
@@ -98,32 +102,31 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct SeqInfo {
     int q_off, q_len, q_start, seq_len_k;
     int last_page;    // logical index of the sequence's last page
-    int num_q_tiles;  // ceil(q_len / 128)
-    int item_off;     // its first work item: items item_off .. item_off + tiles * Hq - 1
+    int item_off;     // its first work item (items numbered as prefill_item_at gives them)
     int bt_row;       // its row of the block table
 };
 
 // The schedule as the kernel reads it: the CTA -> entries lists, and the pieces only in
-// the build with piece support (the kernel parameters stay as small as before for
-// whole-item plans).
+// the extended build (the kernel parameters of plain plans stay small).
 struct DevSchedule {
     int num_ctas;                        // 0: none (the kernel walks a snake order)
     uint16_t off[kPfSchedMaxCtas + 1];
     uint16_t items[kPfSchedMaxItems];
 };
-template <bool kPieces>
+template <bool kExt>
 struct DevPieces {
     PrefillPiece pieces[kPfMaxPieces];
 };
 template <>
 struct DevPieces<false> {};
 
-template <int kSeqs, bool kPieces>
+template <int kSeqs, bool kExt>
 struct TcParams {
     const int32_t *block_table;  // row b of sequence b, bt_stride entries apart
     int64_t bt_stride;
     int causal, num_seqs, num_items;
     int num_q_heads, group;
+    int qp_bytes;         // bytes of a packed item's Q tile (G heads x 128/G rows)
     int block_size, blocks_per_page;
     int64_t num_pages;
     float sc;             // |scale| * log2(e), at least FLT_MIN
@@ -134,12 +137,12 @@ struct TcParams {
     float2 *ws_ml;  // piece partials: (running max, sum of weights) [slot][128 rows]
     SeqInfo seq[kSeqs];
     DevSchedule sched;       // static item -> CTA assignment
-    DevPieces<kPieces> pc;   // pieces of split items (kPieces builds only)
+    DevPieces<kExt> pc;   // pieces of split items (extended build only)
 };
 
 template <int kSeqs>
 struct TcMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, qp, k, v;  // qp: Q in boxes of G heads x 128/G rows (packed items)
     CUtensorMap k_last[kSeqs], v_last[kSeqs];  // cut at each sequence's last token
 };
 
@@ -147,7 +150,10 @@ static_assert(sizeof(TcMaps<kPfMaxSeqs>) + sizeof(TcParams<kPfMaxSeqs, true>) <=
               "the kernel's parameters fit the 32 KB parameter space");
 
 struct Item {
-    int h, g, r0, rows, nblocks, n;  // head, KV head, first row, rows present, blocks, tiles
+    // head (the first of the group for a packed item), KV head, first row of the query
+    // tile, its rows present (per head), key blocks, tiles
+    int h, g, r0, rows, nblocks, n;
+    bool pk;  // packed: lane x holds tile row x / G of head h + x % G
     int b, q_off, q_start, seq_len_k, last_page, bt_row;  // its sequence
     // The tiles [jb, je) this CTA runs: all n of a whole item, or one piece's range; a
     // piece writes its partial to workspace slot `slot` (-1: a whole item, normalised
@@ -155,18 +161,19 @@ struct Item {
     int jb, je, slot;
 };
 
-// kPieces: the schedule may hold pieces of split items.  Launches whose plan has none
-// use the kernel built without them, so whole-item plans run the plain code (piece
-// support measured 1.6% slower on the q=4096 chunk when always compiled in).
-template <int kSeqs, bool kPieces>
-__device__ __forceinline__ bool item_of(const TcParams<kSeqs, kPieces> &p, int k, Item &it) {
+// kExt: the launch may hold pieces of split items and packed last tiles.  Launches with
+// neither use the kernel built without them, so plain plans run the plain code (piece
+// support measured 1.6% slower on the q=4096 chunk when always compiled in, packed
+// tiles another 1.5%).
+template <int kSeqs, bool kExt>
+__device__ __forceinline__ bool item_of(const TcParams<kSeqs, kExt> &p, int k, Item &it) {
     const int G = gridDim.x, b = blockIdx.x;
     int idx, piece = -1;
     if (p.sched.num_ctas) {
         const int x = p.sched.off[b] + k;
         if (x >= p.sched.off[b + 1]) return false;
         idx = p.sched.items[x];
-        if constexpr (kPieces) {
+        if constexpr (kExt) {
             if (idx & kPfPieceBit) {
                 piece = idx & ~kPfPieceBit;
                 idx = p.pc.pieces[piece].item;
@@ -180,9 +187,18 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs, kPieces> &p, int k
     while (sb + 1 < p.num_seqs && idx >= p.seq[sb + 1].item_off) ++sb;
     const SeqInfo &sq = p.seq[sb];
     const int local = idx - sq.item_off;
-    const int qt = sq.num_q_tiles - 1 - local / p.num_q_heads;
-    it.h = local % p.num_q_heads;
-    it.g = it.h / p.group;
+    int qt;
+    if constexpr (kExt) {
+        int hh;
+        it.pk = prefill_item_at(local, sq.q_len, p.num_q_heads, p.group, &qt, &hh);
+        it.g = it.pk ? hh : hh / p.group;
+        it.h = it.pk ? hh * p.group : hh;
+    } else {  // no packed tile: item i is tile nqt - 1 - i / Hq of head i % Hq
+        qt = (sq.q_len + kBM - 1) / kBM - 1 - local / p.num_q_heads;
+        it.pk = false;
+        it.h = local % p.num_q_heads;
+        it.g = it.h / p.group;
+    }
     it.r0 = qt * kBM;
     it.rows = min(kBM, sq.q_len - it.r0);
     it.b = sb;
@@ -199,7 +215,7 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs, kPieces> &p, int k
     it.jb = 0;
     it.je = it.n;
     it.slot = -1;
-    if constexpr (kPieces) {
+    if constexpr (kExt) {
         if (piece >= 0) {
             it.jb = p.pc.pieces[piece].tile_begin;
             it.je = p.pc.pieces[piece].tile_end;
@@ -216,10 +232,10 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs, kPieces> &p, int k
 __device__ int g_test_skip_unit = -1;
 #endif
 
-template <int kSeqs, bool kPieces>
+template <int kSeqs, bool kExt>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps<kSeqs> maps,
-                      const __grid_constant__ TcParams<kSeqs, kPieces> p) {
+                      const __grid_constant__ TcParams<kSeqs, kExt> p) {
     extern __shared__ __align__(16) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // CTA-uniform; nothing has been set up yet
         if (threadIdx.x == 0) atomicOr(p.err, kErrLayout);
@@ -286,19 +302,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             int q_loads = 0;
             Item it;
             bool stop = false;
-            for (int k = 0; !stop && (item_of<kSeqs, kPieces>(p, k, it)); ++k) {
+            for (int k = 0; !stop && (item_of<kSeqs, kExt>(p, k, it)); ++k) {
                 if (k > 0 && !mbar_wait_abort(&bars[kQEmpty], (k - 1) & 1, p.err, abort)) break;
                 ++q_loads;
-                mbar_arrive_expect_tx(&bars[kQFull], kQBytes);
+                const bool pk = kExt && it.pk;
+                mbar_arrive_expect_tx(&bars[kQFull], pk ? p.qp_bytes : kQBytes);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(qs + c * kQChunk, &maps.q, &bars[kQFull], c * kChunkElems, it.h,
-                                it.q_off + it.r0);
+                    tma_load_3d(qs + c * kQChunk, pk ? &maps.qp : &maps.q, &bars[kQFull],
+                                c * kChunkElems, it.h, it.q_off + it.r0);
                 const int32_t *bt = p.block_table + (int64_t)it.bt_row * p.bt_stride;
                 // Page and in-page index of block kb, advanced block by block: a division
                 // per block would take the MUFU, which the softmax warps keep busy (one
                 // per item places the first block of a piece).
-                int blk_lp = kPieces && it.jb ? (4 * it.jb) / p.blocks_per_page : 0;
+                int blk_lp = kExt && it.jb ? (4 * it.jb) / p.blocks_per_page : 0;
                 int blk_in = 4 * it.jb - blk_lp * p.blocks_per_page;
                 for (int j = it.jb; j < it.je && !stop; ++j) {
                     // Page, offset and map of each of the tile's four blocks; blocks past the
@@ -374,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t u = 0, jt = 0;
             Item it;
             bool stop = false;
-            for (int k = 0; !stop && (item_of<kSeqs, kPieces>(p, k, it)); ++k) {
+            for (int k = 0; !stop && (item_of<kSeqs, kExt>(p, k, it)); ++k) {
                 if (!mbar_wait_abort(&bars[kQFull], k & 1, p.err, abort)) break;
                 tc_fence_after();
                 for (int j = it.jb; j < it.je && !stop; ++j) {
@@ -475,13 +492,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t jt = 0;
         Item it;
         bool stop = false;
-        for (int k = 0; !stop && (item_of<kSeqs, kPieces>(p, k, it)); ++k) {
-            const int qpos = it.q_start + it.r0 + row;
+        for (int k = 0; !stop && (item_of<kSeqs, kExt>(p, k, it)); ++k) {
+            // This lane's query row: tile row rpos of head rhead (lanes of a packed item
+            // past G * rows, and rows past the chunk's end, are computed but not stored).
+            int rpos = row, rhead = it.h;
+            if constexpr (kExt) {
+                if (it.pk) {
+                    rpos = row / p.group;
+                    rhead = it.h + (row - rpos * p.group);
+                }
+            }
+            const int qpos = it.q_start + it.r0 + rpos;
             float m_used = -CUDART_INF_F, l = 0.f;
             // First token of block kb = 4j + qq and its in-page index, advanced quarter by
             // quarter (no division: it would wait behind the partner warp's exps on the MUFU).
             int blk_in = 0, blk_tok0 = 0;
-            if (kPieces && it.jb) {  // a piece starts at block 4 * jb
+            if (kExt && it.jb) {  // a piece starts at block 4 * jb
                 const int lp0 = (4 * it.jb) / blocks_per_page;
                 blk_in = 4 * it.jb - lp0 * blocks_per_page;
                 blk_tok0 = lp0 * block_size + blk_in * kBlk;
@@ -615,13 +641,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // warp of the pair, the row's running max (base-2 units) and sum of weights,
             // to the piece's workspace slot; the merge kernel combines the item's pieces.
             // (tcgen05.ld is warp-wide: every lane loads; only rows present store.)
-            const bool piece = kPieces && it.slot >= 0;
+            const bool piece = kExt && it.slot >= 0;
             const float inv = piece ? 1.f : (lt > 0.f ? 1.f / lt : 0.f);
             uint16_t *dst =
-                p.out + ((int64_t)(it.q_off + it.r0 + row) * p.num_q_heads + it.h) * kHeadDim +
+                p.out + ((int64_t)(it.q_off + it.r0 + rpos) * p.num_q_heads + rhead) * kHeadDim +
                 128 * hf;
             float *po = p.ws_o + ((int64_t)it.slot * kBM + row) * kHeadDim + 128 * hf;
-            const bool present = row < it.rows;
+            const bool present = rpos < it.rows;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
@@ -687,8 +713,9 @@ constexpr int kMergeThreads = kMergeRows * kMergeThreadsPerRow;
 constexpr int kMergeRound = 4;  // pieces whose loads are in flight together
 struct MergeSplit {
     int out_row0;   // the item's first row in out
-    int rows;       // its rows present
-    int head;
+    int rows;       // its rows present (TMEM lanes: rows x G for a packed item)
+    int head;       // its head (the group's first, for a packed item)
+    int pack;       // G for a packed item (lane x: row x / G, head + x % G), else 0
     int slot0, npieces;
 };
 struct MergeParams {
@@ -758,8 +785,10 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int rp = d.pack ? r / d.pack : r;
+    const int hh = d.pack ? d.head + (r - rp * d.pack) : d.head;
     uint4 *dst = reinterpret_cast<uint4 *>(
-        p.out + ((int64_t)(d.out_row0 + r) * p.num_q_heads + d.head) * kHeadDim + d0);
+        p.out + ((int64_t)(d.out_row0 + rp) * p.num_q_heads + hh) * kHeadDim + d0);
 #pragma unroll
     for (int i = 0; i < kMergeDims / 8; ++i)
         dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv),
@@ -776,17 +805,18 @@ cudaError_t set_prefill_test_hook(int skip_unit) {
 
 namespace {
 
-template <int kSeqs, bool kPieces>
+template <int kSeqs, bool kExt>
 cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int slot,
                              cudaStream_t stream) {
     cudaError_t e = set_smem_once(
-        reinterpret_cast<const void *>(prefill_tc_kernel<kSeqs, kPieces>), kSmemBytes, slot);
+        reinterpret_cast<const void *>(prefill_tc_kernel<kSeqs, kExt>), kSmemBytes, slot);
     if (e != cudaSuccess) return e;
     TcMaps<kSeqs> maps;
     maps.q = tmaps[0];
-    maps.k = tmaps[1];
-    maps.v = tmaps[2];
-    TcParams<kSeqs, kPieces> p;
+    maps.qp = tmaps[1];
+    maps.k = tmaps[2];
+    maps.v = tmaps[3];
+    TcParams<kSeqs, kExt> p;
     p.block_table = a.block_table;
     p.bt_stride = a.bt_stride;
     p.causal = a.causal;
@@ -794,22 +824,22 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     int items = 0;
     for (int b = 0; b < a.num_seqs; ++b) {
         const PrefillSeq &sq = a.seqs[b];
-        maps.k_last[b] = tmaps[3 + 2 * b];
-        maps.v_last[b] = tmaps[4 + 2 * b];
+        maps.k_last[b] = tmaps[4 + 2 * b];
+        maps.v_last[b] = tmaps[5 + 2 * b];
         SeqInfo &si = p.seq[b];
         si.q_off = sq.q_off;
         si.q_len = sq.q_len;
         si.q_start = sq.q_start;
         si.seq_len_k = sq.q_start + sq.q_len;
         si.last_page = (si.seq_len_k - 1) / a.block_size;
-        si.num_q_tiles = (sq.q_len + kBM - 1) / kBM;
         si.item_off = items;
         si.bt_row = sq.bt_row;
-        items += si.num_q_tiles * a.num_q_heads;
+        items += prefill_chunk_items(sq.q_len, a.num_q_heads, a.group);
     }
     p.num_items = items;
     p.num_q_heads = a.num_q_heads;
     p.group = a.group;
+    p.qp_bytes = kChunks * 128 * a.group * prefill_pack_rows(a.group);
     p.block_size = a.block_size;
     p.blocks_per_page = (a.block_size + kBlk - 1) / kBlk;
     p.num_pages = a.num_pages;
@@ -829,8 +859,8 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
         memcpy(p.sched.items, sc.items, sc.off[G] * sizeof(uint16_t));
         grid = G;
         if (sc.num_pieces > 0) {
-            if (!kPieces || !a.workspace) return cudaErrorInvalidValue;
-            if constexpr (kPieces)
+            if (!kExt || !a.workspace) return cudaErrorInvalidValue;
+            if constexpr (kExt)
                 memcpy(p.pc.pieces, sc.pieces, sc.num_pieces * sizeof(PrefillPiece));
             p.ws_o = static_cast<float *>(a.workspace);
             p.ws_ml = reinterpret_cast<float2 *>(p.ws_o + (size_t)sc.num_pieces * kBM * kHeadDim);
@@ -840,7 +870,7 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
         p.sched.num_ctas = 0;
     }
     if (a.ev_start && (e = record_event(a.ev_start, stream)) != cudaSuccess) return e;
-    e = launch_pdl(prefill_tc_kernel<kSeqs, kPieces>, dim3(grid), dim3(kThreads), kSmemBytes, stream,
+    e = launch_pdl(prefill_tc_kernel<kSeqs, kExt>, dim3(grid), dim3(kThreads), kSmemBytes, stream,
                    maps, p);
     if (e != cudaSuccess) return e;
     if (num_split > 0) {
@@ -856,11 +886,14 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
             int b = 0;
             while (b + 1 < a.num_seqs && idx >= p.seq[b + 1].item_off) ++b;
             const SeqInfo &sq = p.seq[b];
-            const int local = idx - sq.item_off;
-            const int qt = sq.num_q_tiles - 1 - local / a.num_q_heads;
+            int qt, hh;
+            const bool pk =
+                prefill_item_at(idx - sq.item_off, sq.q_len, a.num_q_heads, a.group, &qt, &hh);
+            const int rows = min(kBM, sq.q_len - qt * kBM);
             mp.s[x].out_row0 = sq.q_off + qt * kBM;
-            mp.s[x].rows = min(kBM, sq.q_len - qt * kBM);
-            mp.s[x].head = local % a.num_q_heads;
+            mp.s[x].rows = pk ? rows * a.group : rows;
+            mp.s[x].head = pk ? hh * a.group : hh;
+            mp.s[x].pack = pk ? a.group : 0;
             mp.s[x].slot0 = a.sched->split_slot0[x];
             mp.s[x].npieces = a.sched->split_n[x];
         }
@@ -876,12 +909,16 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
 
 cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream) {
     if (a.num_seqs < 1 || a.num_seqs > kPfMaxSeqs) return cudaErrorInvalidValue;
-    const bool pieces = a.sched && a.sched->num_ctas > 0 && a.sched->num_pieces > 0;
+    // The extended kernel when the plan has pieces of split items or a chunk ends in a
+    // packed query tile.
+    bool ext = a.sched && a.sched->num_ctas > 0 && a.sched->num_pieces > 0;
+    for (int b = 0; b < a.num_seqs; ++b)
+        ext = ext || prefill_last_tile_packed(a.seqs[b].q_len, a.group);
     if (a.num_seqs == 1)
-        return pieces ? launch_prefill_n<1, true>(tmaps, a, 4, stream)
-                      : launch_prefill_n<1, false>(tmaps, a, 1, stream);
-    return pieces ? launch_prefill_n<kPfMaxSeqs, true>(tmaps, a, 5, stream)
-                  : launch_prefill_n<kPfMaxSeqs, false>(tmaps, a, 2, stream);
+        return ext ? launch_prefill_n<1, true>(tmaps, a, 4, stream)
+                   : launch_prefill_n<1, false>(tmaps, a, 1, stream);
+    return ext ? launch_prefill_n<kPfMaxSeqs, true>(tmaps, a, 5, stream)
+               : launch_prefill_n<kPfMaxSeqs, false>(tmaps, a, 2, stream);
 }
 
 }  // namespace pa

@@ -340,3 +340,51 @@ def test_prefill_varlen_split_items_over_two_launches(cuda_lib):
                                 cu, k_lens, True, case.scale)
     assert_attention_close(out, ref, "varlen, two launches with split items")
     assert pa.device_errors() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,q_start,bs", [
+    # a short last query tile runs as one item per KV head holding all G heads' rows
+    (24, 4, 21, 700, 832), (24, 4, 22, 700, 832), (24, 4, 149, 900, 784),
+    (8, 4, 64, 300, 64), (8, 4, 65, 300, 64), (8, 1, 136, 1000, 832),
+    (16, 2, 16, 2000, 16), (4, 4, 1, 900, 832), (32, 4, 16, 0, 832),
+])
+def test_prefill_packed_last_tile_every_element(cuda_lib, hq, hkv, q_len, q_start, bs):
+    pa = cuda_lib
+    npg = -(-(q_start + q_len) // bs) + 2
+    case = workloads.paged_case(900 + q_len + hq, [q_start + q_len], bs, npg, q_rows=q_len,
+                                q_start=q_start, hq=hq, hkv=hkv, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    ref = oracle.prefill(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                         q_start, True, case.scale)
+    for ws in (None, torch.empty(0, dtype=torch.uint8, device="cuda")):  # split, whole
+        out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0],
+                               q_start, True, case.scale, workspace=ws)
+        assert_attention_close(out, ref, f"packed tile hq={hq} hkv={hkv} q={q_len}@{q_start}")
+    assert pa.device_errors() == 0
+
+
+def test_prefill_packed_last_tile_non_causal_and_varlen(cuda_lib):
+    # Non-causal packed items, and a mixed batch whose chunks end in short tiles (3, 21
+    # and 1 rows, packed) beside one that does not (50 rows).
+    pa = cuda_lib
+    case = workloads.paged_case(4321, [3021], 832, 6, q_rows=21, q_start=3000, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    out = pa.prefill_chunk(case.q, case.k_cache, case.v_cache, case.block_table[0], 3000,
+                           False, case.scale)
+    ref = oracle.prefill(bits(case.q), k_host, v_host, case.block_table[0].cpu().numpy(),
+                         3000, False, case.scale)
+    assert_attention_close(out, ref, "packed tile, non-causal")
+    k_lens, q_rows, bs = [131, 4000, 6000, 50], [131, 21, 1, 50], 832
+    npg = sum(-(-L // bs) for L in k_lens) + 2
+    case = workloads.paged_case(4322, k_lens, bs, npg, q_rows=q_rows, device="cuda")
+    k_host, v_host = _oracle_caches_after_write(case, bits(case.k_cache), bits(case.v_cache))
+    _write_chunk(pa, case)
+    cu = case.meta["cu_seqlens_q"]
+    out = pa.prefill_varlen(case.q, case.k_cache, case.v_cache, case.block_table, cu, k_lens,
+                            True, case.scale)
+    ref = oracle.prefill_varlen(bits(case.q), k_host, v_host, case.block_table.cpu().numpy(),
+                                cu, k_lens, True, case.scale)
+    assert_attention_close(out, ref, "varlen with packed tiles")
+    assert pa.device_errors() == 0

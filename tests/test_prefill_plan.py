@@ -1,6 +1,7 @@
 """Host-only checks of the prefill kernel's static work assignment (pa_prefill_plan).
 
-The plan decides which persistent CTA runs which work item (128 query rows of one head);
+The plan decides which persistent CTA runs which work item (128 query rows of one head,
+or of all heads of a GQA group for a chunk's short last query tile);
 it does not change what is computed, so it is checked for validity and balance, with
 the item costs recomputed here from the kernel's streaming rule: an item reads the keys
 up to its last row (causal) or all keys, in page-local blocks of 64 keys, four blocks
@@ -13,18 +14,24 @@ import pytest
 from test_abi_host import lib  # noqa: F401  (builds and loads libpa.so)
 
 
-def item_costs(q_len, q_start, causal, hq, bs):
+def item_tiles(q_len, q_start, causal, r0, bs):
+    rows = min(128, q_len - r0)
+    nkeys = q_start + r0 + rows if causal else q_start + q_len
+    full, rem = divmod(nkeys, bs)
+    nblocks = full * math.ceil(bs / 64) + math.ceil(rem / 64)
+    return math.ceil(nblocks / 4)
+
+
+def item_costs(q_len, q_start, causal, hq, bs, hkv=4):
+    # Items from the last query tile to the first, one per head; a last tile of r rows
+    # with r * G <= 128 (G = hq / hkv > 1) runs as hkv packed items instead of hq.
     nqt = math.ceil(q_len / 128)
-    bpp = math.ceil(bs / 64)
+    G = hq // hkv
+    r_last = q_len - 128 * (nqt - 1)
     costs = []
-    for i in range(nqt * hq):
-        qt = nqt - 1 - i // hq
-        r0 = qt * 128
-        rows = min(128, q_len - r0)
-        nkeys = q_start + r0 + rows if causal else q_start + q_len
-        full, rem = divmod(nkeys, bs)
-        nblocks = full * bpp + math.ceil(rem / 64)
-        costs.append(math.ceil(nblocks / 4) + 1)
+    for qt in range(nqt - 1, -1, -1):
+        n = hkv if (qt == nqt - 1 and G > 1 and r_last * G <= 128) else hq
+        costs += [item_tiles(q_len, q_start, causal, qt * 128, bs) + 1] * n
     return costs
 
 
@@ -50,7 +57,7 @@ SHAPES = [
 @pytest.mark.parametrize("q_len,q_start,causal,hq,bs,G", SHAPES)
 def test_every_item_runs_exactly_once_on_a_valid_cta(lib, q_len, q_start, causal, hq, bs, G):
     import paged_kv_cache_09_gb300 as pa
-    cta, max_cost = pa.prefill_plan(q_len, q_start, causal, hq, bs, G)
+    cta, max_cost = pa.prefill_plan(q_len, q_start, causal, hq, 4, bs, G)
     costs = item_costs(q_len, q_start, causal, hq, bs)
     assert len(cta) == len(costs)
     ctas = min(G, len(costs))
@@ -68,7 +75,7 @@ def test_every_item_runs_exactly_once_on_a_valid_cta(lib, q_len, q_start, causal
 def test_headline_chunk_is_balanced_to_the_lower_bound(lib):
     import paged_kv_cache_09_gb300 as pa
     costs = item_costs(4096, 4096, True, 24, 832)
-    _, max_cost = pa.prefill_plan(4096, 4096, True, 24, 832, 152)
+    _, max_cost = pa.prefill_plan(4096, 4096, True, 24, 4, 832, 152)
     lb = math.ceil(sum(costs) / 152)
     assert max_cost <= lb + 1
     assert snake_max(costs, 152) - max_cost >= 5  # 143 -> 129 in cost units
@@ -76,20 +83,20 @@ def test_headline_chunk_is_balanced_to_the_lower_bound(lib):
 
 def test_plan_is_deterministic_and_cached(lib):
     import paged_kv_cache_09_gb300 as pa
-    a = pa.prefill_plan(4096, 4096, True, 24, 832, 152)
-    pa.prefill_plan(2048, 0, True, 24, 832, 152)
-    b = pa.prefill_plan(4096, 4096, True, 24, 832, 152)
+    a = pa.prefill_plan(4096, 4096, True, 24, 4, 832, 152)
+    pa.prefill_plan(2048, 0, True, 24, 4, 832, 152)
+    b = pa.prefill_plan(4096, 4096, True, 24, 4, 832, 152)
     assert a == b
 
 
 def test_plan_refuses_bad_sizes_and_oversized_problems(lib):
     import paged_kv_cache_09_gb300 as pa
     with pytest.raises(pa.PAError):
-        pa.prefill_plan(0, 0, True, 24, 832, 152)
+        pa.prefill_plan(0, 0, True, 24, 4, 832, 152)
     with pytest.raises(pa.PAError):
-        pa.prefill_plan(128, -1, True, 24, 832, 152)
+        pa.prefill_plan(128, -1, True, 24, 4, 832, 152)
     with pytest.raises(pa.PAError):  # 33000 rows x 24 heads: 6192 items > 6144
-        pa.prefill_plan(33000, 0, True, 24, 832, 152)
+        pa.prefill_plan(33000, 0, True, 24, 4, 832, 152)
 
 
 SPLIT_SHAPES = SHAPES + [
@@ -107,10 +114,10 @@ def test_split_plan_covers_every_key_tile_once(lib, q_len, q_start, causal, hq, 
     # tiles; every other item runs whole on one CTA; the busiest CTA's cost (tiles + 1 per
     # whole item, + 2 per piece) is the reported one, and never above the unsplit plan's.
     import paged_kv_cache_09_gb300 as pa
-    cta, pieces, max_cost = pa.prefill_plan_pieces(q_len, q_start, causal, hq, bs, G)
+    cta, pieces, max_cost = pa.prefill_plan_pieces(q_len, q_start, causal, hq, 4, bs, G)
     costs = item_costs(q_len, q_start, causal, hq, bs)
     assert len(cta) == len(costs)
-    _, unsplit = pa.prefill_plan(q_len, q_start, causal, hq, bs, G)
+    _, unsplit = pa.prefill_plan(q_len, q_start, causal, hq, 4, bs, G)
     load = [0] * G
     for i, b in enumerate(cta):
         if b >= 0:
@@ -137,12 +144,37 @@ def test_split_plan_balances_the_tail_chunk_and_short_chunks(lib):
     import paged_kv_cache_09_gb300 as pa
     # The q=1685 tail: 336 items of ~52 tiles on 152 CTAs; whole items leave the busiest
     # CTA at 149 (three items); pieces bring it near the mean.
-    _, pieces, split = pa.prefill_plan_pieces(1685, 12288, True, 24, 832, 152)
-    _, whole = pa.prefill_plan(1685, 12288, True, 24, 832, 152)
+    _, pieces, split = pa.prefill_plan_pieces(1685, 12288, True, 24, 4, 832, 152)
+    _, whole = pa.prefill_plan(1685, 12288, True, 24, 4, 832, 152)
     mean = sum(item_costs(1685, 12288, True, 24, 832)) / 152
     assert whole >= 140 and pieces and split <= mean + 10
     # 24 one-row items over 8192 keys (33 tiles each) on 152 CTAs: whole items leave 128
     # CTAs idle; pieces spread each item over several CTAs.
-    _, pieces, split = pa.prefill_plan_pieces(1, 8192, True, 24, 832, 152)
-    _, whole = pa.prefill_plan(1, 8192, True, 24, 832, 152)
+    _, pieces, split = pa.prefill_plan_pieces(1, 8192, True, 24, 4, 832, 152)
+    _, whole = pa.prefill_plan(1, 8192, True, 24, 4, 832, 152)
     assert pieces and split * 3 <= whole
+
+
+@pytest.mark.parametrize("q_len,hq,hkv,packed", [
+    (21, 24, 4, True), (22, 24, 4, False), (1, 24, 4, True), (1685, 24, 4, True),
+    (1686, 24, 4, False), (64, 8, 4, True), (65, 8, 4, False), (8, 16, 1, True),
+    (9, 16, 1, False), (5, 4, 4, False), (128 + 32, 16, 4, True),
+])
+def test_short_last_tile_runs_as_one_item_per_kv_head(lib, q_len, hq, hkv, packed):
+    # The last query tile's r rows of all G = hq / hkv heads of a KV head share one item
+    # when r * G <= 128: hkv items for that tile instead of hq.
+    import paged_kv_cache_09_gb300 as pa
+    cta, _ = pa.prefill_plan(q_len, 1000, True, hq, hkv, 832, 152)
+    nqt = math.ceil(q_len / 128)
+    assert len(cta) == (nqt - 1) * hq + (hkv if packed else hq)
+    assert len(cta) == len(item_costs(q_len, 1000, True, hq, 832, hkv))
+    cta, pieces, _ = pa.prefill_plan_pieces(q_len, 1000, True, hq, hkv, 832, 152)
+    assert len(cta) == (nqt - 1) * hq + (hkv if packed else hq)
+
+
+def test_plan_refuses_a_group_that_does_not_divide(lib):
+    import paged_kv_cache_09_gb300 as pa
+    with pytest.raises(pa.PAError):
+        pa.prefill_plan(100, 0, True, 24, 5, 832, 152)
+    with pytest.raises(pa.PAError):
+        pa.prefill_plan_pieces(100, 0, True, 24, 0, 832, 152)
