@@ -66,7 +66,7 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one split launch of the headline (32K) step in an ncu
 # capture of the current split kernel (summarised under profiles/); None whenever the
 # kernel changes after a capture.
-SPLIT_32K_DRAM_BYTES = 134_290_176 + 3_086_592
+SPLIT_32K_DRAM_BYTES = 134_292_736 + 3_537_408
 # The same for one prefill launch of the q=4096 chunk over 4096 prior tokens.
 PREFILL_Q4096_DRAM_BYTES = 86_165_248 + 17_116_416
 
