@@ -26,7 +26,7 @@ stream (A/B/A), all in this run.
 
 Other legs, reported under "legs": the 4K/8K/16K/32K sweep (same pool), 32K in generic
 16- and 64-token pages, the serving step at 8K (new token appended: slot derived in the
-kernel, KV write, decode; 16 copies of a 64-page pool) with its own e2e, block_size 784
+kernel, KV write, decode; 32 copies of a 64-page pool) with its own e2e, block_size 784
 at 8K, batched decode (16 sequences, 4K-32K, appended token), the q=4096 prefill chunk
 over 4096 prior tokens (chunk KV write + prefill; TFLOP/s counts the causal work
 4*D*Hq*sum_i(4096+i+1) = 6.185e11), the q=1685 tail chunk over 12288 prior tokens and
@@ -66,7 +66,7 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one split launch of the headline (32K) step in an ncu
 # capture of the current split kernel (summarised under profiles/); None whenever the
 # kernel changes after a capture.
-SPLIT_32K_DRAM_BYTES = 134_292_736 + 3_537_408
+SPLIT_32K_DRAM_BYTES = 134_296_576 + 3_398_144
 # The same for one prefill launch of the q=4096 chunk over 4096 prior tokens.
 PREFILL_Q4096_DRAM_BYTES = 86_165_248 + 17_116_416
 
@@ -324,9 +324,12 @@ def attn_fn(pa, case, s, max_seq_len):
     return call
 
 
-def headline_replicas(device, n=16, block_size=832, new_tokens=1):
+def headline_replicas(device, n=32, block_size=832, new_tokens=1):
     """n copies of the 8K workload, each its own shuffled 64-page pool (seeds 1002, 2002,
-    ...; the first is the headline case): 16 x 33.5 MB of K/V read in rotation, 4x L2."""
+    ...): 32 x 33.5 MB of K/V read in rotation, 8x L2.  The decode prefetches each split's
+    first tiles into L2 before it waits for the previous kernel; with 16 copies some of
+    those lines were still in L2 when the same copy came round again (an ncu capture saw
+    8% of a launch's bytes come from L2)."""
     return [workloads.paged_case(1002 + 1000 * r, [8192], block_size, 64,
                                  new_tokens=new_tokens, device=device) for r in range(n)]
 
@@ -408,13 +411,13 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
 
 def l2check_leg(pa, flush):
     """For an ncu capture of dram__bytes_read.sum per split launch (--cache-control none):
-    32 consecutive 8K decode steps over 16 copies of the workload in turn (the headline
+    64 consecutive 8K decode steps over 32 copies of the workload in turn (the 8K legs'
     timing), then 16 steps of one copy (L2 warm, the control).  Small pools (11 pages per
-    copy) keep the device footprint under 1 GB."""
+    copy) keep the device footprint under 1.5 GB."""
     reps = [workloads.paged_case(1002 + 1000 * r, [8192], 832, 11, new_tokens=1,
-                                 device="cuda") for r in range(16)]
+                                 device="cuda") for r in range(32)]
     fns = [append_step_fn(pa, c, 8192)[0] for c in reps]
-    r = {"rotation_us_per_step": time_stream(fns, 32, 0, flush) * 1e3,
+    r = {"rotation_us_per_step": time_stream(fns, 64, 0, flush) * 1e3,
          "one_copy_us_per_step": time_stream(fns[:1], 16, 0, flush) * 1e3}
     del reps, fns
     torch.cuda.empty_cache()
@@ -534,7 +537,7 @@ def e2e_append_fns(pa, cases):
 
 def step8k_leg(pa, steps, warmup, flush, peaks):
     """The serving step at 8K: each step appends its sequence's newest token (slot derived
-    in the kernel, KV write) and decodes over 8192 keys; 16 copies of the workload in
+    in the kernel, KV write) and decodes over 8192 keys; 32 copies of the workload in
     turn.  Its end-to-end form (host buffers) is timed between two device timings."""
     reps = headline_replicas("cuda")
     fns = [append_step_fn(pa, c, 8192)[0] for c in reps]

@@ -181,11 +181,15 @@ __device__ int g_test_consumer_delay_ns = 0;
 #endif
 
 // Tiles of its split (two ring stages) that a CTA prefetches into L2 before waiting for
-// the previous kernel on the stream.  Measured in streams of steps against no prefetch:
-// 4K 8.44 -> 7.98 us, 8K 10.95 -> 10.84, 32K 24.66 -> 24.23, 32K in 16-token pages
-// 26.2 -> 25.6; batched decode 188.3 -> 190.1 us.  Eight or sixteen tiles were slower at
-// 8K with 784-token pages and in 16-token pages (the prefetch outlasts the wait and
-// delays the first loads), two gained less.
+// the previous kernel on the stream, when its split has at most four times as many.
+// Measured in streams of steps that rotate over three 1 GiB pools (so that no step finds
+// lines an earlier step prefetched), against no prefetch: 4K (8-tile splits) 8.34 ->
+// 7.97 us; 8K (14 tiles) 11.06 -> 10.83; 32K (54 tiles) 25.22 -> 25.21.  In rotations
+// over one pool the longer splits seemed to gain more (32K 25.45 -> 24.87), but only
+// because some prefetched lines stayed in L2 until the same sequence came round again;
+// an ncu capture of such a rotation saw a 32K launch read 4.5 of its 134 MB from L2.
+// Four tiles gained more than two; eight or sixteen were slower (the prefetch outlasts
+// the wait and delays the first loads).
 constexpr int kDecPrefetchTiles = 4;
 
 template <int kDecConsumers, int kDecStages>
@@ -231,14 +235,19 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32, 1)
         const int tpp = p.tiles_per_page;
         const int t0 = split * p.tiles_per_split;
         const int t_end =
-            min(t0 + min(p.tiles_per_split, kDecPrefetchTiles),
-                seq_tiles(p.max_seq_len, p.block_size, tpp));  // inside the table row
+            p.tiles_per_split > 4 * kDecPrefetchTiles
+                ? t0
+                : min(t0 + kDecPrefetchTiles,
+                      seq_tiles(p.max_seq_len, p.block_size, tpp));  // inside the table row
         int lp = t0 / tpp, tip = t0 - lp * tpp;
         int page = t0 < t_end ? __ldcg(bt + lp) : 0;
+        // Evict-first, like the loads that use these lines: a prefetched line that
+        // outlived its use would otherwise stay in L2 at normal priority.
+        const uint64_t pol = l2_evict_first_policy();
         for (int t = t0; t < t_end; ++t) {
             if (page >= 0 && page < p.num_pages) {  // boxes inside the pool only
-                tma_prefetch_l2_5d(&maps.k, 0, tip * kDecTile, 0, g, page);
-                tma_prefetch_l2_5d(&maps.v, 0, tip * kDecTile, 0, g, page);
+                tma_prefetch_l2_5d_hint(&maps.k, 0, tip * kDecTile, 0, g, page, pol);
+                tma_prefetch_l2_5d_hint(&maps.v, 0, tip * kDecTile, 0, g, page, pol);
             }
             if (++tip == tpp && t + 1 < t_end) {
                 tip = 0;

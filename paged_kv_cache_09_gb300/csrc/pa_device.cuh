@@ -166,14 +166,16 @@ __device__ __forceinline__ void tma_load_4d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
-// Prefetch of one 5-D box into L2 (no shared memory, no barrier).  A box outside the
-// tensor fetches nothing.
-__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap *m, int c0, int c1, int c2,
-                                                   int c3, int c4) {
-    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global [%0, {%1, %2, %3, %4, %5}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-                 : "memory");
+// Prefetch of one 5-D box into L2 with an L2 cache policy (no shared memory, no
+// barrier).  A box outside the tensor fetches nothing.
+__device__ __forceinline__ void tma_prefetch_l2_5d_hint(const CUtensorMap *m, int c0, int c1,
+                                                        int c2, int c3, int c4,
+                                                        uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.5d.L2.global.tile.L2::cache_hint"
+        " [%0, {%1, %2, %3, %4, %5}], %6;" ::"l"(reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
+        : "memory");
 }
 
 // 4-D tiled load of one box into shared memory, completing on `bar`.
