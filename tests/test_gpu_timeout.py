@@ -39,6 +39,8 @@ def test_lib(cuda_lib):
                               P, P, sz, P, P, P, P]
     lib.pa_prefill_chunk.argtypes = [P, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32, i32,
                                      f32, P, P, sz, P]
+    lib.pa_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_prefill_workspace_size.restype = sz
     lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, P]
     assert lib.pa_test_hook(-1, -1, 0) == PA_OK
     yield lib
@@ -70,14 +72,16 @@ def _decode(lib, case, max_seq_len):
     return out
 
 
-def _prefill(lib, case):
+def _prefill(lib, case, ws=None):
     q_len, hq, d = case.q.shape
     out = torch.empty_like(case.q)
     rc = lib.pa_prefill_chunk(case.q.data_ptr(), case.k_cache.data_ptr(),
                               case.v_cache.data_ptr(), case.k_cache.stride(0),
                               case.k_cache.shape[0], case.block_table[0].data_ptr(), q_len,
                               case.q_start, 1, hq, case.k_cache.shape[2], d, case.block_size,
-                              case.scale, out.data_ptr(), None, 0, _stream())
+                              case.scale, out.data_ptr(),
+                              None if ws is None else ws.data_ptr(),
+                              0 if ws is None else ws.numel(), _stream())
     assert rc == PA_OK
     return out
 
@@ -166,3 +170,32 @@ def test_decode_late_consumers_with_a_reloaded_stage(test_lib, cuda_lib, seq_len
     ref = oracle.decode(bits(case.q), k_ref, v_ref, case.block_table.cpu().numpy(),
                         case.seq_lens.cpu().numpy(), case.scale)
     assert_attention_close(out, ref, f"late consumers, reloaded stage, L={seq_len}")
+
+
+def test_prefill_split_and_packed_wait_that_runs_out(test_lib, cuda_lib):
+    # The extended prefill kernel (items split into pieces, a packed last tile) on the
+    # same failure path: one row over 8000 prior keys runs as 4 packed items cut into
+    # pieces, and every CTA loses its K/V ring unit 1.  The merge kernel then combines
+    # whatever the pieces left; the test checks the error and the next call.
+    lib = test_lib
+    q_len, q_start, bs = 1, 8000, 832
+    case = workloads.paged_case(378, [q_start + q_len], bs, 12, q_rows=q_len, q_start=q_start,
+                                device="cuda")
+    slots = cuda_lib.slot_mapping(case.positions, case.block_table, bs, seq_idx=case.seq_idx)
+    cuda_lib.reshape_and_cache(case.new_k, case.new_v, case.k_cache, case.v_cache, slots)
+    torch.cuda.synchronize()
+    need = lib.pa_prefill_workspace_size(q_len, q_start, 1, 24, 4, 256, bs)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert _errors(lib) == (PA_OK, 0)
+    assert lib.pa_test_hook(-1, 1, 0) == PA_OK
+    _prefill(lib, case, ws)
+    rc, errs = _errors(lib)
+    assert rc == PA_ERR_TIMEOUT and errs & DEVERR_TIMEOUT, (rc, errs)
+    assert lib.pa_test_hook(-1, -1, 0) == PA_OK
+    good = _prefill(lib, case, ws)
+    assert _errors(lib) == (PA_OK, 0)
+    ref = oracle.prefill(bits(case.q), bits(case.k_cache), bits(case.v_cache),
+                         case.block_table[0].cpu().numpy(), q_start, True, case.scale)
+    assert_attention_close(good, ref, "split, packed prefill after a timed-out call")
+    assert cuda_lib.device_errors() == 0
