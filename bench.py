@@ -596,6 +596,65 @@ def cpu_oracle_timing(case_h, seconds, num_threads=None):
     return el / n, n
 
 
+def timed_host(fn, seconds):
+    """Mean host seconds of fn() (after one untimed call), repeated until `seconds` pass."""
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return el / n, n
+
+
+def cpu_per_config(seconds):
+    """The fp64 oracle on the host cores for the other configurations, with the same
+    inputs as the GPU legs: the tiny decode (1701 keys), the 8K decode, the batched decode
+    (16 sequences, 1.3 GB of K/V) and a sample of the q=4096 chunk's outputs (every 64th
+    row, all 24 heads), each repeated for about `seconds`."""
+    import oracle
+    from workloads import bits
+    nt = oracle.max_threads()
+    r = {}
+    for name, make, label in (("tiny_decode_1701", workloads.tiny_decode, "1701 keys"),
+                              ("decode_8k", workloads.decode_8k, "8192 keys"),
+                              ("batched_decode_16", workloads.batched_decode,
+                               "16 sequences, 318,193 keys")):
+        c = make(device="cuda")
+        kv = (bits(c.k_cache), bits(c.v_cache))
+        h = dict(q=bits(c.q), k=kv[0], v=kv[1], block_table=c.block_table.cpu().numpy(),
+                 seq_lens=c.seq_lens.cpu().numpy(), scale=c.scale)
+        nbytes = int(c.seq_lens.sum().item()) * KV_BYTES_PER_TOKEN
+        del c, kv
+        torch.cuda.empty_cache()
+        sec, n = timed_host(oracle_decode_step(h), seconds)
+        r[name] = {"value": nbytes / sec / 1e9, "unit": "GB/s", "cores": nt,
+                   "ms_per_step": sec * 1e3,
+                   "sample": f"{n} full decode steps ({label}), fp64, {nt} threads"}
+        del h
+    c = workloads.prefill_chunk("cuda")
+    q, k, v = bits(c.q), bits(c.k_cache), bits(c.v_cache)
+    bt = c.block_table[0].cpu().numpy()
+    scale, q_start = c.scale, c.q_start
+    slots = oracle.slot_mapping(c.positions.cpu().numpy(), c.block_table.cpu().numpy(),
+                                c.block_size, seq_idx=c.seq_idx.cpu().numpy())
+    oracle.reshape_and_cache(bits(c.new_k), bits(c.new_v), k, v, slots, c.block_size)
+    del c
+    torch.cuda.empty_cache()
+    rows = np.repeat(np.arange(0, 4096, 64, dtype=np.int32), workloads.HQ)
+    heads = np.tile(np.arange(workloads.HQ, dtype=np.int32), 64)
+    flops = 4.0 * workloads.HEAD_DIM * float(np.sum(q_start + rows.astype(np.float64) + 1))
+    sec, n = timed_host(lambda: oracle.prefill_rows(q, k, v, bt, q_start, True, scale, rows,
+                                                    heads), seconds)
+    r["prefill_q4096_over_4096"] = {
+        "value": flops / sec / 1e9, "unit": "GFLOP/s", "cores": nt,
+        "sample": f"{n} passes over 64 of the chunk's 4096 rows (every 64th) x 24 heads, "
+                  f"fp64, {nt} threads; the whole chunk would take "
+                  f"{sec * 4096 / 64:.1f} s"}
+    return r
+
+
 def headline_workload(device):
     """The headline: the 7 sequences of 32768 keys a 1 GiB pool holds (BS 832, 5% of K
     rows x8), on disjoint pages; one step decodes one of them."""
@@ -831,7 +890,8 @@ def main():
                          f"{oracle.max_threads()} threads",
                "single_thread": {"value": nbytes / per_one / 1e9, "unit": "GB/s", "cores": 1,
                                  "ms_per_step": per_one * 1e3,
-                                 "sample": f"{n_one} steps of the same workload, one thread"}}
+                                 "sample": f"{n_one} steps of the same workload, one thread"},
+               "per_config": cpu_per_config(max(1.0, args.cpu_seconds / 4))}
 
     if rank != 0:
         return
