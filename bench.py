@@ -345,6 +345,7 @@ def decode_leg(pa, fns, tokens, seqs, steps, warmup, flush, peaks, rotation):
     r = {"context_tokens": tokens, "kv_bytes": nbytes, "ms_per_step": step_ms,
          "kv_gbs": nbytes / (step_ms * 1e-3) / 1e9,
          "split_kernel_ms": k_ms, "split_kernel_ms_min": min(kms),
+         "split_kernel_ms_median": statistics.median(kms),
          "split_kernel_gbs": nbytes / (k_ms * 1e-3) / 1e9,
          "tokens_per_s": seqs / (step_ms * 1e-3), "rotation": rotation}
     r["kv_pct_of_hbm_peak"] = 100.0 * r["kv_gbs"] / peaks["hbm_gbs"]
@@ -399,7 +400,7 @@ def prefill_leg(pa, steps, warmup, flush, peaks, make="prefill_chunk"):
     step_ms, k_ms = statistics.mean(ms), statistics.mean(kms)
     r = {"q_len": q_len, "q_start": q_start, "causal_flops": flops, "workspace_bytes": need,
          "ms_per_step": step_ms, "step_tflops": flops / (step_ms * 1e-3) / 1e12,
-         "kernel_ms": k_ms, "kernel_ms_min": min(kms),
+         "kernel_ms": k_ms, "kernel_ms_min": min(kms), "kernel_ms_median": statistics.median(kms),
          "kernel_tflops": flops / (k_ms * 1e-3) / 1e12}
     peak = peaks["bf16_tflops"]
     r["roofline"] = {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
@@ -762,7 +763,7 @@ def main():
         clocks.start()
 
     # ---- headline: timed K steps, barrier + synchronize on both sides
-    value = kernel_gbs = k_ms = e2e_val = e2e_ms = alone_ms = again_ms = None
+    value = kernel_gbs = k_ms = k_min = k_med = e2e_val = e2e_ms = alone_ms = again_ms = None
     step_ms = None
     h2d = d2h = 0
     head = None
@@ -784,6 +785,7 @@ def main():
         value = sum_over_ranks(nbytes_rank, ws) / (total_ms * 1e-3) / 1e9
         kms = time_main_kernel(pa, fns[0], args.steps, args.warmup, flush)
         k_ms = statistics.mean(kms)
+        k_min, k_med = min(kms), statistics.median(kms)
         kernel_gbs = HEADLINE_CTX * KV_BYTES_PER_TOKEN / (k_ms * 1e-3) / 1e9
         alone_ms = statistics.mean(time_steps(graph_of(fns[0]).replay, args.steps,
                                               args.warmup, flush))
@@ -927,7 +929,8 @@ def main():
                      "traffic_unit": "bytes per launch",
                      "kernel": "decode_split_kernel",
                      "algorithmic_bytes_per_launch": HEADLINE_CTX * KV_BYTES_PER_TOKEN,
-                     "kernel_ms": k_ms, "peak_source": f"{peaks['source']} hbm_gbs",
+                     "kernel_ms": k_ms, "kernel_ms_min": k_min, "kernel_ms_median": k_med,
+                     "peak_source": f"{peaks['source']} hbm_gbs",
                      "kernel_timing": "library events around the split launch of an eager "
                                       "step after an L2 flush, mean of K launches"},
         "cpu_baseline": cpu,
