@@ -25,7 +25,7 @@
 // Problems too large for the schedule arrays walk the items longest first in a snake
 // order instead (item k of CTA b: k*G + b for even k, k*G + G-1-b for odd k).
 //
-// Warp roles (320 threads):
+// Warp roles (576 threads):
 //   warp 0    TMA producer: the item's Q tile (4 boxes of 64 dims x 128 rows, 64 KB),
 //             then per tile four K units (one 64-dim chunk x 256 keys, 32 KB each) and
 //             four V units (64 keys x 256 dims) into a 5-slot ring of 32 KB.  Boxes are
@@ -42,8 +42,13 @@
 //             moves only when it grows by more than 8 (log2 units; then both warps
 //             rescale their half of the O row in TMEM).  Each warp writes P = P_hi + P_lo
 //             (two BF16 parts, so that P keeps ~16 significant bits) for its keys over
-//             that quarter of S.  At the end the pair adds its two partial row sums and
-//             each warp normalises and stores its half of O as BF16.
+//             that quarter of S.  At the end the pair adds its two partial row sums,
+//             hands them to the epilogue warps through shared memory and starts on its
+//             next item.
+//   warps 10-17 epilogue: two per TMEM lane quarter (128 O columns each); when an
+//             item's last PV is done, they load O into registers (BF16, normalised),
+//             release O to the next item's PVs, then store the rows to out (a piece of a
+//             split item: fp32 partials to the workspace).
 // TMEM columns: O [0, 256), S [256, 512); P of quarter q: hi at 256+64q, lo at +32.
 //
 // Every wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT, flags the CTA to
@@ -68,7 +73,8 @@ constexpr int kQChunk = kBM * 128;            // 64 dims x 128 rows: 16 KB
 constexpr int kQBytes = kChunks * kQChunk;    // 64 KB
 constexpr int kRing = kPfRing;
 constexpr int kSoftmaxWarps = 8;              // two per TMEM lane quarter
-constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
+constexpr int kEpilogueWarps = 8;             // two per TMEM lane quarter
+constexpr int kThreads = (2 + kSoftmaxWarps + kEpilogueWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;
 static_assert(kBN == 4 * kBlk && kBN == 256, "tile = four 64-key blocks");
@@ -80,7 +86,8 @@ constexpr int kOffQ = 0;
 constexpr int kOffRing = kQBytes;
 constexpr int kOffXchg = kOffRing + kRing * kUnit;  // row maxima / sums of warp pairs
 constexpr int kXchgBytes = 4 * 2 * 2 * 32 * 4;      // [lane quarter][phase][half][lane]
-constexpr int kOffBars = kOffXchg + kXchgBytes;
+constexpr int kOffRowSum = kOffXchg + kXchgBytes;   // an item's row sums, to the epilogue
+constexpr int kOffBars = kOffRowSum + kBM * 4;
 enum Bar {
     kRingFull = 0,
     kRingEmpty = kRingFull + kRing,
@@ -90,6 +97,7 @@ enum Bar {
     kPFull,               // [4] quarters
     kPvDone = kPFull + 4, // [4] quarters
     kOEmpty = kPvDone + 4,
+    kEpiReady,            // the softmax warps handed an item's row sums to the epilogue
     kDrain,
     kPair,                // [4] the two softmax warps of a lane quarter meet here
     kNumBars = kPair + 4
@@ -244,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *qs = smem + kOffQ;
     uint8_t *ring = smem + kOffRing;
     float *xchg = reinterpret_cast<float *>(smem + kOffXchg);
+    float *rowsum = reinterpret_cast<float *>(smem + kOffRowSum);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -264,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[kPvDone + i], 1);
             mbar_init(&bars[kPair + i], 2);
         }
-        mbar_init(&bars[kOEmpty], kSoftmaxWarps);
+        mbar_init(&bars[kOEmpty], kEpilogueWarps);
+        mbar_init(&bars[kEpiReady], kSoftmaxWarps / 2);  // one warp of each pair
         mbar_init(&bars[kDrain], 1);
         *abort = 0;
         fence_mbar_init();
@@ -456,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&bars[kDrain]);
             mbar_wait(&bars[kDrain], 0, p.err);
         }
-    } else {
-        // ------------------------------------------------------------ softmax + epilogue
+    } else if (warp < 2 + kSoftmaxWarps) {
+        // ------------------------------------------------------------ softmax
         // Two warps per TMEM lane quarter: warp sw (0..7) owns rows 32*(warp % 4) + lane
         // and half hf = sw / 4 of every 64-key quarter (keys 32*hf .. 32*hf + 31) and of
         // the O columns (128*hf .. 128*hf + 127).  The pair agrees on each quarter's row
@@ -493,14 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
         bool stop = false;
         for (int k = 0; !stop && (item_of<kSeqs, kExt>(p, k, it)); ++k) {
-            // This lane's query row: tile row rpos of head rhead (lanes of a packed item
-            // past G * rows, and rows past the chunk's end, are computed but not stored).
-            int rpos = row, rhead = it.h;
+            // This lane's query row is tile row rpos (of head it.h + row % G in a packed
+            // item; lanes past G * rows, and rows past the chunk's end, are computed but
+            // not stored).
+            int rpos = row;
             if constexpr (kExt) {
-                if (it.pk) {
-                    rpos = row / p.group;
-                    rhead = it.h + (row - rpos * p.group);
-                }
+                if (it.pk) rpos = row / p.group;
             }
             const int qpos = it.q_start + it.r0 + rpos;
             float m_used = -CUDART_INF_F, l = 0.f;
@@ -626,61 +634,106 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (stop) break;
-            // epilogue: the row sum is the pair's two partial sums; wait for the item's
-            // last PV, normalise this warp's half of the row and store it as BF16.
+            // The row sum is the pair's two partial sums.  One warp of the pair hands it to
+            // the epilogue warps (and, for a piece, stores the row's running max and sum
+            // to the workspace), and the pair goes on with its next item at once.  The
+            // epilogue reads the sums before it releases O, and the next item's sums are
+            // written only after that item's first PV, which waits for that release.
             bool ok = true;
             const float lt = l + exchange(l, ok);
-            if (!__all_sync(0xffffffffu, ok &&
-                                             mbar_wait_abort(&bars[kPvDone + 3],
-                                                             (jt + (it.je - it.jb) - 1) & 1,
-                                                           p.err, abort)))
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (hf == 0) {
+                rowsum[row] = lt;
+                if (kExt && it.slot >= 0 && rpos < it.rows)
+                    p.ws_ml[(int64_t)it.slot * kBM + row] = make_float2(m_used, lt);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kEpiReady]);
+            }
+            jt += it.je - it.jb;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // Two warps per TMEM lane quarter: warp ew (0..7) takes rows 32*(warp % 4) + lane
+        // and O columns 128*eh .. 128*eh + 127, eh = ew / 4.  Once the softmax warps have
+        // handed over an item's row sums and its last PV is done, a whole item's warp
+        // loads its 128 columns (four loads of 32), normalises them into BF16 registers,
+        // releases O to the next item's PVs and only then stores its rows to out: the next
+        // item's first PV waits for that release.  A piece of a split item keeps fp32 (its
+        // unnormalised partial goes to the workspace slot, and the merge kernel combines
+        // the item's pieces), so it stores each column block as it loads it and releases
+        // O after the last load.  (tcgen05.ld is warp-wide: every lane loads; only rows
+        // present store.)
+        const int lq = warp & 3;
+        const int eh = (warp - 2 - kSoftmaxWarps) >> 2;
+        const int row = lq * 32 + lane;
+        const uint32_t obase = tmem + ((uint32_t)(lq * 32) << 16) + kColO + 128 * eh;
+        uint32_t jt = 0;
+        Item it;
+        for (int k = 0; item_of<kSeqs, kExt>(p, k, it); ++k) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_abort(&bars[kEpiReady], k & 1, p.err, abort) &&
+                                mbar_wait_abort(&bars[kPvDone + 3],
+                                                (jt + (it.je - it.jb) - 1) & 1, p.err, abort)))
                 break;
             tc_fence_after();
-            // Whole item: this warp's half of the row, normalised, as BF16 to out.  A piece
-            // of a split item: this warp's half of the row's unnormalised O and, from one
-            // warp of the pair, the row's running max (base-2 units) and sum of weights,
-            // to the piece's workspace slot; the merge kernel combines the item's pieces.
-            // (tcgen05.ld is warp-wide: every lane loads; only rows present store.)
-            const bool piece = kExt && it.slot >= 0;
-            const float inv = piece ? 1.f : (lt > 0.f ? 1.f / lt : 0.f);
-            uint16_t *dst =
-                p.out + ((int64_t)(it.q_off + it.r0 + rpos) * p.num_q_heads + rhead) * kHeadDim +
-                128 * hf;
-            float *po = p.ws_o + ((int64_t)it.slot * kBM + row) * kHeadDim + 128 * hf;
-            const bool present = rpos < it.rows;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(obase + 32 * c, r);
-                tc_wait_ld();
-                if (present && piece) {
-                    float4 *d4 = reinterpret_cast<float4 *>(po + 32 * c);
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        d4[q4] = make_float4(__uint_as_float(r[4 * q4]),
-                                             __uint_as_float(r[4 * q4 + 1]),
-                                             __uint_as_float(r[4 * q4 + 2]),
-                                             __uint_as_float(r[4 * q4 + 3]));
-                } else if (present) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        d4[q4] = make_uint4(
-                            pack_bf16x2(__uint_as_float(r[8 * q4]) * inv,
-                                        __uint_as_float(r[8 * q4 + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * inv,
-                                        __uint_as_float(r[8 * q4 + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * inv,
-                                        __uint_as_float(r[8 * q4 + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * inv,
-                                        __uint_as_float(r[8 * q4 + 7]) * inv));
+            const float lt = rowsum[row];
+            int rpos = row, rhead = it.h;
+            if constexpr (kExt) {
+                if (it.pk) {
+                    rpos = row / p.group;
+                    rhead = it.h + (row - rpos * p.group);
                 }
             }
-            if (piece && present && hf == 0)
-                p.ws_ml[(int64_t)it.slot * kBM + row] = make_float2(m_used, lt);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kOEmpty]);
+            const bool present = rpos < it.rows;
+            if (kExt && it.slot >= 0) {
+                float *po = p.ws_o + ((int64_t)it.slot * kBM + row) * kHeadDim + 128 * eh;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(obase + 32 * c, r);
+                    tc_wait_ld();
+                    if (c == 3) {  // O is read: the next item may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[kOEmpty]);
+                    }
+                    if (present) {
+                        float4 *d4 = reinterpret_cast<float4 *>(po + 32 * c);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            d4[q4] = make_float4(__uint_as_float(r[4 * q4]),
+                                                 __uint_as_float(r[4 * q4 + 1]),
+                                                 __uint_as_float(r[4 * q4 + 2]),
+                                                 __uint_as_float(r[4 * q4 + 3]));
+                    }
+                }
+            } else {
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                uint32_t b[64];  // this warp's 128 columns of the row as BF16 pairs
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(obase + 16 * c, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        b[8 * c + i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv,
+                                                   __uint_as_float(r[2 * i + 1]) * inv);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kOEmpty]);  // O is read
+                if (present) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(
+                        p.out +
+                        ((int64_t)(it.q_off + it.r0 + rpos) * p.num_q_heads + rhead) * kHeadDim +
+                        128 * eh);
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; ++q4)
+                        d4[q4] = make_uint4(b[4 * q4], b[4 * q4 + 1], b[4 * q4 + 2],
+                                            b[4 * q4 + 3]);
+                }
+            }
             jt += it.je - it.jb;
         }
     }
