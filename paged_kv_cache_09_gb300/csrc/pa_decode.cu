@@ -189,7 +189,9 @@ __device__ int g_test_consumer_delay_ns = 0;
 // because some prefetched lines stayed in L2 until the same sequence came round again;
 // an ncu capture of such a rotation saw a 32K launch read 4.5 of its 134 MB from L2.
 // Four tiles gained more than two; eight or sixteen were slower (the prefetch outlasts
-// the wait and delays the first loads).
+// the wait and delays the first loads); six were 1% faster in the 8K sweep but 2-4%
+// slower in the 8K legs that rotate 32 copies of a 64-page pool, and in the kernel timed
+// alone.
 constexpr int kDecPrefetchTiles = 4;
 
 template <int kDecConsumers, int kDecStages>
