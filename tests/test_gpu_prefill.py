@@ -347,6 +347,7 @@ def test_prefill_varlen_split_items_over_two_launches(cuda_lib):
     (24, 4, 21, 700, 832), (24, 4, 22, 700, 832), (24, 4, 149, 900, 784),
     (8, 4, 64, 300, 64), (8, 4, 65, 300, 64), (8, 1, 136, 1000, 832),
     (16, 2, 16, 2000, 16), (4, 4, 1, 900, 832), (32, 4, 16, 0, 832),
+    (24, 8, 40, 500, 832), (20, 4, 25, 300, 64), (28, 4, 146, 1000, 784),
 ])
 def test_prefill_packed_last_tile_every_element(cuda_lib, hq, hkv, q_len, q_start, bs):
     pa = cuda_lib
