@@ -301,14 +301,14 @@ int pa_prefill_varlen(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v
  *
  * Work items run from the chunk's last query tile (the longest under causal masking) to
  * its first; within a tile, one item per query head: item i is the 128 query rows of tile
- * ceil(q_len / 128) - 1 - i / num_q_heads of head i % num_q_heads.  One exception, with
- * G = num_q_heads / num_kv_heads > 1: when the last tile's r rows satisfy r <= 128 / G,
- * that tile runs as num_kv_heads packed items (items 0 .. num_kv_heads - 1, then the
- * other tiles as above, shifted): packed item g holds the r rows of all G query heads of
- * KV head g (its row x is tile row x / G of query head g * G + x % G).  An item's cost is
- * the number of 256-key tiles it reads (64-key page-local blocks, four per tile) plus
- * one.  pa_prefill_chunk runs min(num_ctas, items) persistent CTAs, with num_ctas = the
- * device's SM count.
+ * ceil(q_len / 128) - 1 - i / num_q_heads of head i % num_q_heads.  One exception: the
+ * last tile, of r rows, runs as items of hp query heads, hp the largest divisor of
+ * G = num_q_heads / num_kv_heads with hp * r <= 128, when that is more than 1 (items
+ * 0 .. num_q_heads / hp - 1, then the other tiles as above, shifted): packed item j holds
+ * the r rows of query heads j*hp .. j*hp + hp - 1, which share one KV head (its row x is
+ * tile row x / hp of query head j*hp + x % hp).  An item's cost is the number of 256-key
+ * tiles it reads (64-key page-local blocks, four per tile) plus one.  pa_prefill_chunk
+ * runs min(num_ctas, items) persistent CTAs, with num_ctas = the device's SM count.
  *   cta_of_item  int32 [items] (host) or NULL: the CTA each item runs on
  *   num_items    (host, or NULL) the item count
  *   max_cost     (host, or NULL) the largest per-CTA total cost

@@ -493,16 +493,22 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
                           pa_bf16 *out, void *workspace, size_t workspace_bytes,
                           const DeviceInfo &dev, cudaEvent_t ev_start, cudaEvent_t ev_stop,
                           cudaStream_t stream) {
-    CUtensorMap maps[4 + 2 * pa::kPfMaxSeqs];
+    constexpr int kM = 3 + pa::kPfMaxPackMaps;  // index of the first per-sequence map
+    CUtensorMap maps[kM + 2 * pa::kPfMaxSeqs];
     const int group = num_q_heads / num_kv_heads;
-    const int pack_rows = pa::prefill_pack_rows(group);
-    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, total_q, 1, pa::kPfQRows) ||
-        !(pack_rows > 0
-              ? make_rows_map(&maps[1], q, head_dim, num_q_heads, total_q, group, pack_rows)
-              : make_rows_map(&maps[1], q, head_dim, num_q_heads, total_q, 1, pa::kPfQRows)) ||
-        !make_cache_map(&maps[2], k_cache, head_dim, num_kv_heads, block_size, num_pages,
+    if (!make_rows_map(&maps[0], q, head_dim, num_q_heads, total_q, 1, pa::kPfQRows))
+        return PA_ERR_CUDA;
+    // Q for packed items: one map per divisor hp > 1 of the group, largest first.
+    int npack = 0;
+    for (int hp = group; hp > 1 && npack < pa::kPfMaxPackMaps; --hp)
+        if (group % hp == 0 &&
+            !make_rows_map(&maps[1 + npack++], q, head_dim, num_q_heads, total_q, hp,
+                           pa::kPfQRows / hp))
+            return PA_ERR_CUDA;
+    for (int i = npack; i < pa::kPfMaxPackMaps; ++i) maps[1 + i] = maps[0];
+    if (!make_cache_map(&maps[kM - 2], k_cache, head_dim, num_kv_heads, block_size, num_pages,
                         page_stride, pa::kPfBlock) ||
-        !make_cache_map(&maps[3], v_cache, head_dim, num_kv_heads, block_size, num_pages,
+        !make_cache_map(&maps[kM - 1], v_cache, head_dim, num_kv_heads, block_size, num_pages,
                         page_stride, pa::kPfBlock))
         return PA_ERR_CUDA;
     for (int b = 0; b < nseq; ++b) {
@@ -510,9 +516,9 @@ static int prefill_launch(const pa_bf16 *q, int total_q, const pa_bf16 *k_cache,
         // so rows past it come back as zeros.
         const int seq_len_k = seqs[b].q_start + seqs[b].q_len;
         const int last_rows = seq_len_k - ((seq_len_k - 1) / block_size) * block_size;
-        if (!make_cache_map(&maps[4 + 2 * b], k_cache, head_dim, num_kv_heads, last_rows,
+        if (!make_cache_map(&maps[kM + 2 * b], k_cache, head_dim, num_kv_heads, last_rows,
                             num_pages, page_stride, pa::kPfBlock) ||
-            !make_cache_map(&maps[5 + 2 * b], v_cache, head_dim, num_kv_heads, last_rows,
+            !make_cache_map(&maps[kM + 1 + 2 * b], v_cache, head_dim, num_kv_heads, last_rows,
                             num_pages, page_stride, pa::kPfBlock))
             return PA_ERR_CUDA;
     }

@@ -170,42 +170,45 @@ __host__ __device__ inline int prefill_item_tiles(int q_len, int q_start, int ca
 }
 
 // Packed last query tile.  A chunk's last query tile holds r = q_len - 128 * (tiles - 1)
-// rows.  When r <= 128 / G (G = Hq / Hkv query heads per KV head, G > 1), those rows of
-// all G query heads of one KV head fit one 128-row item: item row x is tile row x / G of
-// query head g * G + x % G (Q read as one box of G heads x 128 / G rows).  The tile then
-// runs as Hkv items instead of Hq items that would be mostly empty rows (the q=1685 tail
-// chunk: 21 rows, 4 items instead of 24; a one-row chunk: 4 items of 6 rows).
-__host__ __device__ inline int prefill_pack_rows(int group) {
-    return group > 1 ? kPfQRows / group : 0;
+// rows.  It runs as items of hp query heads each, hp the largest divisor of the GQA group
+// G = Hq / Hkv with hp * r <= 128 (hp = 1: one head per item, not packed): item row x is
+// tile row x / hp of query head h0 + x % hp, and Q is read as one box of hp heads x
+// 128 / hp rows.  The hp heads of an item share one KV head (hp divides G), so the tile
+// runs as Hq / hp items instead of Hq items of r rows: the q=1685 tail chunk (21 rows,
+// G = 6) as 4 items instead of 24, a 40-row tail as 8 (hp = 3), a 60-row tail as 12.
+constexpr int kPfMaxPackMaps = 3;  // divisors > 1 of a group of at most 8: {8, 4, 2}, {6, 3, 2}
+__host__ __device__ inline int prefill_tile_heads(int q_len, int group) {
+    const int r = q_len - ((q_len - 1) / kPfQRows) * kPfQRows;  // rows of the last tile
+    for (int hp = group; hp > 1; --hp)
+        if (group % hp == 0 && hp * r <= kPfQRows) return hp;
+    return 1;
 }
-__host__ __device__ inline bool prefill_last_tile_packed(int q_len, int group) {
-    return q_len - ((q_len - 1) / kPfQRows) * kPfQRows <= prefill_pack_rows(group);
-}
-// Work items of one chunk, and what item i of it is: query tile *qt, and query head *h
-// (for the packed item, KV head *h); returns whether item i is the packed one.  Items run
-// from the chunk's last (longest, under causal masking) query tile to its first.
+// Work items of one chunk, and what item i of it is: query tile *qt, its first query
+// head *h0 and its heads *hp (1 unless it is one of the packed last tile's items).  Items
+// run from the chunk's last (longest, under causal masking) query tile to its first.
 __host__ __device__ inline int prefill_chunk_items(int q_len, int num_q_heads, int group) {
     const int nqt = (q_len + kPfQRows - 1) / kPfQRows;
-    return prefill_last_tile_packed(q_len, group) ? (nqt - 1) * num_q_heads + num_q_heads / group
-                                                  : nqt * num_q_heads;
+    return (nqt - 1) * num_q_heads + num_q_heads / prefill_tile_heads(q_len, group);
 }
-__host__ __device__ inline bool prefill_item_at(int i, int q_len, int num_q_heads, int group,
-                                                int *qt, int *h) {
+__host__ __device__ inline void prefill_item_at(int i, int q_len, int num_q_heads, int group,
+                                                int *qt, int *h0, int *hp) {
     const int nqt = (q_len + kPfQRows - 1) / kPfQRows;
-    if (prefill_last_tile_packed(q_len, group)) {
-        const int num_kv_heads = num_q_heads / group;
-        if (i < num_kv_heads) {
+    const int php = prefill_tile_heads(q_len, group);
+    if (php > 1) {
+        const int n_last = num_q_heads / php;
+        if (i < n_last) {
             *qt = nqt - 1;
-            *h = i;
-            return true;
+            *h0 = i * php;
+            *hp = php;
+            return;
         }
-        i -= num_kv_heads;
+        i -= n_last;
         *qt = nqt - 2 - i / num_q_heads;
     } else {
         *qt = nqt - 1 - i / num_q_heads;
     }
-    *h = i % num_q_heads;
-    return false;
+    *h0 = i % num_q_heads;
+    *hp = 1;
 }
 
 // Static assignment of prefill work items to the persistent CTAs (items numbered as
@@ -283,9 +286,10 @@ struct PrefillArgs {
     int num_sms;                    // persistent grid size bound
 };
 
-// tmaps: Q (boxes of 1 head x 128 rows), Q for packed items (G heads x 128 / G rows;
-// a copy of the first when the group does not pack), K, V, then the K and V maps cut at
-// each sequence's last token (2 per sequence).
+// tmaps: Q (boxes of 1 head x 128 rows); kPfMaxPackMaps maps of Q for packed items, one
+// per divisor hp > 1 of the group, largest first (boxes of hp heads x 128 / hp rows;
+// copies of the first map where the group has fewer such divisors); K, V; then the K and
+// V maps cut at each sequence's last token (2 per sequence).
 cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaStream_t stream);
 
 #ifdef PA_TEST_HOOKS

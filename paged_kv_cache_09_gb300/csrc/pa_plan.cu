@@ -1,7 +1,7 @@
 // pa_plan.cu -- static work assignment for the persistent prefill kernel (host only).
 //
-// The causal chunk's work items (128 query rows of one head, or of the GQA group's heads
-// for a packed last tile) differ in length: row tile r of a chunk at q_start reads
+// The causal chunk's work items (128 query rows of one head, or of several heads of a
+// GQA group for a packed last tile) differ in length: row tile r of a chunk at q_start reads
 // q_start + r*128 + 128 keys.  With about five items per
 // CTA, walking them in a fixed order leaves some CTAs well above the mean (the q=4096
 // chunk over 4096 prior tokens: 138 tiles on the busiest CTA against a mean of 123.8).
@@ -165,8 +165,8 @@ void compute_plan(const PlanKey &k, CachedPlan &out) {
     for (const auto &c : k.chunks) {
         const int n = prefill_chunk_items(c.first, k.hq, k.group);
         for (int i = 0; i < n; ++i) {
-            int qt, h;
-            prefill_item_at(i, c.first, k.hq, k.group, &qt, &h);
+            int qt, h0, hp;
+            prefill_item_at(i, c.first, k.hq, k.group, &qt, &h0, &hp);
             cost.push_back(prefill_item_tiles(c.first, c.second, k.causal, qt * kPfQRows, k.bs) +
                            1);
         }

@@ -15,11 +15,11 @@
 // the PV of quarter q runs while the softmax of quarter q+1 is computed, and the tensor
 // core only waits for the softmax of each tile's first quarter.
 //
-// Work item = (128 query rows of one head).  A chunk's last query tile, when its r rows
-// times the GQA group G fit 128 rows, runs instead as one packed item per KV head: its
-// TMEM lane x holds tile row x / G of query head g*G + x % G (Q comes in as boxes of G
-// heads x 128/G rows), so the six heads of a group share one pass over their K/V rather
-// than each taking a 128-row item with r rows present.  Persistent CTAs, one per SM, run the items
+// Work item = (128 query rows of one head).  A chunk's last query tile of r rows runs
+// instead as packed items of hp heads, hp the largest divisor of the GQA group G with
+// hp * r <= 128: TMEM lane x holds tile row x / hp of query head h0 + x % hp (Q comes in
+// as boxes of hp heads x 128/hp rows), so the heads of a group share passes over their
+// K/V rather than each taking a 128-row item with r rows present.  Persistent CTAs, one per SM, run the items
 // the host planner assigned to them (a static schedule that balances the causal items'
 // unequal lengths across CTAs, passed in the kernel parameters), longest first.
 // Problems too large for the schedule arrays walk the items longest first in a snake
@@ -134,7 +134,9 @@ struct TcParams {
     int64_t bt_stride;
     int causal, num_seqs, num_items;
     int num_q_heads, group;
-    int qp_bytes;         // bytes of a packed item's Q tile (G heads x 128/G rows)
+    // packed items: heads per item of each packed Q map, and the bytes of its Q tile
+    // (hp heads x 128/hp rows, four 64-dim chunks); 0 past the group's divisors
+    int qp_hp[kPfMaxPackMaps], qp_bytes[kPfMaxPackMaps];
     int block_size, blocks_per_page;
     int64_t num_pages;
     float sc;             // |scale| * log2(e), at least FLT_MIN
@@ -150,7 +152,9 @@ struct TcParams {
 
 template <int kSeqs>
 struct TcMaps {
-    CUtensorMap q, qp, k, v;  // qp: Q in boxes of G heads x 128/G rows (packed items)
+    CUtensorMap q;
+    CUtensorMap qp[kPfMaxPackMaps];  // Q in boxes of hp heads x 128/hp rows (packed items)
+    CUtensorMap k, v;
     CUtensorMap k_last[kSeqs], v_last[kSeqs];  // cut at each sequence's last token
 };
 
@@ -158,10 +162,11 @@ static_assert(sizeof(TcMaps<kPfMaxSeqs>) + sizeof(TcParams<kPfMaxSeqs, true>) <=
               "the kernel's parameters fit the 32 KB parameter space");
 
 struct Item {
-    // head (the first of the group for a packed item), KV head, first row of the query
+    // head (the first of its heads for a packed item), KV head, first row of the query
     // tile, its rows present (per head), key blocks, tiles
     int h, g, r0, rows, nblocks, n;
-    bool pk;  // packed: lane x holds tile row x / G of head h + x % G
+    int hp;   // heads of the item: 1, or a packed item's (lane x: row x / hp, head h + x % hp)
+    int qpi;  // a packed item's Q map
     int b, q_off, q_start, seq_len_k, last_page, bt_row;  // its sequence
     // The tiles [jb, je) this CTA runs: all n of a whole item, or one piece's range; a
     // piece writes its partial to workspace slot `slot` (-1: a whole item, normalised
@@ -196,17 +201,16 @@ __device__ __forceinline__ bool item_of(const TcParams<kSeqs, kExt> &p, int k, I
     const SeqInfo &sq = p.seq[sb];
     const int local = idx - sq.item_off;
     int qt;
+    it.qpi = 0;
     if constexpr (kExt) {
-        int hh;
-        it.pk = prefill_item_at(local, sq.q_len, p.num_q_heads, p.group, &qt, &hh);
-        it.g = it.pk ? hh : hh / p.group;
-        it.h = it.pk ? hh * p.group : hh;
+        prefill_item_at(local, sq.q_len, p.num_q_heads, p.group, &qt, &it.h, &it.hp);
+        while (it.qpi + 1 < kPfMaxPackMaps && p.qp_hp[it.qpi] != it.hp) ++it.qpi;
     } else {  // no packed tile: item i is tile nqt - 1 - i / Hq of head i % Hq
         qt = (sq.q_len + kBM - 1) / kBM - 1 - local / p.num_q_heads;
-        it.pk = false;
         it.h = local % p.num_q_heads;
-        it.g = it.h / p.group;
+        it.hp = 1;
     }
+    it.g = it.h / p.group;
     it.r0 = qt * kBM;
     it.rows = min(kBM, sq.q_len - it.r0);
     it.b = sb;
@@ -315,12 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; !stop && (item_of<kSeqs, kExt>(p, k, it)); ++k) {
                 if (k > 0 && !mbar_wait_abort(&bars[kQEmpty], (k - 1) & 1, p.err, abort)) break;
                 ++q_loads;
-                const bool pk = kExt && it.pk;
-                mbar_arrive_expect_tx(&bars[kQFull], pk ? p.qp_bytes : kQBytes);
+                const bool pk = kExt && it.hp > 1;
+                mbar_arrive_expect_tx(&bars[kQFull], pk ? p.qp_bytes[it.qpi] : kQBytes);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(qs + c * kQChunk, pk ? &maps.qp : &maps.q, &bars[kQFull],
-                                c * kChunkElems, it.h, it.q_off + it.r0);
+                    tma_load_3d(qs + c * kQChunk, pk ? &maps.qp[it.qpi] : &maps.q,
+                                &bars[kQFull], c * kChunkElems, it.h, it.q_off + it.r0);
                 const int32_t *bt = p.block_table + (int64_t)it.bt_row * p.bt_stride;
                 // Page and in-page index of block kb, advanced block by block: a division
                 // per block would take the MUFU, which the softmax warps keep busy (one
@@ -503,12 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
         bool stop = false;
         for (int k = 0; !stop && (item_of<kSeqs, kExt>(p, k, it)); ++k) {
-            // This lane's query row is tile row rpos (of head it.h + row % G in a packed
-            // item; lanes past G * rows, and rows past the chunk's end, are computed but
+            // This lane's query row is tile row rpos (of head it.h + row % hp in a packed
+            // item; lanes past hp * rows, and rows past the chunk's end, are computed but
             // not stored).
             int rpos = row;
             if constexpr (kExt) {
-                if (it.pk) rpos = row / p.group;
+                if (it.hp > 1) rpos = row / it.hp;
             }
             const int qpos = it.q_start + it.r0 + rpos;
             float m_used = -CUDART_INF_F, l = 0.f;
@@ -679,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float lt = rowsum[row];
             int rpos = row, rhead = it.h;
             if constexpr (kExt) {
-                if (it.pk) {
-                    rpos = row / p.group;
-                    rhead = it.h + (row - rpos * p.group);
+                if (it.hp > 1) {
+                    rpos = row / it.hp;
+                    rhead = it.h + (row - rpos * it.hp);
                 }
             }
             const bool present = rpos < it.rows;
@@ -766,9 +770,9 @@ constexpr int kMergeThreads = kMergeRows * kMergeThreadsPerRow;
 constexpr int kMergeRound = 4;  // pieces whose loads are in flight together
 struct MergeSplit {
     int out_row0;   // the item's first row in out
-    int rows;       // its rows present (TMEM lanes: rows x G for a packed item)
+    int rows;       // its rows present (TMEM lanes: rows x hp for a packed item)
     int head;       // its head (the group's first, for a packed item)
-    int pack;       // G for a packed item (lane x: row x / G, head + x % G), else 0
+    int pack;       // hp for a packed item (lane x: row x / hp, head + x % hp), else 0
     int slot0, npieces;
 };
 struct MergeParams {
@@ -865,10 +869,11 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
         reinterpret_cast<const void *>(prefill_tc_kernel<kSeqs, kExt>), kSmemBytes, slot);
     if (e != cudaSuccess) return e;
     TcMaps<kSeqs> maps;
+    constexpr int kM = 3 + kPfMaxPackMaps;  // the first per-sequence map
     maps.q = tmaps[0];
-    maps.qp = tmaps[1];
-    maps.k = tmaps[2];
-    maps.v = tmaps[3];
+    for (int i = 0; i < kPfMaxPackMaps; ++i) maps.qp[i] = tmaps[1 + i];
+    maps.k = tmaps[kM - 2];
+    maps.v = tmaps[kM - 1];
     TcParams<kSeqs, kExt> p;
     p.block_table = a.block_table;
     p.bt_stride = a.bt_stride;
@@ -877,8 +882,8 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     int items = 0;
     for (int b = 0; b < a.num_seqs; ++b) {
         const PrefillSeq &sq = a.seqs[b];
-        maps.k_last[b] = tmaps[4 + 2 * b];
-        maps.v_last[b] = tmaps[5 + 2 * b];
+        maps.k_last[b] = tmaps[kM + 2 * b];
+        maps.v_last[b] = tmaps[kM + 1 + 2 * b];
         SeqInfo &si = p.seq[b];
         si.q_off = sq.q_off;
         si.q_len = sq.q_len;
@@ -892,7 +897,15 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
     p.num_items = items;
     p.num_q_heads = a.num_q_heads;
     p.group = a.group;
-    p.qp_bytes = kChunks * 128 * a.group * prefill_pack_rows(a.group);
+    // The packed Q maps' heads per item: the group's divisors > 1, largest first (as the
+    // maps were made).
+    int npack = 0;
+    for (int hp = a.group; hp > 1 && npack < kPfMaxPackMaps; --hp)
+        if (a.group % hp == 0) {
+            p.qp_hp[npack] = hp;
+            p.qp_bytes[npack++] = kChunks * 128 * hp * (kBM / hp);
+        }
+    for (; npack < kPfMaxPackMaps; ++npack) p.qp_hp[npack] = p.qp_bytes[npack] = 0;
     p.block_size = a.block_size;
     p.blocks_per_page = (a.block_size + kBlk - 1) / kBlk;
     p.num_pages = a.num_pages;
@@ -939,14 +952,13 @@ cudaError_t launch_prefill_n(const CUtensorMap *tmaps, const PrefillArgs &a, int
             int b = 0;
             while (b + 1 < a.num_seqs && idx >= p.seq[b + 1].item_off) ++b;
             const SeqInfo &sq = p.seq[b];
-            int qt, hh;
-            const bool pk =
-                prefill_item_at(idx - sq.item_off, sq.q_len, a.num_q_heads, a.group, &qt, &hh);
+            int qt, h0, hp;
+            prefill_item_at(idx - sq.item_off, sq.q_len, a.num_q_heads, a.group, &qt, &h0, &hp);
             const int rows = min(kBM, sq.q_len - qt * kBM);
             mp.s[x].out_row0 = sq.q_off + qt * kBM;
-            mp.s[x].rows = pk ? rows * a.group : rows;
-            mp.s[x].head = pk ? hh * a.group : hh;
-            mp.s[x].pack = pk ? a.group : 0;
+            mp.s[x].rows = rows * hp;
+            mp.s[x].head = h0;
+            mp.s[x].pack = hp > 1 ? hp : 0;
             mp.s[x].slot0 = a.sched->split_slot0[x];
             mp.s[x].npieces = a.sched->split_n[x];
         }
@@ -966,7 +978,7 @@ cudaError_t launch_prefill(const CUtensorMap *tmaps, const PrefillArgs &a, cudaS
     // packed query tile.
     bool ext = a.sched && a.sched->num_ctas > 0 && a.sched->num_pieces > 0;
     for (int b = 0; b < a.num_seqs; ++b)
-        ext = ext || prefill_last_tile_packed(a.seqs[b].q_len, a.group);
+        ext = ext || prefill_tile_heads(a.seqs[b].q_len, a.group) > 1;
     if (a.num_seqs == 1)
         return ext ? launch_prefill_n<1, true>(tmaps, a, 4, stream)
                    : launch_prefill_n<1, false>(tmaps, a, 1, stream);

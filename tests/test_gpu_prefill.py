@@ -343,11 +343,14 @@ def test_prefill_varlen_split_items_over_two_launches(cuda_lib):
 
 
 @pytest.mark.parametrize("hq,hkv,q_len,q_start,bs", [
-    # a short last query tile runs as one item per KV head holding all G heads' rows
+    # a short last query tile runs as items of several heads of a KV head
     (24, 4, 21, 700, 832), (24, 4, 22, 700, 832), (24, 4, 149, 900, 784),
     (8, 4, 64, 300, 64), (8, 4, 65, 300, 64), (8, 1, 136, 1000, 832),
     (16, 2, 16, 2000, 16), (4, 4, 1, 900, 832), (32, 4, 16, 0, 832),
     (24, 8, 40, 500, 832), (20, 4, 25, 300, 64), (28, 4, 146, 1000, 784),
+    # tails too long for the whole group: 3 heads per item (22..42 rows), 2 (43..64)
+    (24, 4, 40, 8000, 832), (24, 4, 60, 900, 784), (24, 4, 128 + 30, 2000, 64),
+    (32, 4, 20, 1000, 832), (16, 4, 40, 3000, 832), (24, 4, 64, 7000, 832),
 ])
 def test_prefill_packed_last_tile_every_element(cuda_lib, hq, hkv, q_len, q_start, bs):
     pa = cuda_lib

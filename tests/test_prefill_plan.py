@@ -22,15 +22,21 @@ def item_tiles(q_len, q_start, causal, r0, bs):
     return math.ceil(nblocks / 4)
 
 
+def tile_heads(q_len, G):
+    """Heads per item of a chunk's last query tile: the largest divisor hp of G with
+    hp * r <= 128 (r: the tile's rows), 1 if none is above 1."""
+    r = q_len - 128 * (math.ceil(q_len / 128) - 1)
+    return next((hp for hp in range(G, 1, -1) if G % hp == 0 and hp * r <= 128), 1)
+
+
 def item_costs(q_len, q_start, causal, hq, bs, hkv=4):
-    # Items from the last query tile to the first, one per head; a last tile of r rows
-    # with r * G <= 128 (G = hq / hkv > 1) runs as hkv packed items instead of hq.
+    # Items from the last query tile to the first, one per head; the last tile runs as
+    # hq / hp items of hp heads each (hp from tile_heads).
     nqt = math.ceil(q_len / 128)
-    G = hq // hkv
-    r_last = q_len - 128 * (nqt - 1)
+    hp = tile_heads(q_len, hq // hkv)
     costs = []
     for qt in range(nqt - 1, -1, -1):
-        n = hkv if (qt == nqt - 1 and G > 1 and r_last * G <= 128) else hq
+        n = hq // hp if qt == nqt - 1 else hq
         costs += [item_tiles(q_len, q_start, causal, qt * 128, bs) + 1] * n
     return costs
 
@@ -155,21 +161,23 @@ def test_split_plan_balances_the_tail_chunk_and_short_chunks(lib):
     assert pieces and split * 3 <= whole
 
 
-@pytest.mark.parametrize("q_len,hq,hkv,packed", [
-    (21, 24, 4, True), (22, 24, 4, False), (1, 24, 4, True), (1685, 24, 4, True),
-    (1686, 24, 4, False), (64, 8, 4, True), (65, 8, 4, False), (8, 16, 1, True),
-    (9, 16, 1, False), (5, 4, 4, False), (128 + 32, 16, 4, True),
+@pytest.mark.parametrize("q_len,hq,hkv,hp", [
+    (21, 24, 4, 6), (22, 24, 4, 3), (42, 24, 4, 3), (43, 24, 4, 2), (64, 24, 4, 2),
+    (65, 24, 4, 1), (1, 24, 4, 6), (1685, 24, 4, 6), (1686, 24, 4, 3), (128 + 60, 24, 4, 2),
+    (64, 8, 4, 2), (65, 8, 4, 1), (8, 16, 1, 16), (9, 16, 1, 8), (33, 32, 4, 2),
+    (5, 4, 4, 1), (128 + 32, 16, 4, 4), (40, 24, 8, 3), (25, 20, 4, 5), (26, 20, 4, 1),
 ])
-def test_short_last_tile_runs_as_one_item_per_kv_head(lib, q_len, hq, hkv, packed):
-    # The last query tile's r rows of all G = hq / hkv heads of a KV head share one item
-    # when r * G <= 128: hkv items for that tile instead of hq.
+def test_short_last_tile_runs_as_items_of_several_heads(lib, q_len, hq, hkv, hp):
+    # The last query tile's r rows of hp heads of a KV head share one item, hp the largest
+    # divisor of G = hq / hkv with hp * r <= 128: hq / hp items for that tile instead of hq.
     import paged_kv_cache_09_gb300 as pa
+    assert tile_heads(q_len, hq // hkv) == hp
     cta, _ = pa.prefill_plan(q_len, 1000, True, hq, hkv, 832, 152)
     nqt = math.ceil(q_len / 128)
-    assert len(cta) == (nqt - 1) * hq + (hkv if packed else hq)
+    assert len(cta) == (nqt - 1) * hq + hq // hp
     assert len(cta) == len(item_costs(q_len, 1000, True, hq, 832, hkv))
     cta, pieces, _ = pa.prefill_plan_pieces(q_len, 1000, True, hq, hkv, 832, 152)
-    assert len(cta) == (nqt - 1) * hq + (hkv if packed else hq)
+    assert len(cta) == (nqt - 1) * hq + hq // hp
 
 
 def test_plan_refuses_a_group_that_does_not_divide(lib):
