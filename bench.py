@@ -68,7 +68,7 @@ L2_FLUSH_BYTES = 512 << 20
 # kernel changes after a capture.
 SPLIT_32K_DRAM_BYTES = 134_296_576 + 3_398_144
 # The same for one prefill launch of the q=4096 chunk over 4096 prior tokens.
-PREFILL_Q4096_DRAM_BYTES = 86_228_736 + 17_671_424
+PREFILL_Q4096_DRAM_BYTES = 86_582_528 + 18_139_904
 
 
 def parse():
